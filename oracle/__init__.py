@@ -1,0 +1,182 @@
+"""fp64 CPU oracle of the speculative-decoding verification pass.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s ``cpu_baseline`` / reference arm may import this package. The
+product library (``speculative_decoding_token_verify_gb300``) never imports it
+and shares no code with it.
+
+The arithmetic lives in ``spec_oracle.c`` (plain C, double precision, loops in
+ascending index order). This module only compiles it with gcc and marshals
+numpy arrays through ctypes. Logits are passed either as ``float32`` arrays or
+as ``uint16`` arrays holding raw bfloat16 bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB = os.path.join(_HERE, "libspec_oracle.so")
+
+F32, BF16 = 0, 1
+STOCHASTIC, GREEDY, FLY = 0, 1, 2
+
+FLAG_Q_ZERO = 1
+FLAG_Z_ZERO = 2
+FLAG_CDF_FALLBACK = 4
+FLAG_REST_ZERO = 8
+FLAG_BAD_ROW = 16
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile spec_oracle.c into a shared library next to it (gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    P = ctypes.c_void_p
+    i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.oracle_verify.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.c_int, P, i64, P, i64,
+                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, ctypes.c_int]
+    lib.oracle_verify.restype = ctypes.c_int
+    lib.oracle_confidence.argtypes = [i32, i32, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
+    lib.oracle_confidence.restype = ctypes.c_int
+    lib.oracle_estimator_update.argtypes = [i32, i32, P, P, P, dbl, P, P]
+    lib.oracle_estimator_update.restype = ctypes.c_int
+    lib.oracle_estimator_loss.argtypes = [i32, i32, P, P, P]
+    lib.oracle_estimator_loss.restype = dbl
+    lib.oracle_row_stats.argtypes = [i64, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
+    lib.oracle_row_stats.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(z):
+    z = np.ascontiguousarray(z)
+    if z.dtype == np.float32:
+        return z, F32
+    if z.dtype == np.uint16:
+        return z, BF16
+    raise TypeError(f"logits must be float32 or uint16 (raw bf16 bits), got {z.dtype}")
+
+
+def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_params=None,
+           nthreads=1):
+    """Verify B sequences. zt [B,K+1,V], zd [B,K,V] or None, x [B,K] int32,
+    u [B,K+1] float32 or None.
+
+    Returns a dict of numpy arrays: out_tokens [B,K+1] int32, accepted_len [B],
+    pos_stats [B,K+1,4] (lse_t, h_t, log_ratio, f), feature [B,K], conf [B,K]
+    (NaN without est_params), margin [B] (smallest decision margin), flags [B].
+    """
+    lib = _load()
+    zt, dt = _logits(zt)
+    B, K1, V = zt.shape
+    K = K1 - 1
+    if zd is not None:
+        zd, dd = _logits(zd)
+        assert dd == dt and zd.shape == (B, K, V)
+    x = np.ascontiguousarray(x, dtype=np.int32)
+    assert x.shape == (B, K)
+    if u is not None:
+        u = np.ascontiguousarray(u, dtype=np.float32)
+        assert u.shape == (B, K + 1)
+    est = None if est_params is None else np.ascontiguousarray(est_params, dtype=np.float64)
+    out = dict(
+        out_tokens=np.empty((B, K + 1), np.int32),
+        accepted_len=np.empty(B, np.int32),
+        pos_stats=np.empty((B, K + 1, 4), np.float64),
+        feature=np.full((B, K), np.nan),
+        conf=np.full((B, K), np.nan),
+        margin=np.empty(B, np.float64),
+        flags=np.empty(B, np.int32),
+    )
+    rc = lib.oracle_verify(B, K, V, dt, mode, _ptr(zt), V, _ptr(zd), V, _ptr(x), _ptr(u),
+                           float(fly_theta), int(fly_window), _ptr(est),
+                           _ptr(out["out_tokens"]), _ptr(out["accepted_len"]),
+                           _ptr(out["pos_stats"]), _ptr(out["conf"]) if est is not None else None,
+                           _ptr(out["feature"]) if zd is not None else None,
+                           _ptr(out["margin"]), _ptr(out["flags"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify rejected its arguments")
+    return out
+
+
+def confidence(zd, est_params=None, nthreads=1):
+    """feature [B,K] = logit(q_max) of each draft row; conf [B,K] if est_params."""
+    lib = _load()
+    zd, dt = _logits(zd)
+    B, K, V = zd.shape
+    est = None if est_params is None else np.ascontiguousarray(est_params, dtype=np.float64)
+    feat = np.empty((B, K), np.float64)
+    conf = np.full((B, K), np.nan)
+    flags = np.empty(B, np.int32)
+    rc = lib.oracle_confidence(B, K, V, dt, _ptr(zd), V, _ptr(est), _ptr(feat),
+                               _ptr(conf) if est is not None else None, _ptr(flags), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_confidence rejected its arguments")
+    return feat, conf, flags
+
+
+def estimator_update(feature, accepted_len, params, lr):
+    """One gradient step; returns (new_params [K+1], grad [K+1], counts [K+1])."""
+    lib = _load()
+    f = np.ascontiguousarray(feature, dtype=np.float64)
+    B, K = f.shape
+    n = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    p = np.array(params, dtype=np.float64, copy=True)
+    assert p.shape == (K + 1,)
+    g = np.empty(K + 1, np.float64)
+    c = np.empty(K + 1, np.int64)
+    rc = lib.oracle_estimator_update(B, K, _ptr(f), _ptr(n), _ptr(p), float(lr), _ptr(g), _ptr(c))
+    if rc != 0:
+        raise ValueError("oracle_estimator_update rejected its arguments")
+    return p, g, c
+
+
+def estimator_loss(feature, accepted_len, params):
+    lib = _load()
+    f = np.ascontiguousarray(feature, dtype=np.float64)
+    B, K = f.shape
+    n = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    p = np.ascontiguousarray(params, dtype=np.float64)
+    return lib.oracle_estimator_loss(B, K, _ptr(f), _ptr(n), _ptr(p))
+
+
+def row_stats(z, nthreads=1):
+    """Per-row (lse, normalised entropy, argmax, logit(q_max)) of z [..., V]."""
+    lib = _load()
+    z, dt = _logits(z)
+    V = z.shape[-1]
+    rows = int(np.prod(z.shape[:-1]))
+    lse = np.empty(rows, np.float64)
+    h = np.empty(rows, np.float64)
+    am = np.empty(rows, np.int32)
+    fq = np.empty(rows, np.float64)
+    rc = lib.oracle_row_stats(rows, V, dt, _ptr(z), V, _ptr(lse), _ptr(h), _ptr(am), _ptr(fq),
+                              int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_row_stats rejected its arguments")
+    shp = z.shape[:-1]
+    return lse.reshape(shp), h.reshape(shp), am.reshape(shp), fq.reshape(shp)

@@ -1,0 +1,492 @@
+/*
+ * spec_oracle.c -- plain, slow, fp64 CPU oracle of the speculative-decoding
+ * verification pass.
+ *
+ * TEST INFRASTRUCTURE. Only tests/, __graft_entry__.smoke() and bench.py's
+ * cpu_baseline / reference arm load this file's library. The CUDA library
+ * shares no code with it and never calls it.
+ *
+ * Every floating-point step is done in double precision from the exact input
+ * values (fp32, or bf16 widened by appending 16 zero bits). Every loop runs in
+ * ascending index order, with no blocking, fusion or reordering, so that each
+ * function reads against the passage it cites.
+ *
+ * Sources, cited by page title and section:
+ *  [SD]  "Speculative Decoding: как черновая модель ускоряет генерацию LLM без
+ *        потери качества", sections "Алгоритм на каждом шаге" (steps 1-4) and
+ *        "Математика верификации".
+ *  [AV]  "Verificación Adaptativa sin una cabeza de confianza", sections
+ *        "Solución: Estimador de aceptación ajustado en línea",
+ *        "Puntuar la Distribución", "Ajuste de los Coeficientes", footnote 1.
+ *  [FLy] "Training-Free Loosely Speculative Decoding: Accepting Semantically
+ *        Correct Drafts Beyond Exact Match", section 2.A ("Mecanismo de
+ *        Verificação de Dois Níveis"): 2.A.1 entropy gate, 2.A.2 deferral window.
+ *
+ * Readings where the pages are silent are listed beside the code that takes
+ * them; each is also recorded in the repository's design notes.
+ *
+ * Pins: every function here is pinned by tests/test_oracle_pins.py against
+ * closed forms, the worked example of [AV] footnote 1, brute force on tiny
+ * vocabularies and a Monte Carlo chi-square test of losslessness ([SD]).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_F32 0
+#define OR_BF16 1
+
+#define OR_STOCHASTIC 0
+#define OR_GREEDY 1
+#define OR_FLY 2
+
+/* degenerate-case bits written to flags[b] */
+#define OR_FLAG_Q_ZERO 1     /* q(x_i) == 0 at a tested position            */
+#define OR_FLAG_Z_ZERO 2     /* residual mass 0 after a reject: fell back to p */
+#define OR_FLAG_CDF_FALLBACK 4 /* no cumulative value exceeded u*Z           */
+#define OR_FLAG_REST_ZERO 8  /* q_max == 1 exactly: logit(q_max) clamped      */
+#define OR_FLAG_BAD_ROW 16   /* a row with no finite logit                    */
+
+/* logit(q_max) when the complement mass is exactly zero */
+#define OR_F_CLAMP 30.0
+
+static double logit_at(const void *row, int dtype, int64_t v) {
+    if (dtype == OR_F32) return (double)((const float *)row)[v];
+    uint32_t bits = ((uint32_t)((const uint16_t *)row)[v]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Softmax of one vocabulary row: p_v = exp(z_v - m) / sum_w exp(z_w - m),
+ * m = max_v z_v ([SD] "Математика верификации": p(x) and q(x) are the
+ * target's and the draft's next-token distributions). Writes p[0..V) and
+ * returns lse = m + log(sum). Returns 0 and sets *ok = 0 when no logit is
+ * finite. */
+static double softmax_row(const void *row, int dtype, int32_t V, double *p, int *ok) {
+    double m = -INFINITY;
+    for (int32_t v = 0; v < V; ++v) {
+        double z = logit_at(row, dtype, v);
+        if (z > m) m = z;
+    }
+    if (!(m > -INFINITY) || isinf(m)) {
+        *ok = 0;
+        for (int32_t v = 0; v < V; ++v) p[v] = 0.0;
+        return 0.0;
+    }
+    double s = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+        p[v] = exp(logit_at(row, dtype, v) - m);
+        s += p[v];
+    }
+    for (int32_t v = 0; v < V; ++v) p[v] /= s;
+    *ok = 1;
+    return m + log(s);
+}
+
+/* Index of the largest logit; ties go to the lowest index (reading: the pages
+ * do not say how ties break). */
+static int32_t argmax_row(const void *row, int dtype, int32_t V) {
+    int32_t best = 0;
+    double bz = logit_at(row, dtype, 0);
+    for (int32_t v = 1; v < V; ++v) {
+        double z = logit_at(row, dtype, v);
+        if (z > bz) { bz = z; best = v; }
+    }
+    return best;
+}
+
+/* Normalised entropy h = -sum_{p_v>0} p_v ln p_v / ln V ([FLy] 2.A.1: the
+ * gate reads the normalised entropy of the target's prediction; reading:
+ * natural logarithm divided by ln V, so a uniform row gives 1). */
+static double norm_entropy(const double *p, int32_t V) {
+    double h = 0.0;
+    for (int32_t v = 0; v < V; ++v)
+        if (p[v] > 0.0) h -= p[v] * log(p[v]);
+    return h / log((double)V);
+}
+
+/* logit(q_max) = ln q_max - ln(sum_{v != argmax} q_v) ([AV] "Puntuar la
+ * Distribución": the feature is the log-odds of the draft's most likely
+ * token). The complement is summed directly rather than formed as 1 - q_max. */
+static double logit_qmax(const double *q, int32_t V, int32_t amax, int *flags) {
+    double rest = 0.0;
+    for (int32_t v = 0; v < V; ++v)
+        if (v != amax) rest += q[v];
+    if (rest <= 0.0) {
+        *flags |= OR_FLAG_REST_ZERO;
+        return OR_F_CLAMP;
+    }
+    return log(q[amax]) - log(rest);
+}
+
+/* Inverse-CDF draw from the unnormalised weights r[0..V) with total Z: the
+ * smallest v whose running sum (ascending v) exceeds u*Z. Writes the distance
+ * of u to the nearer boundary of v's interval, in units of Z, to *margin. */
+static int32_t inverse_cdf(const double *r, int32_t V, double Z, double u,
+                           double *margin, int *flags) {
+    double target = u * Z;
+    double c = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+        double prev = c;
+        c += r[v];
+        if (c > target) {
+            double a = (target - prev) / Z, b = (c - target) / Z;
+            *margin = a < b ? a : b;
+            return v;
+        }
+    }
+    /* rounding left u*Z at or above the total: largest v with mass */
+    *flags |= OR_FLAG_CDF_FALLBACK;
+    *margin = 0.0;
+    for (int32_t v = V - 1; v >= 0; --v)
+        if (r[v] > 0.0) return v;
+    return V - 1;
+}
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+static double dmin(double a, double b) { return a < b ? a : b; }
+
+/* One sequence of the verification pass.
+ *  zt: K+1 target rows, row j at zt + j*t_stride elements.
+ *  zd: K draft rows (NULL allowed in greedy / FLy mode).
+ *  x:  K draft tokens.  u: K+1 uniforms (NULL allowed in greedy / FLy mode).
+ * Scratch: p, q, r of V doubles each. */
+static void verify_one(int32_t K, int32_t V, int dtype, int mode,
+                       const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
+                       const int32_t *x, const float *u, double fly_theta, int32_t fly_window,
+                       const double *est, int32_t *out_tokens, int32_t *acc_len,
+                       double *pos_stats, double *conf, double *feature,
+                       double *margin, int *flags, double *p, double *q, double *r) {
+    const size_t es = dtype == OR_F32 ? 4 : 2;
+    const char *tbase = (const char *)zt;
+    const char *dbase = (const char *)zd;
+    double mg = INFINITY;
+    int fl = 0;
+
+    /* Per-position statistics (written whether or not the position is reached). */
+    for (int32_t j = 0; j <= K; ++j) {
+        const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
+        int ok;
+        double lse_t = softmax_row(trow, dtype, V, p, &ok);
+        if (!ok) fl |= OR_FLAG_BAD_ROW;
+        double h = norm_entropy(p, V);
+        double lr = NAN, f = NAN;
+        if (j < K && zd) {
+            const void *drow = dbase + (size_t)j * (size_t)d_stride * es;
+            int okd;
+            double lse_d = softmax_row(drow, dtype, V, q, &okd);
+            if (!okd) fl |= OR_FLAG_BAD_ROW;
+            int32_t amax_d = argmax_row(drow, dtype, V);
+            f = logit_qmax(q, V, amax_d, &fl);
+            lr = (logit_at(trow, dtype, x[j]) - lse_t) - (logit_at(drow, dtype, x[j]) - lse_d);
+            if (feature) feature[j] = f;
+            /* [AV] "Puntuar la Distribución": confidence = sigmoid of the
+             * shared slope times logit(q_max) plus the position's intercept;
+             * params = [omega, beta_1 .. beta_K], draft position j uses
+             * beta_{j+1}. */
+            if (conf && est) conf[j] = sigmoid(est[0] * f + est[1 + j]);
+        }
+        if (pos_stats) {
+            pos_stats[4 * j + 0] = lse_t;
+            pos_stats[4 * j + 1] = h;
+            pos_stats[4 * j + 2] = lr;
+            pos_stats[4 * j + 3] = f;
+        }
+    }
+
+    int32_t n = 0, token = -1;
+    if (mode == OR_STOCHASTIC) {
+        /* [SD] "Математика верификации": accept x_i with probability 1 when
+         * p(x_i) >= q(x_i), else with probability p(x_i)/q(x_i); i.e. accept
+         * iff u_i < min(1, p(x_i)/q(x_i)). [SD] step 4: stop at the first
+         * rejection and draw the correction from norm(max(0, p - q)). */
+        int rejected = 0;
+        for (int32_t i = 0; i < K; ++i) {
+            const void *trow = tbase + (size_t)i * (size_t)t_stride * es;
+            const void *drow = dbase + (size_t)i * (size_t)d_stride * es;
+            int ok;
+            softmax_row(trow, dtype, V, p, &ok);
+            softmax_row(drow, dtype, V, q, &ok);
+            double px = p[x[i]], qx = q[x[i]];
+            double acc;
+            if (qx > 0.0) {
+                acc = dmin(1.0, px / qx);
+            } else {
+                /* q(x) = 0: the ratio is +inf if p(x) > 0, else the draft is
+                 * rejected (reading; the pages assume x ~ q). */
+                fl |= OR_FLAG_Q_ZERO;
+                acc = px > 0.0 ? 1.0 : 0.0;
+            }
+            mg = dmin(mg, fabs((double)u[i] - acc));
+            if ((double)u[i] < acc) { ++n; continue; }
+            double Z = 0.0;
+            for (int32_t v = 0; v < V; ++v) {
+                r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
+                Z += r[v];
+            }
+            if (!(Z > 0.0)) {
+                /* only reachable through rounding: draw from p itself */
+                fl |= OR_FLAG_Z_ZERO;
+                Z = 0.0;
+                for (int32_t v = 0; v < V; ++v) { r[v] = p[v]; Z += r[v]; }
+            }
+            double cm;
+            token = inverse_cdf(r, V, Z, (double)u[K], &cm, &fl);
+            mg = dmin(mg, cm);
+            rejected = 1;
+            break;
+        }
+        if (!rejected) {
+            /* Bonus token after K acceptances (reading: a draw from the target's
+             * row K, standard for rejection-sampling verification). */
+            const void *trow = tbase + (size_t)K * (size_t)t_stride * es;
+            int ok;
+            softmax_row(trow, dtype, V, p, &ok);
+            double Z = 0.0;
+            for (int32_t v = 0; v < V; ++v) Z += p[v];
+            double cm;
+            token = inverse_cdf(p, V, Z, (double)u[K], &cm, &fl);
+            mg = dmin(mg, cm);
+        }
+    } else if (mode == OR_GREEDY) {
+        /* Exact match: accept x_i iff it is the target's top prediction
+         * ([FLy] section 1; [SD] "Проверка результата", greedy output is
+         * reproducible). The correction is the target's argmax at the stop. */
+        n = K;
+        for (int32_t i = 0; i < K; ++i) {
+            const void *trow = tbase + (size_t)i * (size_t)t_stride * es;
+            int32_t a = argmax_row(trow, dtype, V);
+            if (x[i] != a) { n = i; token = a; break; }
+        }
+        if (n == K) token = argmax_row(tbase + (size_t)K * (size_t)t_stride * es, dtype, V);
+    } else {
+        /* [FLy] 2.A: a deviation at j (x_j differs from the target's argmax)
+         * is rejected at once when the target's normalised entropy h_j < theta;
+         * when h_j >= theta it is deferred: accepted if none of the next W draft
+         * positions deviates, rejected retroactively if one does, and rejected
+         * conservatively if the window does not fit inside the draft. */
+        n = K;
+        for (int32_t j = 0; j < K; ++j) {
+            const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
+            int32_t a = argmax_row(trow, dtype, V);
+            if (x[j] == a) continue;               /* no deviation: accept j */
+            int ok;
+            softmax_row(trow, dtype, V, p, &ok);
+            double h = norm_entropy(p, V);
+            mg = dmin(mg, fabs(h - fly_theta));
+            int reject;
+            if (h < fly_theta) {
+                reject = 1;                        /* confident target */
+            } else if (j + fly_window > K - 1) {
+                reject = 1;                        /* window past the draft end */
+            } else {
+                reject = 0;
+                for (int32_t k = j + 1; k <= j + fly_window; ++k) {
+                    const void *krow = tbase + (size_t)k * (size_t)t_stride * es;
+                    if (x[k] != argmax_row(krow, dtype, V)) { reject = 1; break; }
+                }
+            }
+            if (reject) { n = j; token = a; break; }
+        }
+        if (n == K) token = argmax_row(tbase + (size_t)K * (size_t)t_stride * es, dtype, V);
+    }
+
+    /* Writeback ([SD] step 4): the accepted prefix, then the correction or
+     * bonus token; unused slots are -1. */
+    for (int32_t j = 0; j <= K; ++j) out_tokens[j] = -1;
+    for (int32_t j = 0; j < n; ++j) out_tokens[j] = x[j];
+    out_tokens[n] = token;
+    *acc_len = n;
+    if (margin) *margin = mg;
+    if (flags) *flags = fl;
+}
+
+/* Full verification over B sequences. Layouts (row-major, elements):
+ *  zt [B][K+1][t_stride] (first V used), zd [B][K][d_stride], x [B][K],
+ *  u [B][K+1], out_tokens [B][K+1], accepted_len [B],
+ *  pos_stats [B][K+1][4] = (lse_t, h_t, log_ratio, f) or NULL,
+ *  est [K+1] or NULL, conf [B][K] or NULL, feature [B][K] or NULL,
+ *  margin [B] or NULL (smallest decision margin of the sequence),
+ *  flags [B] or NULL (OR_FLAG_* bits).
+ * nthreads > 0 sets the OpenMP thread count. Returns 0, or -1 on bad args. */
+int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
+                  const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
+                  const int32_t *x, const float *u, double fly_theta, int32_t fly_window,
+                  const double *est, int32_t *out_tokens, int32_t *accepted_len,
+                  double *pos_stats, double *conf, double *feature,
+                  double *margin, int32_t *flags, int nthreads) {
+    if (B < 0 || K < 1 || V < 2 || !zt || !x || !out_tokens || !accepted_len) return -1;
+    if (mode == OR_STOCHASTIC && (!zd || !u)) return -1;
+    if (t_stride <= 0) t_stride = V;
+    if (d_stride <= 0) d_stride = V;
+    const size_t es = dtype == OR_F32 ? 4 : 2;
+    int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : 1)
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!p || !q || !r) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int32_t b = 0; b < B; ++b) {
+                int fl = 0;
+                verify_one(K, V, dtype, mode,
+                           (const char *)zt + (size_t)b * (size_t)(K + 1) * (size_t)t_stride * es, t_stride,
+                           zd ? (const char *)zd + (size_t)b * (size_t)K * (size_t)d_stride * es : NULL, d_stride,
+                           x + (size_t)b * K, u ? u + (size_t)b * (K + 1) : NULL, fly_theta, fly_window,
+                           est, out_tokens + (size_t)b * (K + 1), accepted_len + b,
+                           pos_stats ? pos_stats + (size_t)b * (K + 1) * 4 : NULL,
+                           conf ? conf + (size_t)b * K : NULL,
+                           feature ? feature + (size_t)b * K : NULL,
+                           margin ? margin + b : NULL, &fl, p, q, r);
+                if (flags) flags[b] = fl;
+            }
+        }
+        free(p);
+        free(q);
+        free(r);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Confidence features of draft rows only: feature[b][i] = logit(q_max) of
+ * draft row (b, i) and conf[b][i] = sigmoid(omega * feature + beta_{i+1})
+ * ([AV] "Puntuar la Distribución"). conf may be NULL; est is needed for conf. */
+int oracle_confidence(int32_t B, int32_t K, int32_t V, int dtype, const void *zd, int64_t d_stride,
+                      const double *est, double *feature, double *conf, int32_t *flags,
+                      int nthreads) {
+    if (B < 0 || K < 1 || V < 2 || !zd || !feature) return -1;
+    if (conf && !est) return -1;
+    if (d_stride <= 0) d_stride = V;
+    const size_t es = dtype == OR_F32 ? 4 : 2;
+    int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : 1)
+    {
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!q) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int32_t b = 0; b < B; ++b) {
+                int fl = 0;
+                for (int32_t i = 0; i < K; ++i) {
+                    const void *drow = (const char *)zd + ((size_t)b * K + i) * (size_t)d_stride * es;
+                    int ok;
+                    softmax_row(drow, dtype, V, q, &ok);
+                    if (!ok) fl |= OR_FLAG_BAD_ROW;
+                    double f = logit_qmax(q, V, argmax_row(drow, dtype, V), &fl);
+                    feature[(size_t)b * K + i] = f;
+                    if (conf) conf[(size_t)b * K + i] = sigmoid(est[0] * f + est[1 + i]);
+                }
+                if (flags) flags[b] = fl;
+            }
+        }
+        free(q);
+    }
+    return bad ? -1 : 0;
+}
+
+/* One online update of the acceptance estimator ([AV] "Ajuste de los
+ * Coeficientes").
+ * Labels: only drafts up to and including the first rejection are eligible;
+ * y_i = 1 for i < n_acc, y_{n_acc} = 0 when n_acc < K, later positions carry
+ * no label.
+ * Step (reading: the pages solve an IRLS Newton system over N steps; this
+ * entry point takes one plain gradient step of size lr on the mean log-loss
+ * over the batch's eligible labels):
+ *   z = omega * f_i + beta_{i+1},  e = sigmoid(z) - y,
+ *   g_omega = (1/N) sum e * f_i,   g_beta_k = (1/N) sum_{i = k-1} e,
+ *   params -= lr * g.
+ * N = 0 leaves params unchanged. grad_out [K+1] and count_out [K+1]
+ * (count_out[0] = N, count_out[k] = labels at draft position k-1) may be NULL.
+ * The loss is accumulated in ascending (b, i) order. */
+int oracle_estimator_update(int32_t B, int32_t K, const double *feature, const int32_t *accepted_len,
+                            double *params, double lr, double *grad_out, int64_t *count_out) {
+    if (B < 0 || K < 1 || !feature || !accepted_len || !params) return -1;
+    double *g = (double *)calloc((size_t)K + 1, sizeof(double));
+    int64_t *cnt = (int64_t *)calloc((size_t)K + 1, sizeof(int64_t));
+    if (!g || !cnt) { free(g); free(cnt); return -1; }
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t n = accepted_len[b];
+        if (n < 0 || n > K) { free(g); free(cnt); return -1; }
+        int32_t last = n < K ? n : K - 1;    /* last eligible position */
+        for (int32_t i = 0; i <= last; ++i) {
+            double y = i < n ? 1.0 : 0.0;
+            double f = feature[(size_t)b * K + i];
+            double e = sigmoid(params[0] * f + params[1 + i]) - y;
+            g[0] += e * f;
+            g[1 + i] += e;
+            cnt[0] += 1;
+            cnt[1 + i] += 1;
+        }
+    }
+    int64_t N = cnt[0];
+    for (int32_t k = 0; k <= K; ++k) {
+        double gk = N > 0 ? g[k] / (double)N : 0.0;
+        if (grad_out) grad_out[k] = gk;
+        if (count_out) count_out[k] = cnt[k];
+    }
+    if (N > 0)
+        for (int32_t k = 0; k <= K; ++k) params[k] -= lr * (g[k] / (double)N);
+    free(g);
+    free(cnt);
+    return 0;
+}
+
+/* Mean log-loss of the same eligible labels, for finite-difference checks of
+ * the update ([AV] "Otras Características Consideradas": log-loss is the mean
+ * negative log-likelihood of the predicted acceptance probability). */
+double oracle_estimator_loss(int32_t B, int32_t K, const double *feature, const int32_t *accepted_len,
+                             const double *params) {
+    double L = 0.0;
+    int64_t N = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t n = accepted_len[b];
+        int32_t last = n < K ? n : K - 1;
+        for (int32_t i = 0; i <= last; ++i) {
+            double s = sigmoid(params[0] * feature[(size_t)b * K + i] + params[1 + i]);
+            L += i < n ? -log(s) : -log(1.0 - s);
+            ++N;
+        }
+    }
+    return N > 0 ? L / (double)N : 0.0;
+}
+
+/* Row statistics of `rows` rows of V logits each (row r at z + r*stride):
+ * lse, normalised entropy, argmax, logit(q_max). Any output may be NULL. */
+int oracle_row_stats(int64_t rows, int32_t V, int dtype, const void *z, int64_t stride,
+                     double *lse, double *entropy, int32_t *argmax, double *fq, int nthreads) {
+    if (rows < 0 || V < 2 || !z) return -1;
+    if (stride <= 0) stride = V;
+    const size_t es = dtype == OR_F32 ? 4 : 2;
+    int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : 1)
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!p) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t r = 0; r < rows; ++r) {
+                const void *row = (const char *)z + (size_t)r * (size_t)stride * es;
+                int ok, fl = 0;
+                double l = softmax_row(row, dtype, V, p, &ok);
+                int32_t a = argmax_row(row, dtype, V);
+                if (lse) lse[r] = ok ? l : NAN;
+                if (entropy) entropy[r] = ok ? norm_entropy(p, V) : NAN;
+                if (argmax) argmax[r] = a;
+                if (fq) fq[r] = ok ? logit_qmax(p, V, a, &fl) : NAN;
+            }
+        }
+        free(p);
+    }
+    return bad ? -1 : 0;
+}
