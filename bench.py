@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Benchmark of the verification pass: verified draft positions per second.
+
+One step = one full pass of the hot path over one batch resident in HBM:
+spec_verify (stochastic rule, residual/bonus draw, logit(q_max) features and
+estimator confidences) followed by spec_estimator_update (one online step of
+the acceptance estimator) -- the large-batch estimator workload,
+B=256 sequences, K=8 draft positions, V=128256, bf16 logits, unless
+--workload says otherwise.
+
+Prints one JSON line (rank 0). With --impl reference the fp64 CPU oracle is
+timed instead, on the host cores, each step a bounded sample of the workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  torchrun --nproc-per-node N bench.py --gpus N ...   (N independent replicas)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s vs ~8 TB/s peak (1 GB300)"
+UNIT = "positions/s"
+KERNEL_SOURCES = ("speculative_decoding_token_verify_gb300/csrc/spec_verify.cu",
+                  "speculative_decoding_token_verify_gb300/csrc/spec_device.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_kernel_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="estimator_B256_K8_V128256_bf16")
+    ap.add_argument("--B", type=int, default=0, help="override the workload's batch size")
+    ap.add_argument("--seed", type=int, default=1003)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def get_workload(args):
+    import workloads
+
+    if args.workload in workloads.WORKLOADS:
+        w = workloads.WORKLOADS[args.workload]
+    else:
+        sweep = {w.name: w for w in workloads.sweep()}
+        if args.workload not in sweep:
+            raise SystemExit(f"unknown workload {args.workload}")
+        w = sweep[args.workload]
+    if args.B:
+        w = w.scaled(B=args.B, name=f"{w.name}@B{args.B}")
+    return w
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, v: float, device=None) -> float:
+    if pg is None:
+        return v
+    import torch
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled=True):
+        self.proc = None
+        self.gpu = gpu_index
+        self.enabled = enabled
+
+    def start(self):
+        if not self.enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                 reasons=dict(hw_slowdown=f[5], hw_thermal_slowdown=f[6],
+                                              sw_thermal_slowdown=f[7], sw_power_cap=f[8])))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 0.5 * max(r["power"] for r in rows)] or rows
+        reasons = sorted({k for r in load for k, v in r["reasons"].items() if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_inputs(w, n_seq, seed):
+    """A bounded sample: the first n_seq sequences of the workload, drawn on
+    the CPU with the workload's recipe."""
+    import workloads
+
+    sub = w.scaled(B=n_seq)
+    inp = workloads.make_inputs(sub, seed, "cpu")
+    return dict(zt=workloads.to_numpy_logits(inp["zt"]), zd=workloads.to_numpy_logits(inp["zd"]),
+                x=inp["x"].numpy(), u=inp["u"].numpy())
+
+
+def oracle_step(w, s, nthreads):
+    import numpy as np
+
+    import oracle
+
+    mode = {"stochastic": oracle.STOCHASTIC, "greedy": oracle.GREEDY, "fly": oracle.FLY}[w.mode]
+    est = np.r_[1.0, np.zeros(w.K)] if w.with_confidence else None
+    zd = s["zd"] if (w.mode == "stochastic" or w.with_confidence) else None
+    r = oracle.verify(s["zt"], zd, s["x"], s["u"] if w.mode == "stochastic" else None, mode=mode,
+                      fly_theta=w.fly_theta, fly_window=w.fly_window, est_params=est,
+                      nthreads=nthreads)
+    if w.with_confidence:
+        oracle.estimator_update(r["feature"], r["accepted_len"], est, w.estimator_lr)
+    return r
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, seed, target_s=1.0):
+    """Time the oracle as it stands on all host cores over a bounded sample
+    (about target_s seconds of wall time, i.e. cores * target_s of CPU work)."""
+    import oracle
+
+    oracle.build()
+    cores = host_cores()
+    probe = oracle_sample_inputs(w, 1, seed)
+    t0 = time.perf_counter()
+    oracle_step(w, probe, 1)
+    t_seq = time.perf_counter() - t0
+    n_seq = max(cores, int(round(target_s / max(t_seq, 1e-6))) * cores)
+    n_seq = min(n_seq, w.B, 16 * cores)
+    s = oracle_sample_inputs(w, n_seq, seed)
+    t0 = time.perf_counter()
+    oracle_step(w, s, cores)
+    dt = time.perf_counter() - t0
+    return {"value": n_seq * w.K / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n_seq} of {w.B} sequences of {w.name} (fp64 C oracle, OpenMP over "
+                      f"sequences, {cores} threads, {dt:.2f} s wall)"}
+
+
+def run_reference(args, w, world, rank, pg):
+    import oracle
+
+    if rank != 0:
+        return 0
+    oracle.build()
+    cores = host_cores()
+    n_seq = min(w.B, cores)
+    s = oracle_sample_inputs(w, n_seq, args.seed)
+    for _ in range(args.warmup):
+        oracle_step(w, s, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, s, cores)
+    dt = time.perf_counter() - t0
+    value = args.steps * n_seq * w.K / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
+                   "mode": w.mode, "step_sample_sequences": n_seq},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: first {n_seq} of {w.B} sequences of {w.name}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    try:
+        kv = dict(line.strip().split("=", 1) for line in open(TRAFFIC_FILE) if "=" in line)
+    except OSError:
+        return None
+    if kv.get("source_sha256") != source_hash():
+        return None
+    if kv.get("workload") != workload_name:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_hbm_peak():
+    try:
+        mp = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(mp["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def run_ours(args, w, world, rank, local, pg):
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+    import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    inp = workloads.make_inputs(w, args.seed + 7919 * rank, dev)
+    with_draft = w.mode == "stochastic" or w.with_confidence
+    zd = inp["zd"] if with_draft else None
+    u = inp["u"] if w.mode == "stochastic" else None
+    est0 = torch.tensor([1.0] + [0.0] * w.K, dtype=torch.float32, device=dev)
+    est = est0.clone()
+    ws = sv.Workspace(dev)
+    out = {"out_tokens": torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev),
+           "accepted_len": torch.empty((w.B,), dtype=torch.int32, device=dev)}
+    if w.with_confidence:
+        out["feature"] = torch.empty((w.B, w.K), dtype=torch.float32, device=dev)
+        out["conf"] = torch.empty((w.B, w.K), dtype=torch.float32, device=dev)
+
+    def step(zt_, zd_, x_, u_):
+        sv.verify(zt_, zd_, x_, u_, mode=w.mode, fly_theta=w.fly_theta, fly_window=w.fly_window,
+                  est_params=est if w.with_confidence else None, out=out, workspace=ws,
+                  want_feature=w.with_confidence, want_conf=w.with_confidence)
+        if w.with_confidence:
+            sv.estimator_update(out["feature"], out["accepted_len"], est, w.estimator_lr)
+
+    launches_per_step = 2 if w.with_confidence else 1
+    for _ in range(args.warmup):
+        step(inp["zt"], zd, inp["x"], u)
+    torch.cuda.synchronize(dev)
+
+    logit_bytes = w.logit_bytes(with_draft)
+    l2_note = ("inputs larger than L2 (%.2f GB of logits per step, L2 129 MB)" % (logit_bytes / 1e9)
+               if logit_bytes > 2 * 129e6 else "L2 flushed between steps")
+    flush = None
+    if logit_bytes <= 2 * 129e6:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    clocks = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
+    clocks.start()
+    ev_v = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(pg, dev)
+    torch.cuda.synchronize(dev)
+    if flush is None:
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev_v[i][0].record(stream)
+            step(inp["zt"], zd, inp["x"], u)
+            ev_v[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = t_start.elapsed_time(t_end)
+    else:
+        total_ms = 0.0
+        for i in range(args.steps):
+            flush.add_(1)
+            ev_v[i][0].record(stream)
+            step(inp["zt"], zd, inp["x"], u)
+            ev_v[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = sum(a.elapsed_time(b) for a, b in ev_v)
+    barrier(pg, dev)
+    step_ms = [a.elapsed_time(b) for a, b in ev_v]
+    total_ms = max_over_ranks(pg, total_ms, dev)
+
+    # the dominant kernel alone: spec_verify's launches, same stream, same region
+    verify_ms = []
+    if w.with_confidence:
+        ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(min(args.steps, 200))]
+        for a, b in ev_k:
+            a.record(stream)
+            sv.verify(inp["zt"], zd, inp["x"], u, mode=w.mode, est_params=est, out=out, workspace=ws,
+                      want_feature=True, want_conf=True)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        verify_ms = [a.elapsed_time(b) for a, b in ev_k]
+    else:
+        verify_ms = step_ms
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg)
+    clk = clocks.stop()
+
+    n_pos = world * args.steps * w.B * w.K
+    value = n_pos / (total_ms / 1e3)
+    kern_s = statistics.mean(verify_ms) / 1e3
+    peak, peak_src = measured_hbm_peak()
+    achieved = logit_bytes / kern_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
+                   "mode": w.mode + ("+confidence+estimator_update" if w.with_confidence else ""),
+                   "l2": l2_note, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm_gbs": logit_bytes * world * args.steps / (total_ms / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "kernel": "verify_kernel<bf16>" if w.dtype == "bf16" else "verify_kernel<f32>",
+                     "algorithmic_bytes_per_launch": logit_bytes,
+                     "kernel_ms_mean": kern_s * 1e3, "kernel_ms_median": statistics.median(verify_ms),
+                     "peak_source": peak_src, "frac_note": "of measured" if "measured" in peak_src
+                     else "of fallback"},
+        "gpu_launches": args.steps * launches_per_step,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.seed)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):
+    """Same metric through the public API with HOST inputs: every step copies
+    its inputs from pinned host memory and reads its results back."""
+    import torch
+
+    h_zt = inp["zt"].cpu().pin_memory()
+    h_zd = zd.cpu().pin_memory() if zd is not None else None
+    h_x = inp["x"].cpu().pin_memory()
+    h_u = u.cpu().pin_memory() if u is not None else None
+    d_zt = torch.empty_like(inp["zt"])
+    d_zd = torch.empty_like(zd) if zd is not None else None
+    d_x = torch.empty_like(inp["x"])
+    d_u = torch.empty_like(u) if u is not None else None
+    res = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in (h_zt, h_zd, h_x, h_u) if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in res.values())
+    steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        d_zt.copy_(h_zt, non_blocking=True)
+        if d_zd is not None:
+            d_zd.copy_(h_zd, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        if d_u is not None:
+            d_u.copy_(h_u, non_blocking=True)
+        step(d_zt, d_zd, d_x, d_u)
+        for k, t in res.items():
+            t.copy_(out[k], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    barrier(pg, dev)
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(pg, a.elapsed_time(b), dev)
+    world = pg.get_world_size() if pg is not None else 1
+    return {"value": world * steps * w.B * w.K / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+
+
+def main():
+    args = parse_args()
+    w = get_workload(args)
+    world, rank, local, pg = dist_setup(args)
+    if world != args.gpus and rank == 0:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, world, rank, pg)
+        return run_ours(args, w, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,196 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification library (libspecverify.so).
+ *
+ * One call verifies, for every sequence b of a batch, the K draft tokens
+ * proposed by a draft model against the target model's logits, writes the
+ * accepted prefix plus one correction (or bonus) token, and optionally the
+ * per-position statistics, the logit(q_max) confidence features and the
+ * online estimator's confidences.
+ *
+ * Sources (page title, section):
+ *  [SD]  "Speculative Decoding: как черновая модель ускоряет генерацию LLM без
+ *        потери качества" -- "Алгоритм на каждом шаге" (draft K tokens, one
+ *        target pass, verify, append the accepted tokens plus one corrected
+ *        token) and "Математика верификации" (accept x_i with probability
+ *        min(1, p(x_i)/q(x_i)); on rejection draw from norm(max(0, p - q))).
+ *  [AV]  "Verificación Adaptativa sin una cabeza de confianza" -- "Puntuar la
+ *        Distribución" (confidence = sigmoid(omega * logit(q_max) + beta_i),
+ *        K+1 parameters) and "Ajuste de los Coeficientes" (labels up to and
+ *        including the first rejection).
+ *  [FLy] "Training-Free Loosely Speculative Decoding: Accepting Semantically
+ *        Correct Drafts Beyond Exact Match" -- 2.A.1 entropy gate, 2.A.2
+ *        deferral window.
+ *
+ * Conventions shared by every call:
+ *  - Pointers named *_logits, draft_tokens, uniforms, out_*, feature, conf,
+ *    est_params, grad_out, count_out and workspace are DEVICE pointers owned
+ *    by the caller (allocated e.g. through PyTorch). The library never
+ *    allocates device memory and never frees what it is given.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = legacy default stream). They return after enqueueing. Host-side
+ *    argument errors are reported before anything is enqueued.
+ *  - Return value: SPEC_OK, or an error code below. The thread-local message
+ *    of the last failure is available through spec_last_error().
+ *  - Logits are row-major: target row (b, j) starts at element
+ *    (b*(K+1) + j) * t_row_stride, draft row (b, i) at (b*K + i) * d_row_stride.
+ *    Strides are in elements and >= V (0 means V). Every row must start on an
+ *    element boundary (4-byte for fp32, 2-byte for bf16); rows starting on a
+ *    16-byte boundary take the fastest path.
+ *  - Logits must be finite or -inf (masked). A row whose logits are all -inf
+ *    raises SPEC_ERR_BAD_ROW in the device status word (see
+ *    spec_get_device_status); its outputs are then unspecified. A draft token
+ *    outside [0, V) is never dereferenced: it counts as rejected and raises
+ *    SPEC_ERR_BAD_TOKEN in the status word.
+ *  - Outputs are deterministic: the same inputs give the same bits on every
+ *    run (fixed reduction orders, no floating-point atomics).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG 1   /* host-validated: nothing was enqueued   */
+#define SPEC_ERR_UNSUPPORTED 2   /* shape/dtype outside the supported range */
+#define SPEC_ERR_CUDA 3          /* a CUDA runtime call or launch failed    */
+#define SPEC_ERR_TIMEOUT 4       /* device status: a bounded wait gave up   */
+#define SPEC_ERR_BAD_ROW 5       /* device status: a row had no finite logit */
+#define SPEC_ERR_BAD_TOKEN 6     /* device status: a draft token was outside [0,V) */
+
+/* limits */
+#define SPEC_MAX_K 31            /* draft positions per sequence            */
+#define SPEC_MAX_V (1 << 20)     /* vocabulary size                         */
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+typedef enum {
+    SPEC_STOCHASTIC = 0, /* [SD] lossless rejection rule + residual/bonus draw */
+    SPEC_GREEDY = 1,     /* exact match with the target's argmax               */
+    SPEC_FLY = 2         /* [FLy] entropy-gated deferral of greedy mismatches   */
+} spec_mode;
+
+typedef struct {
+    int32_t B;            /* sequences, >= 1                                  */
+    int32_t K;            /* draft positions, 1 .. SPEC_MAX_K                 */
+    int32_t V;            /* vocabulary size, 2 .. SPEC_MAX_V                 */
+    int32_t dtype;        /* spec_dtype of both logit tensors                 */
+    int32_t mode;         /* spec_mode                                        */
+    int32_t fly_window;   /* FLy: W >= 1, window of draft positions j+1..j+W  */
+    float fly_theta;      /* FLy: gate threshold on normalised entropy        */
+    int32_t reserved;     /* must be 0                                        */
+    int64_t t_row_stride; /* elements between target rows; 0 => V             */
+    int64_t d_row_stride; /* elements between draft rows; 0 => V              */
+} spec_verify_params;
+
+/*
+ * Bytes of device workspace spec_verify needs for these parameters (16-byte
+ * aligned allocation required). Returns 0 if the parameters are invalid.
+ */
+size_t spec_workspace_size(const spec_verify_params *params);
+
+/*
+ * spec_verify -- one verification pass over B sequences ([SD] steps 3-4).
+ *
+ * Inputs (device):
+ *   target_logits [B][K+1][V]  rows 0..K-1 score the K draft tokens; row K is
+ *                              the target's next-token row after all K drafts.
+ *   draft_logits  [B][K][V]    the draft's rows. Required in SPEC_STOCHASTIC;
+ *                              optional otherwise (NULL: no feature/conf/ratio).
+ *   draft_tokens  [B][K] int32 x_i in [0, V).
+ *   uniforms      [B][K+1] f32 in [0,1): u[b][i] (i < K) tests position i,
+ *                              u[b][K] drives the single residual or bonus
+ *                              inverse-CDF draw. Required in SPEC_STOCHASTIC,
+ *                              ignored otherwise (may be NULL).
+ *   est_params    [K+1] f32    (omega, beta_1..beta_K) or NULL.
+ * Outputs (device):
+ *   out_tokens    [B][K+1] int32  x_0..x_{n-1}, then the correction token at n,
+ *                                 then -1.
+ *   accepted_len  [B] int32       n in [0, K].
+ *   pos_stats     [B][K+1][4] f32 or NULL: (lse of target row j, normalised
+ *                                 entropy of target row j, log p(x_j) - log q(x_j),
+ *                                 logit(q_max) of draft row j); the last two are
+ *                                 NaN at j = K and without draft logits.
+ *   feature       [B][K] f32 or NULL: logit(q_max) of every draft row.
+ *   conf          [B][K] f32 or NULL: sigmoid(omega*feature + beta_{i+1});
+ *                                 needs est_params and draft_logits.
+ * Rules:
+ *   SPEC_STOCHASTIC: accept x_i iff u[b][i] < min(1, p_i(x_i)/q_i(x_i)); stop
+ *     at the first rejection i and draw the correction from
+ *     norm(max(0, p_i - q_i)) by inverse CDF with u[b][K] (smallest v whose
+ *     running sum in ascending v exceeds u*Z); after K acceptances draw the
+ *     bonus token from p_K the same way.
+ *   SPEC_GREEDY: accept x_i iff x_i == argmax p_i (ties: lowest index); the
+ *     correction (or bonus) is the argmax of the stop row.
+ *   SPEC_FLY: a mismatch at j is rejected if h_j < fly_theta; otherwise it is
+ *     accepted iff positions j+1..j+W all exist (j+W <= K-1) and all match.
+ * Workspace: `workspace_bytes` >= spec_workspace_size(params); its content on
+ *   entry is ignored, and it must not be shared by calls that can overlap.
+ * Errors: SPEC_ERR_INVALID_ARG / SPEC_ERR_UNSUPPORTED before any launch;
+ *   SPEC_ERR_CUDA if a launch fails. Device-side conditions (bad rows) land in
+ *   the workspace status word.
+ */
+int spec_verify(const spec_verify_params *params, const void *target_logits,
+                const void *draft_logits, const int32_t *draft_tokens, const float *uniforms,
+                int32_t *out_tokens, int32_t *accepted_len, float *pos_stats,
+                const float *est_params, float *feature, float *conf,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes spec_confidence needs; 0 if the arguments are invalid. */
+size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype);
+
+/*
+ * spec_confidence -- draft-only pass ([AV] "Puntuar la Distribución"): for
+ * every draft row (b, i), feature[b][i] = logit(q_max) = ln q_max - ln(1 - q_max)
+ * and, if est_params and conf are given, conf[b][i] =
+ * sigmoid(omega * feature + beta_{i+1}). Reads B*K*V logits once.
+ * draft_logits [B][K][V] (row stride d_row_stride, 0 => V); feature [B][K]
+ * required; est_params [K+1] and conf [B][K] optional (both or neither).
+ */
+int spec_confidence(int32_t B, int32_t K, int32_t V, int32_t dtype, const void *draft_logits,
+                    int64_t d_row_stride, const float *est_params, float *feature, float *conf,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_estimator_update -- one online step of the acceptance estimator
+ * ([AV] "Ajuste de los Coeficientes"). Labels: y_i = 1 for i < n_acc,
+ * y_{n_acc} = 0 when n_acc < K; later positions carry no label. With
+ * z = omega*f + beta_{i+1} and e = sigmoid(z) - y over the N eligible labels:
+ *   g_omega = (1/N) sum e*f,  g_beta_k = (1/N) sum_{i = k-1} e,
+ *   est_params -= lr * g       (no change when N = 0).
+ * (The page refits by IRLS every N decoding steps; this call is one plain
+ * gradient step of the mean log-loss.)
+ * feature [B][K] f32, accepted_len [B] int32 in [0,K], est_params [K+1] f32
+ * in/out; grad_out [K+1] f32 and count_out [K+1] int32 (N, then labels per
+ * position) are optional. One CTA, fixed summation order: deterministic.
+ * 1 <= K <= 1024; B >= 0.
+ */
+int spec_estimator_update(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                          float *est_params, float lr, float *grad_out, int32_t *count_out,
+                          void *stream);
+
+/*
+ * Synchronously read the device status word of a workspace last used by
+ * spec_verify or spec_confidence (waits for the device). *status_out gets
+ * SPEC_OK or the largest device-side code raised (SPEC_ERR_TIMEOUT,
+ * SPEC_ERR_BAD_ROW, SPEC_ERR_BAD_TOKEN). For tests and debugging.
+ */
+int spec_get_device_status(const void *workspace, int32_t *status_out);
+
+/* Message of the calling thread's last failure ("" if none). */
+const char *spec_last_error(void);
+
+/* Library version string. */
+const char *spec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */
