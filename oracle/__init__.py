@@ -54,7 +54,7 @@ def _load():
     P = ctypes.c_void_p
     i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
     lib.oracle_verify.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.c_int, P, i64, P, i64,
-                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, ctypes.c_int]
+                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_confidence.argtypes = [i32, i32, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
     lib.oracle_confidence.restype = ctypes.c_int
@@ -82,13 +82,16 @@ def _logits(z):
 
 
 def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_params=None,
-           nthreads=1):
+           nthreads=1, want_cdf=False):
     """Verify B sequences. zt [B,K+1,V], zd [B,K,V] or None, x [B,K] int32,
     u [B,K+1] float32 or None.
 
     Returns a dict of numpy arrays: out_tokens [B,K+1] int32, accepted_len [B],
     pos_stats [B,K+1,4] (lse_t, h_t, log_ratio, f), feature [B,K], conf [B,K]
-    (NaN without est_params), margin [B] (smallest decision margin), flags [B].
+    (NaN without est_params), margin_acc [B] (acceptance / FLy-gate margin),
+    margin_cdf [B] (margin of the final draw), margin [B] (the smaller of the
+    two), flags [B], and with want_cdf the normalised running sum of each
+    final draw's weights, cdf [B,V].
     """
     lib = _load()
     zt, dt = _logits(zt)
@@ -109,17 +112,23 @@ def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_param
         pos_stats=np.empty((B, K + 1, 4), np.float64),
         feature=np.full((B, K), np.nan),
         conf=np.full((B, K), np.nan),
-        margin=np.empty(B, np.float64),
+        margin_acc=np.empty(B, np.float64),
+        margin_cdf=np.empty(B, np.float64),
         flags=np.empty(B, np.int32),
     )
+    cdf = np.full((B, V), np.nan) if want_cdf else None
     rc = lib.oracle_verify(B, K, V, dt, mode, _ptr(zt), V, _ptr(zd), V, _ptr(x), _ptr(u),
                            float(fly_theta), int(fly_window), _ptr(est),
                            _ptr(out["out_tokens"]), _ptr(out["accepted_len"]),
                            _ptr(out["pos_stats"]), _ptr(out["conf"]) if est is not None else None,
                            _ptr(out["feature"]) if zd is not None else None,
-                           _ptr(out["margin"]), _ptr(out["flags"]), int(nthreads))
+                           _ptr(out["margin_acc"]), _ptr(out["margin_cdf"]), _ptr(cdf),
+                           _ptr(out["flags"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
+    out["margin"] = np.minimum(out["margin_acc"], out["margin_cdf"])
+    if want_cdf:
+        out["cdf"] = cdf
     return out
 
 

@@ -145,6 +145,17 @@ static int32_t inverse_cdf(const double *r, int32_t V, double Z, double u,
     return V - 1;
 }
 
+/* Normalised running sum of the draw's weights, c[v] = (r_0 + .. + r_v) / Z,
+ * summed in the same ascending order as inverse_cdf (for validity checks of
+ * draws that land within the flag margin of a boundary). */
+static void cumulative(const double *r, int32_t V, double Z, double *c) {
+    double s = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+        s += r[v];
+        c[v] = s / Z;
+    }
+}
+
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 
 static double dmin(double a, double b) { return a < b ? a : b; }
@@ -159,11 +170,13 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
                        const int32_t *x, const float *u, double fly_theta, int32_t fly_window,
                        const double *est, int32_t *out_tokens, int32_t *acc_len,
                        double *pos_stats, double *conf, double *feature,
-                       double *margin, int *flags, double *p, double *q, double *r) {
+                       double *margin_acc, double *margin_cdf, double *cdf_out, int *flags,
+                       double *p, double *q, double *r) {
     const size_t es = dtype == OR_F32 ? 4 : 2;
     const char *tbase = (const char *)zt;
     const char *dbase = (const char *)zd;
-    double mg = INFINITY;
+    double mg = INFINITY;      /* acceptance (and FLy gate) margin */
+    double mc = INFINITY;      /* margin of the final inverse-CDF draw */
     int fl = 0;
 
     /* Per-position statistics (written whether or not the position is reached). */
@@ -233,9 +246,8 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
                 Z = 0.0;
                 for (int32_t v = 0; v < V; ++v) { r[v] = p[v]; Z += r[v]; }
             }
-            double cm;
-            token = inverse_cdf(r, V, Z, (double)u[K], &cm, &fl);
-            mg = dmin(mg, cm);
+            token = inverse_cdf(r, V, Z, (double)u[K], &mc, &fl);
+            if (cdf_out) cumulative(r, V, Z, cdf_out);
             rejected = 1;
             break;
         }
@@ -247,9 +259,8 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
             softmax_row(trow, dtype, V, p, &ok);
             double Z = 0.0;
             for (int32_t v = 0; v < V; ++v) Z += p[v];
-            double cm;
-            token = inverse_cdf(p, V, Z, (double)u[K], &cm, &fl);
-            mg = dmin(mg, cm);
+            token = inverse_cdf(p, V, Z, (double)u[K], &mc, &fl);
+            if (cdf_out) cumulative(p, V, Z, cdf_out);
         }
     } else if (mode == OR_GREEDY) {
         /* Exact match: accept x_i iff it is the target's top prediction
@@ -300,7 +311,8 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
     for (int32_t j = 0; j < n; ++j) out_tokens[j] = x[j];
     out_tokens[n] = token;
     *acc_len = n;
-    if (margin) *margin = mg;
+    if (margin_acc) *margin_acc = mg;
+    if (margin_cdf) *margin_cdf = mc;
     if (flags) *flags = fl;
 }
 
@@ -309,7 +321,12 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
  *  u [B][K+1], out_tokens [B][K+1], accepted_len [B],
  *  pos_stats [B][K+1][4] = (lse_t, h_t, log_ratio, f) or NULL,
  *  est [K+1] or NULL, conf [B][K] or NULL, feature [B][K] or NULL,
- *  margin [B] or NULL (smallest decision margin of the sequence),
+ *  margin_acc [B] or NULL: smallest acceptance margin |u_i - min(1, p/q)| over
+ *    the tested positions (FLy: |h_j - theta| over the gates evaluated),
+ *  margin_cdf [B] or NULL: distance of u to the nearer boundary of the drawn
+ *    token's interval, in units of Z (stochastic mode; +inf otherwise),
+ *  cdf [B][V] or NULL: normalised running sum of the final draw's weights
+ *    (stochastic mode; untouched otherwise),
  *  flags [B] or NULL (OR_FLAG_* bits).
  * nthreads > 0 sets the OpenMP thread count. Returns 0, or -1 on bad args. */
 int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
@@ -317,7 +334,8 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const int32_t *x, const float *u, double fly_theta, int32_t fly_window,
                   const double *est, int32_t *out_tokens, int32_t *accepted_len,
                   double *pos_stats, double *conf, double *feature,
-                  double *margin, int32_t *flags, int nthreads) {
+                  double *margin_acc, double *margin_cdf, double *cdf, int32_t *flags,
+                  int nthreads) {
     if (B < 0 || K < 1 || V < 2 || !zt || !x || !out_tokens || !accepted_len) return -1;
     if (mode == OR_STOCHASTIC && (!zd || !u)) return -1;
     if (t_stride <= 0) t_stride = V;
@@ -344,7 +362,8 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                            pos_stats ? pos_stats + (size_t)b * (K + 1) * 4 : NULL,
                            conf ? conf + (size_t)b * K : NULL,
                            feature ? feature + (size_t)b * K : NULL,
-                           margin ? margin + b : NULL, &fl, p, q, r);
+                           margin_acc ? margin_acc + b : NULL, margin_cdf ? margin_cdf + b : NULL,
+                           cdf ? cdf + (size_t)b * (size_t)V : NULL, &fl, p, q, r);
                 if (flags) flags[b] = fl;
             }
         }

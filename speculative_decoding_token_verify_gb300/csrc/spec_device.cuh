@@ -156,6 +156,174 @@ __device__ __forceinline__ RowAcc acc_unpack(const float4 &v) {
     return a;
 }
 
+// ---- packed arithmetic (sm_100+ f32x2 and bf16x2 forms) -------------------
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\tmov.b64 rc, {%6,%7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0,%1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0,%1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// pair arithmetic used by the hot loop: f32x2 instructions, or two scalar
+// ones when SV_PACKED is 0
+#ifndef SV_PACKED
+#define SV_PACKED 1
+#endif
+__device__ __forceinline__ float2 pfma(float2 a, float2 b, float2 c) {
+#if SV_PACKED
+    return ffma2(a, b, c);
+#else
+    return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+#endif
+}
+
+__device__ __forceinline__ float2 padd(float2 a, float2 b) {
+#if SV_PACKED
+    return fadd2(a, b);
+#else
+    return make_float2(a.x + b.x, a.y + b.y);
+#endif
+}
+
+// elementwise max of two bf16 pairs
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---- streaming accumulator (the hot loop) ---------------------------------
+//
+// Per thread, over the 16-byte chunks of one tile, with a lazy reference mr:
+// exponents are taken relative to mr, which only moves when a chunk max
+// exceeds it by more than kRescale nats (so terms stay below e^8 and the
+// rescale branch is rare after the first chunk). The running max bv and the
+// chunk holding it (bk) are tracked per chunk; the mass of that chunk (C) is
+// kept apart from the rest (S), so that the complement mass R never has to be
+// formed as a difference; its bits are kept too, so that stream_finish() can
+// locate the argmax and sum its other elements without a reload, and return
+// the canonical RowAcc. Logits below kMaskFloor count as masked (zero mass).
+
+constexpr float kMaskFloor = -1.0e29f;
+constexpr float kRescale = 8.0f;
+constexpr uint32_t kMaskBf16x2 = 0xF149F149u;   // bf16 pair (-9.95e29, -9.95e29)
+constexpr float kMaskF32 = -1.0e30f;
+
+struct StreamAcc {
+    float mr;    // reference logit
+    float mrL;   // mr * log2(e)
+    float mrh;   // mr + kRescale (a chunk max above it moves the reference)
+    float S;     // sum of 2^{(z - mr) log2e} over chunks other than the best one
+    float C;     // the same sum over the best chunk
+    float2 T;    // sum of 2^y * y, y = (z - mr) log2e (entropy moment, pairwise)
+    float bv;    // running max
+    int bk;      // chunk (vector) index holding bv
+    uint4 bw;    // that chunk's bits, captured by the caller (so finishing needs no reload)
+};
+
+__device__ __forceinline__ StreamAcc stream_init() {
+    StreamAcc s;
+    s.mr = kMaskFloor;
+    s.mrL = kMaskFloor * kLog2e;
+    s.mrh = kMaskFloor + kRescale;
+    s.S = 0.f;
+    s.C = 0.f;
+    s.T = make_float2(0.f, 0.f);
+    s.bv = neg_inf();
+    s.bk = 0;
+    s.bw = make_uint4(0u, 0u, 0u, 0u);
+    return s;
+}
+
+__device__ __forceinline__ void stream_rescale(StreamAcc &s, float c) {
+    const float d = (s.mr - c) * kLog2e;
+    const float al = ex2(d);
+    const float t = al * fmaf(d, s.S + s.C, s.T.x + s.T.y);
+    s.T = make_float2(t, 0.f);
+    s.S *= al;
+    s.C *= al;
+    s.mr = c;
+    s.mrL = c * kLog2e;
+    s.mrh = c + kRescale;
+}
+
+// fold the exponentials of one chunk given as fp32 pairs
+template <int NP, bool kEnt>
+__device__ __forceinline__ void stream_fold(StreamAcc &s, const float2 (&z)[NP], float c, int k) {
+    if (c > s.mrh) stream_rescale(s, c);
+    const bool nb = c > s.bv;
+    s.bv = nb ? c : s.bv;
+    s.bk = nb ? k : s.bk;
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    const float2 ml = make_float2(-s.mrL, -s.mrL);
+    float2 e[NP];
+    float2 y[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        y[p] = pfma(z[p], L2, ml);
+        e[p] = make_float2(ex2(y[p].x), ex2(y[p].y));
+    }
+    float2 a = e[0];
+#pragma unroll
+    for (int p = 1; p < NP; ++p) a = padd(a, e[p]);
+    const float cs = a.x + a.y;
+    if constexpr (kEnt) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) s.T = pfma(e[p], y[p], s.T);
+    }
+    s.S += nb ? s.C : cs;
+    s.C = nb ? cs : s.C;
+}
+
+template <typename T, bool kEnt>
+__device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k) {
+    if constexpr (sizeof(T) == 2) {
+        if constexpr (kEnt) {
+            w.x = bmax2(w.x, kMaskBf16x2);
+            w.y = bmax2(w.y, kMaskBf16x2);
+            w.z = bmax2(w.z, kMaskBf16x2);
+            w.w = bmax2(w.w, kMaskBf16x2);
+        }
+        const uint32_t m = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+        const float c = fmaxf(bf16_lo(m), bf16_hi(m));
+        float2 z[4];
+        z[0] = make_float2(bf16_lo(w.x), bf16_hi(w.x));
+        z[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+        z[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
+        z[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
+        stream_fold<4, kEnt>(s, z, c, k);
+    } else {
+        float2 z[2];
+        z[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+        z[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+        if constexpr (kEnt) {
+            z[0].x = fmaxf(z[0].x, kMaskF32);
+            z[0].y = fmaxf(z[0].y, kMaskF32);
+            z[1].x = fmaxf(z[1].x, kMaskF32);
+            z[1].y = fmaxf(z[1].y, kMaskF32);
+        }
+        const float c = fmaxf(fmaxf(z[0].x, z[0].y), fmaxf(z[1].x, z[1].y));
+        stream_fold<2, kEnt>(s, z, c, k);
+    }
+}
+
 // ---- element access -------------------------------------------------------
 
 template <typename T> struct Elem;
@@ -219,6 +387,32 @@ __device__ __forceinline__ void load8(const T *row, int v, int V, bool vec_ok, f
 #pragma unroll
         for (int j = 0; j < 8; ++j) z[j] = (v + j < V) ? Elem<T>::load(row + v + j) : neg_inf();
     }
+}
+
+// Canonical RowAcc of one thread's streamed chunks; vector 0 of the tile has
+// row index `vb`.
+template <typename T>
+__device__ __forceinline__ RowAcc stream_finish(const StreamAcc &s, int vb) {
+    constexpr int E = Elem<T>::kPerVec;
+    RowAcc a = acc_empty();
+    if (!(s.bv > kMaskFloor)) return a;          // nothing unmasked seen
+    float z[E];
+    Elem<T>::unpack(s.bw, z);
+    int jf = E - 1;
+#pragma unroll
+    for (int j = E - 1; j >= 0; --j)
+        if (z[j] == s.bv) jf = j;
+    float crest = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+        if (j != jf) crest += ex2(fmaf(z[j], kLog2e, -s.mrL));
+    const float d = (s.mr - s.bv) * kLog2e;      // <= 0: mr is some chunk max <= bv
+    const float al = ex2(d);
+    a.M = s.bv;
+    a.R = al * (s.S + crest);
+    a.T = al * fmaf(d, s.S + s.C, s.T.x + s.T.y);
+    a.I = vb + s.bk * E + jf;
+    return a;
 }
 
 }  // namespace sv

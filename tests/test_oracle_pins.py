@@ -400,3 +400,25 @@ def test_fly_gate_tie_defers():
     zt[0, 0, 0] = 1e-3                                # h just below theta: rejected
     r = oracle.verify(zt, None, x, None, mode=oracle.FLY, fly_theta=1.0, fly_window=2)
     assert r["accepted_len"][0] == 0 and r["out_tokens"][0, 0] == 0
+
+
+def test_cdf_output_brackets_every_draw():
+    # the normalised running sum the oracle reports for its final draw ends at 1
+    # and u[b, K] falls inside the drawn token's interval
+    rng = np.random.default_rng(17)
+    B, K, V = 300, 3, 40
+    zt = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    zd = (zt[:, :K] + rng.normal(0, 1, (B, K, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    u = rng.random((B, K + 1), dtype=np.float32)
+    r = oracle.verify(zt, zd, x, u, want_cdf=True)
+    c = r["cdf"]
+    np.testing.assert_allclose(c[:, -1], 1.0, rtol=1e-13)
+    assert (np.diff(c, axis=1) >= 0).all()
+    for b in range(B):
+        v = r["out_tokens"][b, r["accepted_len"][b]]
+        lo = c[b, v - 1] if v > 0 else 0.0
+        assert lo <= u[b, K] < c[b, v]
+        assert r["margin_cdf"][b] == min(u[b, K] - lo, c[b, v] - u[b, K]) or abs(
+            r["margin_cdf"][b] - min(u[b, K] - lo, c[b, v] - u[b, K])) < 1e-12
+    assert np.isinf(oracle.verify(zt, None, x, None, mode=oracle.GREEDY)["margin_cdf"]).all()
