@@ -67,6 +67,7 @@ extern "C" {
 /* limits */
 #define SPEC_MAX_K 31            /* draft positions per sequence            */
 #define SPEC_MAX_V (1 << 20)     /* vocabulary size                         */
+#define SPEC_STATIC_SCRATCH_BYTES (16u << 20) /* scratch of spec_verify_static */
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
@@ -141,6 +142,37 @@ int spec_verify(const spec_verify_params *params, const void *target_logits,
                 int32_t *out_tokens, int32_t *accepted_len, float *pos_stats,
                 const float *est_params, float *feature, float *conf,
                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify_static -- spec_verify without any device allocation.
+ *
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory, e.g. code that runs where the allocator is
+ * off limits (inside a framework that owns all device memory, a custom
+ * allocator hook, or a host callback) and so cannot provide the workspace
+ * spec_verify asks for. The caller still passes the inputs and outputs,
+ * exactly as for spec_verify; the scratch comes from a fixed array of
+ * SPEC_STATIC_SCRATCH_BYTES (16 MiB) that this library keeps in each GPU's
+ * memory from the moment the library is loaded there until the process exits.
+ *
+ *  - Calls whose spec_workspace_size(params) exceeds that size are rejected
+ *    with SPEC_ERR_UNSUPPORTED before anything is enqueued.
+ *  - The call makes no cudaMalloc, cudaFree or other allocating call. Its
+ *    first call on a device looks up the array's device address there
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array, which keeps what the last call left
+ *    in it; each call clears the parts that must start at zero. Calls that
+ *    can overlap on the GPU (other streams, other threads) race on it:
+ *    serialise them.
+ *  - The device status word lives in that array too; it is not readable
+ *    through spec_get_device_status.
+ * Arguments, rules and errors are those of spec_verify.
+ */
+int spec_verify_static(const spec_verify_params *params, const void *target_logits,
+                       const void *draft_logits, const int32_t *draft_tokens, const float *uniforms,
+                       int32_t *out_tokens, int32_t *accepted_len, float *pos_stats,
+                       const float *est_params, float *feature, float *conf, void *stream);
 
 /* Workspace bytes spec_confidence needs; 0 if the arguments are invalid. */
 size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype);

@@ -96,6 +96,8 @@ SIGNATURES = {
     "spec_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyParams)]),
     "spec_verify": (ctypes.c_int, [ctypes.POINTER(VerifyParams), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, ctypes.c_size_t, _P]),
+    "spec_verify_static": (ctypes.c_int, [ctypes.POINTER(VerifyParams), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          _P]),
     "spec_confidence_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "spec_confidence": (ctypes.c_int, [_I32, _I32, _I32, _I32, _P, ctypes.c_int64, _P, _P, _P, _P,
                                        ctypes.c_size_t, _P]),

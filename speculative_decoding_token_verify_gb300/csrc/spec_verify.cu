@@ -1047,6 +1047,17 @@ static bool vec_ok(const void *p, long long stride, int esize) {
     return (reinterpret_cast<uintptr_t>(p) % 16u) == 0 && ((stride * esize) % 16) == 0;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch for spec_verify_static: a fixed device array in this library's own
+// module, so that the call needs no device allocation. Every GPU that loads
+// the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = (size_t)SPEC_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+static std::mutex g_static_mu;
+static void *g_static_ptr[64];   // device address of g_static_scratch, per device
+
 }  // namespace sv
 
 using namespace sv;
@@ -1192,6 +1203,46 @@ int spec_get_device_status(const void *workspace, int32_t *status_out) {
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "status read failed: %s", cudaGetErrorString(e));
     *status_out = (int32_t)v;
     return SPEC_OK;
+}
+
+
+// Allocation-free variant of spec_verify: the workspace is the library's
+// static scratch array instead of caller memory. The host-side name of that
+// array is not a device address, so its address is looked up once per device
+// (cudaGetSymbolAddress, with that device current) on the first call there.
+int spec_verify_static(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
+                       const int32_t *draft_tokens, const float *uniforms, int32_t *out_tokens,
+                       int32_t *accepted_len, float *pos_stats, const float *est_params, float *feature,
+                       float *conf, void *stream) {
+    g_err.clear();
+    if (!p) return fail(SPEC_ERR_INVALID_ARG, "params is NULL");
+    const size_t need = spec_workspace_size(p);
+    if (need == 0) return check_common(p->B, p->K, p->V, p->dtype);   // sets the message
+    if (need > kStaticScratchBytes)
+        return fail(SPEC_ERR_UNSUPPORTED,
+                    "spec_verify_static: this call needs %zu bytes of scratch, more than the %zu-byte static "
+                    "array; use spec_verify with a caller workspace",
+                    need, kStaticScratchBytes);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(SPEC_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_static_mu);
+        if (!g_static_ptr[dev]) {
+            void *ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+            if (e != cudaSuccess || !ptr)
+                return fail(SPEC_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s",
+                            cudaGetErrorString(e));
+            g_static_ptr[dev] = ptr;
+        }
+        ws = g_static_ptr[dev];
+    }
+    // spec_verify zeroes the counters it needs (cudaMemsetAsync, no allocation)
+    return spec_verify(p, target_logits, draft_logits, draft_tokens, uniforms, out_tokens, accepted_len,
+                       pos_stats, est_params, feature, conf, ws, kStaticScratchBytes, stream);
 }
 
 }  // extern "C"
