@@ -45,37 +45,31 @@ namespace sv {
 #define SV_THREADS 128
 #endif
 #ifndef SV_MIN_BLOCKS
-#define SV_MIN_BLOCKS 4
+#define SV_MIN_BLOCKS 8
 #endif
 #ifndef SV_TILE_BYTES
-#define SV_TILE_BYTES 16384
+#define SV_TILE_BYTES 32768
 #endif
 #ifndef SV_RES_SLICES
-#define SV_RES_SLICES 8
+#define SV_RES_SLICES 16
 #endif
-#ifndef SV_STAGES
-#define SV_STAGES 3
-#endif
-#ifndef SV_STAGE_BYTES
-#define SV_STAGE_BYTES 4096
+#ifndef SV_UNROLL
+#define SV_UNROLL 4
 #endif
 
 constexpr int NT = SV_THREADS;         // threads per CTA (independent warps)
 constexpr int NWARP = NT / 32;
-constexpr int kStages = SV_STAGES;     // bulk-copy ring depth per warp
-constexpr int kStageBytes = SV_STAGE_BYTES;  // bytes per ring stage
-constexpr int kStageVecs = kStageBytes / 16;
+constexpr int kUnroll = SV_UNROLL;     // 16-byte loads per lane in flight
 constexpr int kSlice = 256;            // elements per scan slice (32 lanes x 8)
 constexpr int kResSlices = SV_RES_SLICES;  // slices per residual unit
-constexpr int kStage = 256;            // slice totals staged per warp in shared memory
+constexpr int kResBatch = 4;           // slices whose loads are in flight together
+static_assert(kResSlices % kResBatch == 0, "residual units hold whole batches");
 constexpr unsigned kSpinLimit = 1u << 20;  // polls before giving up (~2 s)
-constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
 constexpr unsigned kFull = 0xffffffffu;
 // lane that publishes results and counts completions: not lane 0, which issues
 // the warp's bulk copies, so its release fences never wait behind them
 constexpr int kSig = 1;
 static_assert(NT % 32 == 0 && NT <= 1024, "CTA size must be a multiple of 32");
-static_assert(kStageBytes % 512 == 0, "a stage must hold a whole number of warp vectors");
 
 enum { MODE_STOCHASTIC = 0, MODE_GREEDY = 1, MODE_FLY = 2, MODE_CONF = 3 };
 
@@ -123,8 +117,8 @@ struct Args {
     int nslice;              // scan slices per row
     unsigned *res_ready;     // [B] published flag per slot
     unsigned *res_done;      // [B] residual units completed per sequence
-    int *res_seq;            // [B] slot -> sequence
-    Draw *draw;              // [B]
+    float4 *slotrec;         // [B] per published slot: (lse_t, lse_d, u, 32*b + n)
+    double *utot;            // [B][nR] residual mass per residual unit
     float *slices;           // [B][nslice] residual mass per slice
 };
 
@@ -147,50 +141,6 @@ __device__ __forceinline__ unsigned atom_add_release(unsigned *p, unsigned v) {
 
 __device__ __forceinline__ void fence_acquire() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
-// ---- bulk copies (TMA) into a warp's shared-memory ring -------------------
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_init_fence() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// arm the barrier for `bytes` and copy them from global to shared memory
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
-    unsigned ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0u;
-}
-
-__device__ __forceinline__ uint4 lds128(const void *p) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(smem_addr(p)));
-    return v;
-}
 
 __device__ __forceinline__ void raise_status(const Args &a, unsigned code) {
     atomicMax(a.ctr + CTR_STATUS, code);
@@ -228,14 +178,12 @@ __device__ __forceinline__ double warp_incl_scan_d(double v, int l) {
 }
 
 // ---------------------------------------------------------------------------
-// Stream units through a per-warp ring of bulk copies. The body of a unit
-// (its 16-byte aligned part) is copied stage by stage into the warp's ring in
-// shared memory by lane 0 (cp.async.bulk, completion counted on one mbarrier
-// per stage); the lanes fold each landed stage and lane 0 refills it. The
-// producer runs up to one stream unit ahead of the consumer, so copies keep
-// flowing across unit boundaries and while the warp finalises or does
-// residual work. Scalars before the first and after the last 16-byte boundary
-// of a tile are read directly.
+// Stream one unit (a tile of one row) with one warp. The tile's 16-byte
+// aligned body is read with kUnroll non-allocating 16-byte loads per lane in
+// flight and folded chunk by chunk; scalars before the first and after the
+// last 16-byte boundary are read directly. Latency is hidden by many resident
+// warps (the kernel keeps its register budget small for that), not by deep
+// per-warp buffers.
 // ---------------------------------------------------------------------------
 template <typename T>
 struct UnitGeo {
@@ -269,66 +217,9 @@ __device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit, uns
     return g;
 }
 
-// Ring state: fi (fills issued) and the producer cursor matter in lane 0; ci
-// (stages consumed) is the same in every lane.
-struct Ring {
-    unsigned char *buf;   // kStages * kStageBytes
-    uint64_t *bar;        // kStages mbarriers
-    unsigned fi, ci;
-    unsigned pf_unit;     // unit whose body is being issued
-    const char *pf_src;
-    unsigned pf_bytes, pf_off;
-    bool ahead;           // pf_unit is the warp's next stream unit, not the current one
-    bool dead;            // a copy never landed (SPEC_ERR_TIMEOUT raised)
-};
-
-// lane 0: issue copies until the ring is full or nothing is left to prefetch
-template <typename T>
-__device__ __forceinline__ void ring_fill(const Args &a, Ring &rg, unsigned next_stream, unsigned per_seq) {
-    while (rg.fi - rg.ci < (unsigned)kStages) {
-        if (rg.pf_off >= rg.pf_bytes) {
-            if (rg.ahead || next_stream >= a.units) return;
-            const UnitGeo<T> g = unit_geo<T>(a, next_stream, per_seq);
-            rg.pf_unit = next_stream;
-            rg.pf_src = reinterpret_cast<const char *>(g.row + g.vb);
-            rg.pf_bytes = g.bytes;
-            rg.pf_off = 0;
-            rg.ahead = true;
-            continue;
-        }
-        const unsigned n = min((unsigned)kStageBytes, rg.pf_bytes - rg.pf_off);
-        const unsigned slot = rg.fi % (unsigned)kStages;
-        // the warp's reads of this slot (ordered before by __syncwarp) come
-        // before the bulk copy that overwrites it
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        bulk_load(rg.buf + slot * kStageBytes, rg.pf_src + rg.pf_off, n, rg.bar + slot);
-        rg.pf_off += n;
-        ++rg.fi;
-    }
-}
-
-// lane 0: point the producer at the stream unit the warp starts now
-template <typename T>
-__device__ __forceinline__ void ring_start(const Args &a, Ring &rg, unsigned unit, unsigned next_stream,
-                                           unsigned per_seq) {
-    if (rg.ahead && rg.pf_unit == unit) {
-        rg.ahead = false;     // already being prefetched
-    } else {
-        const UnitGeo<T> g = unit_geo<T>(a, unit, per_seq);
-        rg.pf_unit = unit;
-        rg.pf_src = reinterpret_cast<const char *>(g.row + g.vb);
-        rg.pf_bytes = g.bytes;
-        rg.pf_off = 0;
-        rg.ahead = false;
-    }
-    ring_fill<T>(a, rg, next_stream, per_seq);
-}
-
-// Fold one unit: head/tail scalars directly, the body stage by stage from the
-// ring. Returns the warp-merged accumulator (identical in every lane).
+// Fold one unit. Returns the warp-merged accumulator (identical in every lane).
 template <typename T, bool kEnt>
-__device__ __forceinline__ RowAcc unit_consume(const Args &a, const UnitGeo<T> &g, Ring &rg, unsigned next_stream,
-                                               unsigned per_seq, int l) {
+__device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l) {
     RowAcc hs = acc_empty(), ts = acc_empty();
     if (l < g.head) {
         float z[1] = {Elem<T>::load(g.row + g.v0 + l)};
@@ -338,45 +229,25 @@ __device__ __forceinline__ RowAcc unit_consume(const Args &a, const UnitGeo<T> &
         float z[1] = {Elem<T>::load(g.row + g.ve + l)};
         acc_chunk<1>(ts, z, g.ve + l);
     }
+    const uint4 *vp = reinterpret_cast<const uint4 *>(g.row + g.vb);
+    const int nvec = (int)(g.bytes / 16u);
     StreamAcc s = stream_init();
-    const unsigned nstage = (g.bytes + kStageBytes - 1) / kStageBytes;
-    for (unsigned c = 0; c < nstage; ++c) {
-        const unsigned slot = rg.ci % (unsigned)kStages;
-        const unsigned par = (rg.ci / (unsigned)kStages) & 1u;
-        if (!rg.dead) {
-            unsigned it = 0;
-            while (!mbar_try_wait(rg.bar + slot, par)) {
-                if (++it >= kWaitLimit) {
-                    rg.dead = true;
-                    break;
-                }
-            }
-            rg.dead = __any_sync(kFull, rg.dead);   // the warp decides as one
-            if (rg.dead && l == 0) raise_status(a, SPEC_ERR_TIMEOUT);
-        }
-        const int nv = (int)(min((unsigned)kStageBytes, g.bytes - c * kStageBytes) / 16u);
-        const unsigned char *st = rg.buf + slot * kStageBytes;
-        uint4 w[kStageVecs / 32];
+    int k = l;
+    for (; k + (kUnroll - 1) * 32 < nvec; k += kUnroll * 32) {
+        uint4 w[kUnroll];
 #pragma unroll
-        for (int j = 0; j < kStageVecs / 32; ++j) {
-            const int v = j * 32 + l;
-            w[j] = v < nv ? lds128(st + v * 16) : make_uint4(0u, 0u, 0u, 0u);
-        }
+        for (int q = 0; q < kUnroll; ++q) w[q] = ldg_stream(vp + k + q * 32);
 #pragma unroll
-        for (int j = 0; j < kStageVecs / 32; ++j) {
-            const int v = j * 32 + l;
-            if (v < nv) stream_chunk<T, kEnt>(s, w[j], (int)c * kStageVecs + v);
+        for (int q = 0; q < kUnroll; ++q) {
+            stream_chunk<T, kEnt>(s, w[q], k + q * 32);
+            // keep the bits of the lane's best chunk (no reload when finishing)
+            if (s.bk == k + q * 32) s.bw = w[q];
         }
-        // keep the bits of this lane's best chunk if it lies in this stage; the
-        // load must have landed before the stage is handed back for a refill
-        if (s.bk >= (int)c * kStageVecs) {
-            s.bw = lds128(st + (s.bk - (int)c * kStageVecs) * 16);
-            asm volatile("mov.b32 %0, %0;\n\tmov.b32 %1, %1;\n\tmov.b32 %2, %2;\n\tmov.b32 %3, %3;"
-                         : "+r"(s.bw.x), "+r"(s.bw.y), "+r"(s.bw.z), "+r"(s.bw.w));
-        }
-        __syncwarp();
-        ++rg.ci;
-        if (l == 0 && !rg.dead) ring_fill<T>(a, rg, next_stream, per_seq);
+    }
+    for (; k < nvec; k += 32) {
+        const uint4 w = ldg_stream(vp + k);
+        stream_chunk<T, kEnt>(s, w, k);
+        if (s.bk == k) s.bw = w;
     }
     const RowAcc vs = stream_finish<T>(s, g.vb);
     return warp_merge(acc_merge(acc_merge(hs, vs), ts));
@@ -420,6 +291,21 @@ template <typename T>
 __device__ __noinline__ void finalize(const Args &a, int b, int l) {
     const int K = a.K;
     const float nan = __int_as_float(0x7fc00000);
+    // loads that do not depend on the row statistics go out first: the draft
+    // token, its uniform and the two logits it indexes
+    const bool conf_only = a.mode == MODE_CONF;
+    int xi = -1;
+    bool bad_tok = false;
+    float ui = 0.f, zx = 0.f, qx = 0.f;
+    if (!conf_only && l < K) {
+        xi = a.x[(size_t)b * K + l];
+        if (a.mode == MODE_STOCHASTIC) ui = a.u[(size_t)b * (K + 1) + l];
+        bad_tok = xi < 0 || xi >= a.V;
+        if (!bad_tok && a.nd_rows > 0) {
+            zx = Elem<T>::load(trow_ptr<T>(a, b, l) + xi);
+            qx = Elem<T>::load(drow_ptr<T>(a, b, l) + xi);
+        }
+    }
     RowAcc tr = acc_empty(), dr = acc_empty();
     {
         // eight partials of each row in flight at a time, merged in tile order
@@ -457,31 +343,13 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l) {
         f = dr.R > 0.f ? -logf(dr.R) : kFeatureClamp;
     }
     if (bad_row) raise_status(a, SPEC_ERR_BAD_ROW);
-    int xi = -1;
-    bool bad_tok = false;
-    if (a.mode != MODE_CONF && l < K) {
-        xi = a.x[(size_t)b * K + l];
-        bad_tok = xi < 0 || xi >= a.V;
-        if (bad_tok) raise_status(a, SPEC_ERR_BAD_TOKEN);
-    }
-    if (a.mode != MODE_CONF && l < K && a.nd_rows > 0) {
-        if (!bad_tok) {
-            const float zx = Elem<T>::load(trow_ptr<T>(a, b, l) + xi);
-            const float qx = Elem<T>::load(drow_ptr<T>(a, b, l) + xi);
-            lr = (zx - lse_t) - (qx - lse_d);
-        } else {
-            lr = neg_inf();
-        }
-    }
+    if (bad_tok) raise_status(a, SPEC_ERR_BAD_TOKEN);
+    if (!conf_only && l < K && a.nd_rows > 0) lr = bad_tok ? neg_inf() : (zx - lse_t) - (qx - lse_d);
     int n = K;
     if (a.mode == MODE_STOCHASTIC) {
         // "Математика верификации": accept iff u < min(1, p/q); lr = +inf
         // (q(x) = 0 < p(x)) accepts, NaN (p(x) = q(x) = 0) rejects
-        bool acc = false;
-        if (l < K) {
-            const float ui = a.u[(size_t)b * (K + 1) + l];
-            acc = lr >= 0.f || ui < ex2(lr * kLog2e);
-        }
+        const bool acc = l < K && (lr >= 0.f || ui < ex2(lr * kLog2e));
         n = min(__ffs(~__ballot_sync(kFull, acc)) - 1, K);
     } else if (a.mode == MODE_GREEDY) {
         const bool acc = l < K && !bad_tok && xi == amax_t;
@@ -535,14 +403,8 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l) {
         a.acc_len[b] = n;
         if (draw) {
             // hand the draw to the residual units of b and publish them
-            Draw d;
-            d.lse_t = lt_n;
-            d.lse_d = ld_n;
-            d.u = a.u[(size_t)b * (K + 1) + K];
-            d.n = n;
-            a.draw[b] = d;
             const unsigned slot = atomicAdd(a.ctr + CTR_RES_ALLOC, 1u);
-            a.res_seq[slot] = b;
+            a.slotrec[slot] = make_float4(lt_n, ld_n, a.u[(size_t)b * (K + 1) + K], __int_as_float(b * 32 + n));
             __threadfence();
             st_release(a.res_ready + slot, 1u);
             atomicAdd(a.ctr + CTR_RES_PUB, (unsigned)a.nR);
@@ -557,6 +419,58 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l) {
 // v whose running sum in ascending v exceeds u * Z.
 // ---------------------------------------------------------------------------
 
+// Per-unit totals make the scan two-level: each residual unit stores its
+// slice sums and, in fp64, their sum in slice order; locate() scans the unit
+// totals, then the slices of one unit, then one slice.
+
+// lane-parallel fp64 inclusive scan over n (<= 32*per) values held
+// contiguously per lane; finds the first index whose running sum exceeds
+// `target`. Returns that index (or -1) and the running sum before it in *P.
+template <int kPer>
+__device__ __forceinline__ int scan_find(const double (&v)[kPer], int n, int l, double target, double base,
+                                         double *P) {
+    double seg = 0.0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) seg += (l * kPer + j < n) ? v[j] : 0.0;
+    const double incl = warp_incl_scan_d(seg, l) + base;
+    double c = incl - seg;
+    int found = -1;
+    double Pf = 0.0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        if (found < 0 && l * kPer + j < n) {
+            const double prev = c;
+            c += v[j];
+            if (c > target) {
+                found = l * kPer + j;
+                Pf = prev;
+            }
+        }
+    }
+    const unsigned m = __ballot_sync(kFull, found >= 0);
+    if (!m) return -1;
+    const int L = __ffs(m) - 1;
+    *P = __shfl_sync(kFull, Pf, L);
+    return __shfl_sync(kFull, found, L);
+}
+
+// the last index in [0, n) with a positive value, warp-wide (-1 if none)
+template <int kPer>
+__device__ __forceinline__ int last_positive(const double (&v)[kPer], int n, int l) {
+    int lm = -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+        if (l * kPer + j < n && v[j] > 0.0) lm = l * kPer + j;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(kFull, lm, o));
+    return lm;
+}
+
+constexpr int kUnitsPerLane = ((SPEC_MAX_V / kSlice + kResSlices - 1) / kResSlices + 31) / 32;  // unit totals per lane
+static_assert((SPEC_MAX_V / kSlice + kResSlices - 1) / kResSlices <= 32 * kUnitsPerLane,
+              "residual units per row exceed the locate scan");
+static_assert(kResSlices <= 32, "a residual unit's slices are scanned one per lane");
+
 // Sum of slice s (elements 256s .. 256s+255) of the draw's weights, per lane
 // (8 elements each), in the fixed order every consumer of slice sums uses.
 template <typename T>
@@ -566,91 +480,53 @@ __device__ __forceinline__ float slice_lane_sum(const Args &a, const T *tr, cons
     return sum8(r);
 }
 
-// Locate the token of a draw whose slice totals are in `sl` (global): the
-// warp sums them in fp64 (Z), then scans them page by page through shared
-// memory to find the slice whose running sum first exceeds u*Z, and rescans
-// that slice lane by lane with an fp64 prefix. Returns the token, or -1 when
-// Z is not positive (only possible through rounding, or a bad row).
+// Locate the token of sequence b's draw from its unit totals (fp64) and slice
+// totals: Z is the sum of the unit totals; the scan picks the unit, then the
+// slice whose running sum first exceeds u*Z, then rescans that slice lane by
+// lane with an fp64 prefix. Returns the token, or -1 when Z is not positive
+// (only possible through rounding, or a bad row).
 template <typename T>
-__device__ int locate_scan(const Args &a, const float *sl, const T *tr, const T *dr, const Draw &d,
-                           float *stage, int l) {
-    const int ne = a.nslice;
-    double z = 0.0;
-    for (int e0 = 0; e0 < ne; e0 += 256) {
-        float v[8];
+__device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l) {
+    const double *ut = a.utot + (size_t)b * a.nR;
+    double v[kUnitsPerLane];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = e0 + j * 32 + l;
-            v[j] = e < ne ? __ldcg(sl + e) : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) z += (double)v[j];
+    for (int j = 0; j < kUnitsPerLane; ++j) {
+        const int i = l * kUnitsPerLane + j;
+        v[j] = i < a.nR ? __ldcg(ut + i) : 0.0;
     }
-    const double Z = warp_sum_d(z);
+    double seg = 0.0;
+#pragma unroll
+    for (int j = 0; j < kUnitsPerLane; ++j) seg += v[j];
+    const double Z = __shfl_sync(kFull, warp_incl_scan_d(seg, l), 31);
     if (!(Z > 0.0)) return -1;
     const double target = (double)d.u * Z;
-    double run = 0.0;
-    int entry = -1, last_mass = -1;
+    // nothing inside a fallback unit or slice may exceed the target: its last
+    // mass is taken
+    const double none = -2.0 * Z - 1.0;
     double P = 0.0;
-    for (int p0 = 0; p0 < ne && entry < 0; p0 += kStage) {
-        const int np = min(kStage, ne - p0);
-        for (int e0 = 0; e0 < np; e0 += 256) {
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = e0 + j * 32 + l;
-                v[j] = e < np ? __ldcg(sl + p0 + e) : 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = e0 + j * 32 + l;
-                if (e < np) stage[e] = v[j];
-            }
-        }
-        __syncwarp();
-        const int per = (np + 31) / 32;
-        const int e0 = min(np, l * per), e1 = min(np, e0 + per);
-        double seg = 0.0;
-        int lm = -1;
-        for (int e = e0; e < e1; ++e) {
-            seg += (double)stage[e];
-            if (stage[e] > 0.f) lm = p0 + e;
-        }
-        const double incl = warp_incl_scan_d(seg, l) + run;
-        double c = incl - seg;
-        int found = -1;
-        double Pf = 0.0;
-        for (int e = e0; e < e1 && found < 0; ++e) {
-            const double prev = c;
-            c += (double)stage[e];
-            if (c > target) {
-                found = p0 + e;
-                Pf = prev;
-            }
-        }
-        const unsigned m = __ballot_sync(kFull, found >= 0);
-        if (m) {
-            const int L = __ffs(m) - 1;
-            entry = __shfl_sync(kFull, found, L);
-            P = __shfl_sync(kFull, Pf, L);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(kFull, lm, o));
-        last_mass = max(last_mass, lm);
-        run = __shfl_sync(kFull, incl, 31);
-        __syncwarp();
+    int unit = scan_find<kUnitsPerLane>(v, a.nR, l, target, 0.0, &P);
+    if (unit < 0) {
+        unit = last_positive<kUnitsPerLane>(v, a.nR, l);
+        if (unit < 0) return -1;
+        P = none;
     }
-    if (entry < 0) {
-        // rounding left u*Z at the total: the last slice with mass
-        if (last_mass < 0) return -1;
-        entry = last_mass;
-        P = -2.0 * Z - 1.0;  // nothing inside exceeds target: take its last mass
+    const int s0 = unit * kResSlices;
+    const int ns = min(kResSlices, a.nslice - s0);
+    double sv[1];
+    sv[0] = l < ns ? (double)__ldcg(a.slices + (size_t)b * a.nslice + s0 + l) : 0.0;
+    double P2 = 0.0;
+    int sl = scan_find<1>(sv, ns, l, target, P, &P2);
+    if (sl < 0) {
+        sl = last_positive<1>(sv, ns, l);
+        if (sl < 0) return -1;
+        P2 = none;
     }
+    const int entry = s0 + sl;
     float r[8];
     const float s = slice_lane_sum<T>(a, tr, dr, entry, l, d.lse_t, d.lse_d, r);
     const double in = warp_incl_scan_d((double)s, l);
     const double ex = in - (double)s;
-    const unsigned hit = __ballot_sync(kFull, P + in > target);
+    const unsigned hit = __ballot_sync(kFull, P2 + in > target);
     int L;
     if (hit) {
         L = __ffs(hit) - 1;
@@ -659,7 +535,7 @@ __device__ int locate_scan(const Args &a, const float *sl, const T *tr, const T 
         L = nz ? 31 - __clz(nz) : 0;
     }
     int tok = -1, lastpos = -1;
-    double cc = P + ex;
+    double cc = P2 + ex;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if (r[j] > 0.f) lastpos = j;
@@ -670,25 +546,46 @@ __device__ int locate_scan(const Args &a, const float *sl, const T *tr, const T 
     return __shfl_sync(kFull, entry * kSlice + L * 8 + tok, L);
 }
 
+// Residual unit t of sequence b: the sums of its slices of the draw's weights
+// (kResBatch slices' loads in flight at a time) and their fp64 total in slice
+// order.
+template <typename T>
+__device__ __forceinline__ void unit_sums(const Args &a, int b, int t, const T *tr, const T *dr, const Draw &d,
+                                          int l) {
+    double tot = 0.0;
+    for (int i0 = 0; i0 < kResSlices; i0 += kResBatch) {
+        float part[kResBatch];
+#pragma unroll
+        for (int i = 0; i < kResBatch; ++i) {
+            float r[8];
+            part[i] = slice_lane_sum<T>(a, tr, dr, t * kResSlices + i0 + i, l, d.lse_t, d.lse_d, r);
+        }
+#pragma unroll
+        for (int i = 0; i < kResBatch; ++i) {
+            const int sidx = t * kResSlices + i0 + i;
+            const float s = warp_sum_f(part[i]);
+            if (sidx < a.nslice) {
+                tot += (double)s;
+                if (l == kSig) a.slices[(size_t)b * a.nslice + sidx] = s;
+            }
+        }
+    }
+    if (l == kSig) a.utot[(size_t)b * a.nR + t] = tot;
+}
+
 // The last residual unit of sequence b: locate its token. If the residual
 // mass vanished (only possible through rounding) the warp redraws from p.
 template <typename T>
-__device__ __noinline__ void locate(const Args &a, int b, const Draw &d, float *stage, int l) {
+__device__ __noinline__ void locate(const Args &a, int b, const Draw &d, int l) {
     const int K = a.K;
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.n < K ? drow_ptr<T>(a, b, d.n) : nullptr;
-    float *sl = a.slices + (size_t)b * a.nslice;
-    int token = locate_scan<T>(a, sl, tr, dr, d, stage, l);
+    int token = locate_scan<T>(a, b, tr, dr, d, l);
     if (token < 0 && dr != nullptr) {
-        // recompute the slice totals of p alone and scan again
-        for (int s = 0; s < a.nslice; ++s) {
-            float r[8];
-            const float t = warp_sum_f(slice_lane_sum<T>(a, tr, nullptr, s, l, d.lse_t, d.lse_d, r));
-            if (l == 0) sl[s] = t;
-        }
+        for (int t = 0; t < a.nR; ++t) unit_sums<T>(a, b, t, tr, nullptr, d, l);
         __threadfence_block();
         __syncwarp();
-        token = locate_scan<T>(a, sl, tr, nullptr, d, stage, l);
+        token = locate_scan<T>(a, b, tr, nullptr, d, l);
     }
     if (token < 0) {
         if (l == 0) raise_status(a, SPEC_ERR_BAD_ROW);
@@ -697,89 +594,53 @@ __device__ __noinline__ void locate(const Args &a, int b, const Draw &d, float *
     if (l == 0) a.out_tokens[(size_t)b * (K + 1) + d.n] = token;
 }
 
-// One residual unit: slices [kResSlices*t, kResSlices*(t+1)) of the stop rows
-// of the sequence in `slot`. The last unit of the sequence locates its token.
+// One residual unit of the sequence published in `slot`. Its record holds
+// (lse_t, lse_d, u, 32*b + n). The last unit of the sequence locates its token.
 template <typename T>
-__device__ __noinline__ void residual_unit(const Args &a, unsigned id, float *stage, int l) {
+__device__ __noinline__ void residual_unit(const Args &a, unsigned id, int l) {
     const int slot = (int)(id / (unsigned)a.nR);
     const int t = (int)(id - (unsigned)slot * (unsigned)a.nR);
-    int b = 0;
-    float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (l == 0) {
-        b = __ldcg(a.res_seq + slot);
-        dv = __ldcg(reinterpret_cast<const float4 *>(a.draw + b));
-    }
-    b = __shfl_sync(kFull, b, 0);
+    const float4 rec = __ldcg(a.slotrec + slot);
+    const int bits = __float_as_int(rec.w);
+    const int b = bits >> 5;
     Draw d;
-    d.lse_t = __shfl_sync(kFull, dv.x, 0);
-    d.lse_d = __shfl_sync(kFull, dv.y, 0);
-    d.u = __shfl_sync(kFull, dv.z, 0);
-    d.n = __shfl_sync(kFull, __float_as_int(dv.w), 0);
+    d.lse_t = rec.x;
+    d.lse_d = rec.y;
+    d.u = rec.z;
+    d.n = bits & 31;
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.n < a.K ? drow_ptr<T>(a, b, d.n) : nullptr;
-    float part[kResSlices];
-#pragma unroll
-    for (int i = 0; i < kResSlices; ++i) {
-        float r[8];
-        part[i] = slice_lane_sum<T>(a, tr, dr, t * kResSlices + i, l, d.lse_t, d.lse_d, r);
-    }
-#pragma unroll
-    for (int i = 0; i < kResSlices; ++i) {
-        const int sidx = t * kResSlices + i;
-        const float s = warp_sum_f(part[i]);
-        if (l == kSig && sidx < a.nslice) a.slices[(size_t)b * a.nslice + sidx] = s;
-    }
+    unit_sums<T>(a, b, t, tr, dr, d, l);
     bool last = false;
     if (l == kSig) last = atom_add_release(a.res_done + b, 1u) == (unsigned)a.nR - 1;
     last = __shfl_sync(kFull, last, kSig);
     if (last) {
         fence_acquire();
-        locate<T>(a, b, d, stage, l);
+        locate<T>(a, b, d, l);
     }
 }
 
 // ---------------------------------------------------------------------------
-// Scheduling, per warp (lane 0 keeps the state). Residual units are claimed
-// with atomicAdd (a CAS loop would serialise the GPU on one counter) and only
-// when the published count suggests one is free; a unit claimed before its
-// sequence is published stays pending while the warp keeps streaming. A warp
-// waits only when it holds no stream unit; every publication depends only on
-// stream units held by running warps, which never wait, so each wait ends.
+// Scheduling, per warp (lane 0 keeps the state). Stream units come first, in
+// sequence-major order, one atomicAdd each, prefetched one job ahead. Once the
+// stream queue is empty the warp turns to residual units: claimed with
+// atomicAdd in publication order (a CAS loop would serialise the GPU on one
+// counter), each run once its sequence is published. A warp waits only when it
+// holds no stream unit and has completed everything it streamed; every
+// publication depends only on stream units held by running warps, which never
+// wait, so each wait ends.
 // ---------------------------------------------------------------------------
 struct Sched {
     unsigned next_stream;   // prefetched stream unit (>= units: none left)
     unsigned pend;          // claimed residual unit not yet run (kNone: none)
-    unsigned res_claim, res_pub, pend_ready;   // loads issued one job ahead
 };
 constexpr unsigned kNone = 0xffffffffu;
-
-__device__ __forceinline__ void sched_prefetch(const Args &a, Sched &q) {
-    if (!a.res_units) return;
-    q.res_claim = ld_relaxed(a.ctr + CTR_RES_CLAIM);
-    q.res_pub = ld_relaxed(a.ctr + CTR_RES_PUB);
-    q.pend_ready = q.pend != kNone ? ld_relaxed(a.res_ready + q.pend / (unsigned)a.nR) : 0u;
-}
 
 enum { JOB_DONE = 0, JOB_STREAM = 1, JOB_RESIDUAL = 2, JOB_WAIT = 3 };
 
 // lane 0: the next job that can start now; JOB_WAIT when the only work left
 // is residual work that is not published yet (see wait_job).
 __device__ __forceinline__ int next_job(const Args &a, Sched &q, unsigned &id) {
-    if (a.res_units) {
-        if (q.pend == kNone && q.res_claim < q.res_pub && q.res_claim < a.res_units) {
-            const unsigned c = atomicAdd(a.ctr + CTR_RES_CLAIM, 1u);
-            if (c < a.res_units) {
-                q.pend = c;
-                q.pend_ready = ld_relaxed(a.res_ready + c / (unsigned)a.nR);
-            }
-        }
-        if (q.pend != kNone && q.pend_ready) {
-            id = q.pend;
-            q.pend = kNone;
-            fence_acquire();           // the slot's data after its flag
-            return JOB_RESIDUAL;
-        }
-    }
     if (q.next_stream < a.units) {
         id = q.next_stream;
         q.next_stream = atomicAdd(a.ctr + CTR_CLAIM, 1u);
@@ -815,72 +676,63 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
 
 // ---------------------------------------------------------------------------
 // The persistent kernel: every warp is an independent worker (no block-wide
-// barrier anywhere). Dynamic shared memory per warp: the bulk-copy ring, its
-// mbarriers and a page of slice totals for the final scan.
+// barrier anywhere, no shared memory).
 // ---------------------------------------------------------------------------
-constexpr int kWarpSmem = kStages * kStageBytes + ((kStages * 8 + 127) / 128) * 128 + kStage * 4;
-
 template <typename T>
 __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a) {
-    extern __shared__ __align__(128) unsigned char dsm[];
     const int l = threadIdx.x & 31;
-    unsigned char *base = dsm + (threadIdx.x >> 5) * kWarpSmem;
-    Ring rg;
-    rg.buf = base;
-    rg.bar = reinterpret_cast<uint64_t *>(base + kStages * kStageBytes);
-    float *stage = reinterpret_cast<float *>(base + kStages * kStageBytes + ((kStages * 8 + 127) / 128) * 128);
-    rg.fi = rg.ci = 0u;
-    rg.pf_unit = kNone;
-    rg.pf_src = nullptr;
-    rg.pf_bytes = rg.pf_off = 0u;
-    rg.ahead = false;
-    rg.dead = false;
-    if (l == 0) {
-        for (int i = 0; i < kStages; ++i) mbar_init(rg.bar + i, 1u);
-        mbar_init_fence();
-    }
-    __syncwarp();
     const unsigned per_seq = (unsigned)a.rows * (unsigned)a.nT;
     Sched q;
     q.pend = kNone;
-    q.res_claim = q.res_pub = q.pend_ready = 0u;
     q.next_stream = 0u;
-    if (l == 0) {
-        q.next_stream = atomicAdd(a.ctr + CTR_CLAIM, 1u);
-        sched_prefetch(a, q);
-    }
+    if (l == 0) q.next_stream = atomicAdd(a.ctr + CTR_CLAIM, 1u);
+    // Completion of a stream unit: its partial and a release-increment of the
+    // sequence's counter go out at once, but the returned count (is this the
+    // sequence's last unit?) is read only after the next unit, so the warp
+    // does not stall on the atomic. The check is always made before the warp
+    // waits or takes other work.
+    int dprev_b = -1;            // sequence of the unit whose count is pending
+    unsigned dprev_old = 0u;     // that count (lane kSig)
     for (;;) {
         int kind = 0;
         unsigned unit = 0;
-        if (l == 0) {
-            kind = next_job(a, q, unit);
-            if (kind == JOB_WAIT) kind = wait_job(a, q, unit);
-            if (kind == JOB_STREAM) ring_start<T>(a, rg, unit, q.next_stream, per_seq);
-            sched_prefetch(a, q);      // consumed at the next job
-        }
+        if (l == 0) kind = next_job(a, q, unit);
         kind = __shfl_sync(kFull, kind, 0);
         unit = __shfl_sync(kFull, unit, 0);
-        if (kind == JOB_DONE || rg.dead) break;
+        if (kind != JOB_STREAM && dprev_b >= 0) {
+            const bool last = __shfl_sync(kFull, dprev_old == per_seq - 1, kSig);
+            if (last) {
+                fence_acquire();
+                finalize<T>(a, dprev_b, l);
+            }
+            dprev_b = -1;
+        }
+        if (kind == JOB_WAIT) {
+            if (l == 0) kind = wait_job(a, q, unit);
+            kind = __shfl_sync(kFull, kind, 0);
+            unit = __shfl_sync(kFull, unit, 0);
+        }
+        if (kind == JOB_DONE) break;
         if (kind == JOB_RESIDUAL) {
-            residual_unit<T>(a, unit, stage, l);
+            residual_unit<T>(a, unit, l);
             continue;
         }
-        const unsigned nxt = __shfl_sync(kFull, q.next_stream, 0);
         const UnitGeo<T> g = unit_geo<T>(a, unit, per_seq);
         // target rows also carry the entropy moment; draft rows do not need it
-        const RowAcc s = g.target ? unit_consume<T, true>(a, g, rg, nxt, per_seq, l)
-                                  : unit_consume<T, false>(a, g, rg, nxt, per_seq, l);
+        const RowAcc s = g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l);
+        if (dprev_b >= 0) {
+            const bool last = __shfl_sync(kFull, dprev_old == per_seq - 1, kSig);
+            if (last) {
+                fence_acquire();
+                finalize<T>(a, dprev_b, l);
+            }
+        }
         const int b = (int)(unit / per_seq);
-        bool last = false;
         if (l == kSig) {
             a.part[unit] = acc_pack(s);
-            last = atom_add_release(a.seq_done + b, 1u) == per_seq - 1;
+            dprev_old = atom_add_release(a.seq_done + b, 1u);
         }
-        last = __shfl_sync(kFull, last, kSig);
-        if (last) {
-            fence_acquire();
-            finalize<T>(a, b, l);
-        }
+        dprev_b = b;
     }
 }
 
@@ -904,7 +756,7 @@ static int fail(int code, const char *fmt, ...) {
 struct Plan {
     int nT, TS, nR, nslice;
     unsigned long long units;
-    size_t seq_off, ready_off, done_off, resseq_off, draw_off, part_off, slice_off;
+    size_t seq_off, ready_off, done_off, rec_off, utot_off, part_off, slice_off;
     size_t zero_bytes, bytes;
 };
 
@@ -914,13 +766,13 @@ struct Plan {
 
 // A stream unit is one warp's share: a tile of at most SV_TILE_BYTES of
 // logits. Small batches split rows further, down to SV_MIN_TILE elements,
-// aiming at ~64K units (about 16 per warp of a full GB300) so that the
+// aiming at ~32K units (about 7 per resident warp of a GB300) so that the
 // queue's tail stays short.
 static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
     const int ts_max = SV_TILE_BYTES / esize;
     int nT = (V + ts_max - 1) / ts_max;
     const long long rows_total = (long long)B * rows;
-    long long want = (65536 + rows_total - 1) / rows_total;
+    long long want = (32768 + rows_total - 1) / rows_total;
     const long long cap = V / SV_MIN_TILE;
     if (want > cap) want = cap;
     if (want > nT) nT = (int)want;
@@ -937,16 +789,17 @@ static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace: [header words | seq_done[B] | res_ready[B] | res_done[B]] (zeroed
-// per call) [res_seq[B] | draw[B] | tile partials B*rows*nT | slices B*nslice]
+// per call) [slot records B | unit totals B*nR | tile partials B*rows*nT |
+// slices B*nslice]
 static void plan_workspace(int B, int rows, int V, int esize, Plan &p) {
     plan_tiles(B, rows, V, esize, p);
     p.seq_off = kHeaderWords * sizeof(unsigned);
     p.ready_off = p.seq_off + (size_t)B * sizeof(unsigned);
     p.done_off = p.ready_off + (size_t)B * sizeof(unsigned);
     p.zero_bytes = p.done_off + (size_t)B * sizeof(unsigned);
-    p.resseq_off = p.zero_bytes;
-    p.draw_off = align_up(p.resseq_off + (size_t)B * sizeof(int), 16);
-    p.part_off = align_up(p.draw_off + (size_t)B * sizeof(Draw), 16);
+    p.rec_off = align_up(p.zero_bytes, 16);
+    p.utot_off = align_up(p.rec_off + (size_t)B * sizeof(float4), 16);
+    p.part_off = align_up(p.utot_off + (size_t)B * p.nR * sizeof(double), 16);
     p.slice_off = align_up(p.part_off + (size_t)B * rows * p.nT * sizeof(float4), 16);
     p.bytes = align_up(p.slice_off + (size_t)B * p.nslice * sizeof(float), 16);
     p.units = (unsigned long long)B * rows * p.nT;
@@ -960,14 +813,11 @@ struct DevInfo {
 static std::mutex g_dev_mu;
 static DevInfo g_dev[64];
 
-constexpr size_t kDynSmem = (size_t)NWARP * kWarpSmem;
+constexpr size_t kDynSmem = 0;
 
 template <typename T>
 static int occupancy() {
     int n = 0;
-    if (cudaFuncSetAttribute(verify_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem) !=
-        cudaSuccess)
-        return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<T>, NT, kDynSmem) != cudaSuccess) n = 0;
     return n;
 }
@@ -1002,8 +852,8 @@ static int launch(Args &a, const Plan &p, int dtype, void *ws, void *stream) {
     a.seq_done = reinterpret_cast<unsigned *>(base + p.seq_off);
     a.res_ready = reinterpret_cast<unsigned *>(base + p.ready_off);
     a.res_done = reinterpret_cast<unsigned *>(base + p.done_off);
-    a.res_seq = reinterpret_cast<int *>(base + p.resseq_off);
-    a.draw = reinterpret_cast<Draw *>(base + p.draw_off);
+    a.slotrec = reinterpret_cast<float4 *>(base + p.rec_off);
+    a.utot = reinterpret_cast<double *>(base + p.utot_off);
     a.part = reinterpret_cast<float4 *>(base + p.part_off);
     a.slices = reinterpret_cast<float *>(base + p.slice_off);
     a.nT = p.nT;
