@@ -13,11 +13,11 @@
 //    last unit of b (per-sequence counter) finalises b: it merges the row
 //    partials, applies the mode's rule, writes the per-position outputs and,
 //    in stochastic mode, publishes b's draw.
-//  * residual units (published sequence, range of 256-element slices),
-//    claimed first whenever one is published: they sum max(0, p - q) (or p for
-//    the bonus draw) per slice of the stop rows while those rows are still in
-//    L2. The warp that completes the last residual unit of b locates the token
-//    by an inverse-CDF scan of the slice sums and one slice.
+//  * residual units (published sequence, a run of 256-element slices),
+//    taken once the stream queue is empty: they sum max(0, p - q) (or p for
+//    the bonus draw) per slice of the stop rows. The warp that completes the
+//    last residual unit of b locates the token by an fp64 inverse-CDF scan of
+//    the slice sums and one slice.
 //
 // A warp waits only when the stream queue is empty and residual work is still
 // to be published; every unit in flight completes without waiting, so the
@@ -50,8 +50,12 @@ namespace sv {
 #ifndef SV_TILE_BYTES
 #define SV_TILE_BYTES 32768
 #endif
-#ifndef SV_RES_SLICES
-#define SV_RES_SLICES 16
+// slices per residual unit: 8 KB (bf16) or 32 KB (fp32) of the two rows
+#ifndef SV_RES_SLICES_BF16
+#define SV_RES_SLICES_BF16 8
+#endif
+#ifndef SV_RES_SLICES_F32
+#define SV_RES_SLICES_F32 16
 #endif
 #ifndef SV_UNROLL
 #define SV_UNROLL 4
@@ -61,13 +65,19 @@ constexpr int NT = SV_THREADS;         // threads per CTA (independent warps)
 constexpr int NWARP = NT / 32;
 constexpr int kUnroll = SV_UNROLL;     // 16-byte loads per lane in flight
 constexpr int kSlice = 256;            // elements per scan slice (32 lanes x 8)
-constexpr int kResSlices = SV_RES_SLICES;  // slices per residual unit
-constexpr int kResBatch = 4;           // slices whose loads are in flight together
-static_assert(kResSlices % kResBatch == 0, "residual units hold whole batches");
-constexpr unsigned kSpinLimit = 1u << 20;  // polls before giving up (~2 s)
+template <typename T>
+__host__ __device__ constexpr int res_slices() { return sizeof(T) == 2 ? SV_RES_SLICES_BF16 : SV_RES_SLICES_F32; }
+// slices whose loads are in flight together: 8 16-byte vectors per lane
+// (two rows) for bf16, 16 for fp32
+constexpr int kResBatch = 4;
+static_assert(SV_RES_SLICES_BF16 % kResBatch == 0 && SV_RES_SLICES_F32 % kResBatch == 0,
+              "residual units hold whole batches");
+constexpr int kStage = 256;            // 16-byte entries of a warp's shared staging buffer (4 KB)
+constexpr int kScanPer = 4 * kStage / 32;  // slice sums per lane in one pass of the locate scan
+constexpr unsigned kSpinLimit = 1u << 20;  // polls before giving up (< 1 s)
 constexpr unsigned kFull = 0xffffffffu;
-// lane that publishes results and counts completions: not lane 0, which issues
-// the warp's bulk copies, so its release fences never wait behind them
+// lane that publishes results and counts completions (lane 0 keeps the
+// scheduling state, so the two sets of long-latency operations stay apart)
 constexpr int kSig = 1;
 static_assert(NT % 32 == 0 && NT <= 1024, "CTA size must be a multiple of 32");
 
@@ -76,8 +86,7 @@ enum { MODE_STOCHASTIC = 0, MODE_GREEDY = 1, MODE_FLY = 2, MODE_CONF = 3 };
 // workspace header words (zeroed before every launch); the busy counters sit
 // on separate 128-byte lines so that their atomics and polls do not queue on
 // one L2 slice
-enum { CTR_CLAIM = 0, CTR_STATUS = 32, CTR_RES_ALLOC = 64, CTR_RES_CLAIM = 96, CTR_RES_PUB = 128,
-       kHeaderWords = 160 };
+enum { CTR_CLAIM = 0, CTR_STATUS = 32, CTR_RES_ALLOC = 64, CTR_RES_CLAIM = 96, kHeaderWords = 128 };
 
 // what finalise hands to the residual units of a sequence
 struct Draw {
@@ -105,6 +114,7 @@ struct Args {
     int nd_rows;             // draft rows streamed per sequence (K or 0)
     int rows;
     int nT;                  // tiles per row
+    int gsh;                 // log2 of the lane-group size that merges one row's partials
     int TS;                  // tile size (elements, multiple of 8)
     unsigned units;          // B * rows * nT
     int t_vec_ok, d_vec_ok;  // rows start on 16-byte boundaries
@@ -115,11 +125,11 @@ struct Args {
     unsigned res_units;      // B * nR in stochastic mode, else 0
     int nR;                  // residual units per sequence
     int nslice;              // scan slices per row
+    int sstride;             // slice sums per sequence in `slices` (nslice rounded up to 4)
     unsigned *res_ready;     // [B] published flag per slot
     unsigned *res_done;      // [B] residual units completed per sequence
     float4 *slotrec;         // [B] per published slot: (lse_t, lse_d, u, 32*b + n)
-    double *utot;            // [B][nR] residual mass per residual unit
-    float *slices;           // [B][nslice] residual mass per slice
+    float *slices;           // [B][sstride] residual mass per slice
 };
 
 __device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
@@ -140,6 +150,15 @@ __device__ __forceinline__ unsigned atom_add_release(unsigned *p, unsigned v) {
 }
 
 __device__ __forceinline__ void fence_acquire() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// 16-byte global -> shared copies that hold no registers while in flight
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 
 
 __device__ __forceinline__ void raise_status(const Args &a, unsigned code) {
@@ -281,52 +300,76 @@ __device__ __forceinline__ float sum8(const float (&r)[8]) {
     return s;
 }
 
+__device__ __forceinline__ RowAcc shfl_acc(const RowAcc &a, int src) {
+    RowAcc b;
+    b.M = __shfl_sync(kFull, a.M, src);
+    b.R = __shfl_sync(kFull, a.R, src);
+    b.T = __shfl_sync(kFull, a.T, src);
+    b.I = __shfl_sync(kFull, a.I, src);
+    return b;
+}
+
+// Merge the tile partials of every row of sequence b: whole rows at a time
+// are staged in the warp's shared buffer with asynchronous copies (all in
+// flight together, no registers held), then lane j folds target row j and
+// draft row j in tile order. nT <= kStage always (tiles hold >= 4096 of at
+// most 2^20 elements).
+__device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *buf, RowAcc &tr, RowAcc &dr) {
+    const int nT = a.nT;
+    const int rc = kStage / nT;                // whole rows per staging pass
+    const float4 *base = a.part + (size_t)b * a.rows * nT;
+    const int drow = a.nt_rows + l;            // row index of lane l's draft row
+    tr = acc_empty();
+    dr = acc_empty();
+    for (int r0 = 0; r0 < a.rows; r0 += rc) {
+        const int rn = min(rc, a.rows - r0);
+        const int cnt = rn * nT;
+        for (int i = l; i < cnt; i += 32) cp_async16(buf + i, base + (size_t)r0 * nT + i);
+        cp_async_wait_all();
+        __syncwarp();
+        const bool ht = l < a.nt_rows && l >= r0 && l < r0 + rn;
+        const bool hd = l < a.nd_rows && drow >= r0 && drow < r0 + rn;
+        const float4 *pt = buf + (l - r0) * nT;
+        const float4 *pd = buf + (drow - r0) * nT;
+        for (int t = 0; t < nT; ++t) {
+            if (ht) tr = acc_merge(tr, acc_unpack(pt[t]));
+            if (hd) dr = acc_merge(dr, acc_unpack(pd[t]));
+        }
+        __syncwarp();
+    }
+}
+
 // ---------------------------------------------------------------------------
-// Finalise sequence b with one warp: lane j merges the tile partials of
-// target row j and draft row j (ascending tiles), then the lanes apply the
-// mode's rule, write the per-position outputs and, in stochastic mode, publish
-// the draw of b for the residual units.
+// Finalise sequence b with one warp: the lanes merge the row partials (lane j
+// ends with target row j and draft row j), apply the mode's rule, write the
+// per-position outputs and, in stochastic mode, publish the draw of b for the
+// residual units.
 // ---------------------------------------------------------------------------
 template <typename T>
-__device__ __noinline__ void finalize(const Args &a, int b, int l) {
+__device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) {
     const int K = a.K;
     const float nan = __int_as_float(0x7fc00000);
     // loads that do not depend on the row statistics go out first: the draft
     // token, its uniform and the two logits it indexes
     const bool conf_only = a.mode == MODE_CONF;
+    const bool draw = a.mode == MODE_STOCHASTIC;   // the token at n comes from locate()
+    // the draw's slot is taken first; its value is needed only at the end
+    unsigned slot = 0u;
+    if (draw && l == kSig) slot = atomicAdd(a.ctr + CTR_RES_ALLOC, 1u);
     int xi = -1;
     bool bad_tok = false;
     float ui = 0.f, zx = 0.f, qx = 0.f;
+    if (draw && l <= K) ui = a.u[(size_t)b * (K + 1) + l];   // lane K: the residual / bonus uniform
     if (!conf_only && l < K) {
         xi = a.x[(size_t)b * K + l];
-        if (a.mode == MODE_STOCHASTIC) ui = a.u[(size_t)b * (K + 1) + l];
         bad_tok = xi < 0 || xi >= a.V;
         if (!bad_tok && a.nd_rows > 0) {
             zx = Elem<T>::load(trow_ptr<T>(a, b, l) + xi);
             qx = Elem<T>::load(drow_ptr<T>(a, b, l) + xi);
         }
     }
-    RowAcc tr = acc_empty(), dr = acc_empty();
-    {
-        // eight partials of each row in flight at a time, merged in tile order
-        const float4 *tp = a.part + ((size_t)b * a.rows + l) * a.nT;
-        const float4 *dp = a.part + ((size_t)b * a.rows + a.nt_rows + l) * a.nT;
-        const bool has_t = l < a.nt_rows, has_d = l < a.nd_rows;
-        for (int t0 = 0; t0 < a.nT; t0 += 8) {
-            float4 vt[8], vd[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const bool in = t0 + j < a.nT;
-                vt[j] = (has_t && in) ? __ldcg(tp + t0 + j) : acc_pack(acc_empty());
-                vd[j] = (has_d && in) ? __ldcg(dp + t0 + j) : acc_pack(acc_empty());
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                tr = acc_merge(tr, acc_unpack(vt[j]));
-                dr = acc_merge(dr, acc_unpack(vd[j]));
-            }
-        }
-    }
+    RowAcc tr, dr;
+    merge_rows(a, b, l, buf, tr, dr);
     float lse_t = nan, h = nan, lse_d = nan, f = nan, lr = nan;
     int amax_t = -1;
     bool bad_row = false;
@@ -394,20 +437,16 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l) {
     const float lt_n = __shfl_sync(kFull, lse_t, n);
     const float ld_n = __shfl_sync(kFull, lse_d, n);
     const int am_n = __shfl_sync(kFull, amax_t, n);
-    const bool draw = a.mode == MODE_STOCHASTIC;   // the token at n comes from locate()
-    for (int j = l; j <= K; j += 32) {
-        if (draw && j == n) continue;
-        a.out_tokens[(size_t)b * (K + 1) + j] = j < n ? a.x[(size_t)b * K + j] : (j == n ? am_n : -1);
-    }
+    const float u_draw = __shfl_sync(kFull, ui, K);
+    // K <= 31: lane j writes position j (lane j holds draft token j)
+    if (l <= K && !(draw && l == n)) a.out_tokens[(size_t)b * (K + 1) + l] = l < n ? xi : (l == n ? am_n : -1);
     if (l == kSig) {
         a.acc_len[b] = n;
         if (draw) {
-            // hand the draw to the residual units of b and publish them
-            const unsigned slot = atomicAdd(a.ctr + CTR_RES_ALLOC, 1u);
-            a.slotrec[slot] = make_float4(lt_n, ld_n, a.u[(size_t)b * (K + 1) + K], __int_as_float(b * 32 + n));
-            __threadfence();
+            // hand the draw to the residual units of b; the release store
+            // orders the record before the flag
+            a.slotrec[slot] = make_float4(lt_n, ld_n, u_draw, __int_as_float(b * 32 + n));
             st_release(a.res_ready + slot, 1u);
-            atomicAdd(a.ctr + CTR_RES_PUB, (unsigned)a.nR);
         }
     }
 }
@@ -419,57 +458,8 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l) {
 // v whose running sum in ascending v exceeds u * Z.
 // ---------------------------------------------------------------------------
 
-// Per-unit totals make the scan two-level: each residual unit stores its
-// slice sums and, in fp64, their sum in slice order; locate() scans the unit
-// totals, then the slices of one unit, then one slice.
-
-// lane-parallel fp64 inclusive scan over n (<= 32*per) values held
-// contiguously per lane; finds the first index whose running sum exceeds
-// `target`. Returns that index (or -1) and the running sum before it in *P.
-template <int kPer>
-__device__ __forceinline__ int scan_find(const double (&v)[kPer], int n, int l, double target, double base,
-                                         double *P) {
-    double seg = 0.0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) seg += (l * kPer + j < n) ? v[j] : 0.0;
-    const double incl = warp_incl_scan_d(seg, l) + base;
-    double c = incl - seg;
-    int found = -1;
-    double Pf = 0.0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        if (found < 0 && l * kPer + j < n) {
-            const double prev = c;
-            c += v[j];
-            if (c > target) {
-                found = l * kPer + j;
-                Pf = prev;
-            }
-        }
-    }
-    const unsigned m = __ballot_sync(kFull, found >= 0);
-    if (!m) return -1;
-    const int L = __ffs(m) - 1;
-    *P = __shfl_sync(kFull, Pf, L);
-    return __shfl_sync(kFull, found, L);
-}
-
-// the last index in [0, n) with a positive value, warp-wide (-1 if none)
-template <int kPer>
-__device__ __forceinline__ int last_positive(const double (&v)[kPer], int n, int l) {
-    int lm = -1;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-        if (l * kPer + j < n && v[j] > 0.0) lm = l * kPer + j;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(kFull, lm, o));
-    return lm;
-}
-
-constexpr int kUnitsPerLane = ((SPEC_MAX_V / kSlice + kResSlices - 1) / kResSlices + 31) / 32;  // unit totals per lane
-static_assert((SPEC_MAX_V / kSlice + kResSlices - 1) / kResSlices <= 32 * kUnitsPerLane,
-              "residual units per row exceed the locate scan");
-static_assert(kResSlices <= 32, "a residual unit's slices are scanned one per lane");
+// Each residual unit stores the fp32 sums of its slices; locate() scans all
+// slice sums of the sequence in fp64, then rescans one slice lane by lane.
 
 // Sum of slice s (elements 256s .. 256s+255) of the draw's weights, per lane
 // (8 elements each), in the fixed order every consumer of slice sums uses.
@@ -480,48 +470,95 @@ __device__ __forceinline__ float slice_lane_sum(const Args &a, const T *tr, cons
     return sum8(r);
 }
 
-// Locate the token of sequence b's draw from its unit totals (fp64) and slice
-// totals: Z is the sum of the unit totals; the scan picks the unit, then the
-// slice whose running sum first exceeds u*Z, then rescans that slice lane by
-// lane with an fp64 prefix. Returns the token, or -1 when Z is not positive
-// (only possible through rounding, or a bad row).
-template <typename T>
-__device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l) {
-    const double *ut = a.utot + (size_t)b * a.nR;
-    double v[kUnitsPerLane];
-#pragma unroll
-    for (int j = 0; j < kUnitsPerLane; ++j) {
-        const int i = l * kUnitsPerLane + j;
-        v[j] = i < a.nR ? __ldcg(ut + i) : 0.0;
-    }
+// Stage slice sums c0 .. c0 + 32*kScanPer - 1 of one sequence (row start
+// 16-byte aligned) in the warp's buffer; lane l then owns the contiguous run
+// l*kScanPer .. of the chunk. Entries past n are not staged and read as 0.
+__device__ __forceinline__ void stage_slices(const float *ss, int n, int c0, int l, float4 *buf) {
+    const int cn = min(4 * kStage, n - c0);
+    const float4 *src = reinterpret_cast<const float4 *>(ss + c0);
+    for (int i = l; i < (cn + 3) / 4; i += 32) cp_async16(buf + i, src + i);
+    cp_async_wait_all();
+    __syncwarp();
+}
+
+__device__ __forceinline__ float staged(const float4 *buf, int i, int cn) {
+    return i < cn ? reinterpret_cast<const float *>(buf)[i] : 0.f;
+}
+
+// fp64 sum of lane l's run of the staged chunk, in ascending order
+__device__ __forceinline__ double run_sum(const float4 *buf, int l, int cn) {
     double seg = 0.0;
-#pragma unroll
-    for (int j = 0; j < kUnitsPerLane; ++j) seg += v[j];
-    const double Z = __shfl_sync(kFull, warp_incl_scan_d(seg, l), 31);
+#pragma unroll 8
+    for (int j = 0; j < kScanPer; ++j) seg += (double)staged(buf, l * kScanPer + j, cn);
+    return seg;
+}
+
+// Locate the token of sequence b's draw from its slice sums: Z is their fp64
+// total; the scan picks the slice whose fp64 running sum first exceeds u*Z,
+// then rescans that slice lane by lane with an fp64 prefix. Returns the token,
+// or -1 when Z is not positive (only possible through rounding, or a bad row).
+template <typename T>
+__device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l, float4 *buf) {
+    const float *ss = a.slices + (size_t)b * a.sstride;
+    const int n = a.nslice;
+    constexpr int kChunk = 32 * kScanPer;
+    // pass 1: Z
+    double Z = 0.0;
+    for (int c0 = 0; c0 < n; c0 += kChunk) {
+        stage_slices(ss, n, c0, l, buf);
+        Z += warp_sum_d(run_sum(buf, l, n - c0));
+        __syncwarp();
+    }
     if (!(Z > 0.0)) return -1;
     const double target = (double)d.u * Z;
-    // nothing inside a fallback unit or slice may exceed the target: its last
-    // mass is taken
-    const double none = -2.0 * Z - 1.0;
-    double P = 0.0;
-    int unit = scan_find<kUnitsPerLane>(v, a.nR, l, target, 0.0, &P);
-    if (unit < 0) {
-        unit = last_positive<kUnitsPerLane>(v, a.nR, l);
-        if (unit < 0) return -1;
-        P = none;
+    // pass 2: the first slice whose running sum exceeds the target (a single
+    // chunk is still staged)
+    double P = 0.0;   // running sum before the current chunk
+    int entry = -1;
+    double P2 = 0.0;  // running sum before slice `entry`
+    for (int c0 = 0; c0 < n; c0 += kChunk) {
+        if (n > kChunk) stage_slices(ss, n, c0, l, buf);
+        const int cn = n - c0;
+        const double seg = run_sum(buf, l, cn);
+        const double incl = warp_incl_scan_d(seg, l) + P;
+        double c = incl - seg;
+        int found = -1;
+        double Pf = 0.0;
+        for (int j = 0; j < kScanPer; ++j) {
+            const double prev = c;
+            c += (double)staged(buf, l * kScanPer + j, cn);
+            if (c > target) {
+                found = c0 + l * kScanPer + j;
+                Pf = prev;
+                break;
+            }
+        }
+        const unsigned m = __ballot_sync(kFull, found >= 0);
+        if (n > kChunk) __syncwarp();
+        if (m) {
+            const int L = __ffs(m) - 1;
+            entry = __shfl_sync(kFull, found, L);
+            P2 = __shfl_sync(kFull, Pf, L);
+            break;
+        }
+        P = __shfl_sync(kFull, incl, 31);
     }
-    const int s0 = unit * kResSlices;
-    const int ns = min(kResSlices, a.nslice - s0);
-    double sv[1];
-    sv[0] = l < ns ? (double)__ldcg(a.slices + (size_t)b * a.nslice + s0 + l) : 0.0;
-    double P2 = 0.0;
-    int sl = scan_find<1>(sv, ns, l, target, P, &P2);
-    if (sl < 0) {
-        sl = last_positive<1>(sv, ns, l);
-        if (sl < 0) return -1;
-        P2 = none;
+    if (entry < 0) {
+        // rounding left the target at or above the total: the last positive
+        // mass is taken (nothing inside that slice may exceed the target)
+        for (int c0 = ((n - 1) / kChunk) * kChunk; c0 >= 0 && entry < 0; c0 -= kChunk) {
+            __syncwarp();
+            stage_slices(ss, n, c0, l, buf);
+            int lm = -1;
+            for (int j = 0; j < kScanPer; ++j)
+                if (staged(buf, l * kScanPer + j, n - c0) > 0.f) lm = l * kScanPer + j;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(kFull, lm, o));
+            if (lm >= 0) entry = c0 + lm;
+        }
+        if (entry < 0) return -1;
+        P2 = -2.0 * Z - 1.0;
     }
-    const int entry = s0 + sl;
     float r[8];
     const float s = slice_lane_sum<T>(a, tr, dr, entry, l, d.lse_t, d.lse_d, r);
     const double in = warp_incl_scan_d((double)s, l);
@@ -546,46 +583,107 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
     return __shfl_sync(kFull, entry * kSlice + L * 8 + tok, L);
 }
 
-// Residual unit t of sequence b: the sums of its slices of the draw's weights
-// (kResBatch slices' loads in flight at a time) and their fp64 total in slice
-// order.
-template <typename T>
-__device__ __forceinline__ void unit_sums(const Args &a, int b, int t, const T *tr, const T *dr, const Draw &d,
-                                          int l) {
-    double tot = 0.0;
-    for (int i0 = 0; i0 < kResSlices; i0 += kResBatch) {
-        float part[kResBatch];
+// Lane sums of kResBatch whole slices s0 .. of 16-byte aligned rows: every
+// load of the batch is issued before any arithmetic. Same per-lane order as
+// slice_lane_sum.
+template <typename T, bool kDraft>
+__device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int l, float lse_t, float lse_d,
+                                           float (&part)[kResBatch]) {
+    constexpr int E = Elem<T>::kPerVec;
+    constexpr int NV = 8 / E;   // 16-byte vectors per lane per slice per row
+    uint4 wt[kResBatch][NV], wd[kResBatch][kDraft ? NV : 1];
 #pragma unroll
-        for (int i = 0; i < kResBatch; ++i) {
-            float r[8];
-            part[i] = slice_lane_sum<T>(a, tr, dr, t * kResSlices + i0 + i, l, d.lse_t, d.lse_d, r);
-        }
+    for (int i = 0; i < kResBatch; ++i)
 #pragma unroll
-        for (int i = 0; i < kResBatch; ++i) {
-            const int sidx = t * kResSlices + i0 + i;
-            const float s = warp_sum_f(part[i]);
-            if (sidx < a.nslice) {
-                tot += (double)s;
-                if (l == kSig) a.slices[(size_t)b * a.nslice + sidx] = s;
+        for (int k = 0; k < NV; ++k) wt[i][k] = ldg_stream(tr + (s0 + i) * kSlice + l * 8 + k * E);
+    if constexpr (kDraft) {
+#pragma unroll
+        for (int i = 0; i < kResBatch; ++i)
+#pragma unroll
+            for (int k = 0; k < NV; ++k) wd[i][k] = ldg_stream(dr + (s0 + i) * kSlice + l * 8 + k * E);
+    }
+#pragma unroll
+    for (int i = 0; i < kResBatch; ++i) {
+        float r[8];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            float zt[E];
+            Elem<T>::unpack(wt[i][k], zt);
+            if constexpr (kDraft) {
+                float zd[E];
+                Elem<T>::unpack(wd[i][k], zd);
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const float p = ex2((zt[j] - lse_t) * kLog2e);
+                    const float q = ex2((zd[j] - lse_d) * kLog2e);
+                    r[k * E + j] = fmaxf(p - q, 0.f);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < E; ++j) r[k * E + j] = ex2((zt[j] - lse_t) * kLog2e);
             }
         }
+        part[i] = sum8(r);
     }
-    if (l == kSig) a.utot[(size_t)b * a.nR + t] = tot;
 }
 
-// The last residual unit of sequence b: locate its token. If the residual
-// mass vanished (only possible through rounding) the warp redraws from p.
+// Slices s0 .. s0 + res_slices<T>() - 1 of the draw's weights (kResBatch slices'
+// loads in flight at a time); lane kSig stores their sums.
 template <typename T>
-__device__ __noinline__ void locate(const Args &a, int b, const Draw &d, int l) {
+__device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T *tr, const T *dr, const Draw &d,
+                                          int l) {
+#pragma unroll
+    for (int i0 = 0; i0 < res_slices<T>(); i0 += kResBatch) {
+        float part[kResBatch];
+        const bool fast = a.t_vec_ok && (dr == nullptr || a.d_vec_ok) && (s0 + i0 + kResBatch) * kSlice <= a.V;
+        if (fast && dr) {
+            batch_fast<T, true>(tr, dr, s0 + i0, l, d.lse_t, d.lse_d, part);
+        } else if (fast) {
+            batch_fast<T, false>(tr, dr, s0 + i0, l, d.lse_t, d.lse_d, part);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kResBatch; ++i) {
+                float r[8];
+                part[i] = slice_lane_sum<T>(a, tr, dr, s0 + i0 + i, l, d.lse_t, d.lse_d, r);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kResBatch; ++i) {
+            const int sidx = s0 + i0 + i;
+            const float s = warp_sum_f(part[i]);
+            if (l == kSig && sidx < a.nslice) a.slices[(size_t)b * a.sstride + sidx] = s;
+        }
+    }
+}
+
+__device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
+    const float4 rec = __ldcg(a.slotrec + slot);
+    const int bits = __float_as_int(rec.w);
+    b = bits >> 5;
+    Draw d;
+    d.lse_t = rec.x;
+    d.lse_d = rec.y;
+    d.u = rec.z;
+    d.n = bits & 31;
+    return d;
+}
+
+// The last residual unit of the sequence in `slot` completed: locate its
+// token. If the residual mass vanished (only possible through rounding) the
+// warp redraws from p.
+template <typename T>
+__device__ __noinline__ void locate(const Args &a, int slot, int l, float4 *buf) {
+    int b;
+    const Draw d = decode_slot(a, slot, b);
     const int K = a.K;
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.n < K ? drow_ptr<T>(a, b, d.n) : nullptr;
-    int token = locate_scan<T>(a, b, tr, dr, d, l);
+    int token = locate_scan<T>(a, b, tr, dr, d, l, buf);
     if (token < 0 && dr != nullptr) {
-        for (int t = 0; t < a.nR; ++t) unit_sums<T>(a, b, t, tr, nullptr, d, l);
-        __threadfence_block();
+        for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T>(a, b, s0, tr, nullptr, d, l);
+        __threadfence();
         __syncwarp();
-        token = locate_scan<T>(a, b, tr, nullptr, d, l);
+        token = locate_scan<T>(a, b, tr, nullptr, d, l, buf);
     }
     if (token < 0) {
         if (l == 0) raise_status(a, SPEC_ERR_BAD_ROW);
@@ -594,66 +692,69 @@ __device__ __noinline__ void locate(const Args &a, int b, const Draw &d, int l) 
     if (l == 0) a.out_tokens[(size_t)b * (K + 1) + d.n] = token;
 }
 
-// One residual unit of the sequence published in `slot`. Its record holds
-// (lse_t, lse_d, u, 32*b + n). The last unit of the sequence locates its token.
+// One residual unit: part t of the sequence published in slot id / nR. Lane
+// kSig stores the slice sums and release-increments the sequence's residual
+// counter; the returned count (lane kSig) says whether this was its last unit.
+struct ResDone {
+    int slot;
+    unsigned old;
+};
+
 template <typename T>
-__device__ __noinline__ void residual_unit(const Args &a, unsigned id, int l) {
+__device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l) {
     const int slot = (int)(id / (unsigned)a.nR);
     const int t = (int)(id - (unsigned)slot * (unsigned)a.nR);
-    const float4 rec = __ldcg(a.slotrec + slot);
-    const int bits = __float_as_int(rec.w);
-    const int b = bits >> 5;
-    Draw d;
-    d.lse_t = rec.x;
-    d.lse_d = rec.y;
-    d.u = rec.z;
-    d.n = bits & 31;
+    int b;
+    const Draw d = decode_slot(a, slot, b);
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.n < a.K ? drow_ptr<T>(a, b, d.n) : nullptr;
-    unit_sums<T>(a, b, t, tr, dr, d, l);
-    bool last = false;
-    if (l == kSig) last = atom_add_release(a.res_done + b, 1u) == (unsigned)a.nR - 1;
-    last = __shfl_sync(kFull, last, kSig);
-    if (last) {
-        fence_acquire();
-        locate<T>(a, b, d, l);
-    }
+    unit_sums<T>(a, b, t * res_slices<T>(), tr, dr, d, l);
+    ResDone r;
+    r.slot = slot;
+    r.old = 0u;
+    if (l == kSig) r.old = atom_add_release(a.res_done + b, 1u);
+    return r;
 }
 
 // ---------------------------------------------------------------------------
-// Scheduling, per warp (lane 0 keeps the state). Stream units come first, in
-// sequence-major order, one atomicAdd each, prefetched one job ahead. Once the
-// stream queue is empty the warp turns to residual units: claimed with
-// atomicAdd in publication order (a CAS loop would serialise the GPU on one
-// counter), each run once its sequence is published. A warp waits only when it
-// holds no stream unit and has completed everything it streamed; every
-// publication depends only on stream units held by running warps, which never
-// wait, so each wait ends.
+// Scheduling, per warp (lane 0 keeps the state). Nothing on the stream path
+// waits for a reply:
+//
+//  * Stream units come in sequence-major order, one atomicAdd each, claimed
+//    one unit ahead.
+//  * Residual units are taken once the stream queue is empty: claimed with
+//    atomicAdd in publication order and run when their sequence's draw is
+//    published, polled with a short backoff (bounded; SPEC_ERR_TIMEOUT). Run
+//    together at the end, they stream the stop rows at full bandwidth; mixed
+//    into the stream phase they cost more than they save.
+//
+// A warp waits only when it holds no stream unit and has resolved every
+// completion it owes; each publication depends only on stream units held by
+// running warps, which never wait, so every wait ends.
 // ---------------------------------------------------------------------------
 struct Sched {
-    unsigned next_stream;   // prefetched stream unit (>= units: none left)
-    unsigned pend;          // claimed residual unit not yet run (kNone: none)
+    unsigned ns;       // claimed next stream unit (>= units: none left)
+    unsigned pend;     // claimed residual unit (kNone: none)
 };
 constexpr unsigned kNone = 0xffffffffu;
 
 enum { JOB_DONE = 0, JOB_STREAM = 1, JOB_RESIDUAL = 2, JOB_WAIT = 3 };
 
-// lane 0: the next job that can start now; JOB_WAIT when the only work left
-// is residual work that is not published yet (see wait_job).
+// lane 0: the next job that can start now; JOB_WAIT when no stream unit is
+// left and residual work remains (see wait_job).
 __device__ __forceinline__ int next_job(const Args &a, Sched &q, unsigned &id) {
-    if (q.next_stream < a.units) {
-        id = q.next_stream;
-        q.next_stream = atomicAdd(a.ctr + CTR_CLAIM, 1u);
+    if (q.ns < a.units) {
+        id = q.ns;
+        q.ns = atomicAdd(a.ctr + CTR_CLAIM, 1u);
         return JOB_STREAM;
     }
     return a.res_units ? JOB_WAIT : JOB_DONE;
 }
 
-// lane 0: wait for a residual unit. Called only when the warp holds no stream
-// unit and has completed every unit it streamed, so the sequences it waits for
-// depend only on other warps' units, none of which waits.
+// lane 0: wait for a residual unit that can run. Called only when no stream
+// unit is left and the warp has resolved every completion it owes.
 __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
-    unsigned ns = 64;
+    unsigned ns = 32;
     for (unsigned it = 0; it < kSpinLimit; ++it) {
         if (q.pend == kNone) {
             if (ld_relaxed(a.ctr + CTR_RES_CLAIM) >= a.res_units) return JOB_DONE;
@@ -662,13 +763,13 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
             q.pend = c;
         }
         if (ld_relaxed(a.res_ready + q.pend / (unsigned)a.nR)) {
+            fence_acquire();
             id = q.pend;
             q.pend = kNone;
-            fence_acquire();
             return JOB_RESIDUAL;
         }
         __nanosleep(ns);
-        ns = min(ns * 2u, 2048u);
+        ns = min(ns * 2u, 256u);
     }
     raise_status(a, SPEC_ERR_TIMEOUT);
     return JOB_DONE;
@@ -676,36 +777,43 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
 
 // ---------------------------------------------------------------------------
 // The persistent kernel: every warp is an independent worker (no block-wide
-// barrier anywhere, no shared memory).
+// barrier anywhere; shared memory only as each warp's own staging buffer).
 // ---------------------------------------------------------------------------
+enum { DUE_NONE = 0, DUE_STREAM = 1, DUE_RESIDUAL = 2 };
+
 template <typename T>
 __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a) {
     const int l = threadIdx.x & 31;
     const unsigned per_seq = (unsigned)a.rows * (unsigned)a.nT;
+    __shared__ float4 s_stage[NWARP][kStage];   // per-warp staging for finalize and locate
+    float4 *const wbuf = s_stage[threadIdx.x >> 5];
     Sched q;
     q.pend = kNone;
-    q.next_stream = 0u;
-    if (l == 0) q.next_stream = atomicAdd(a.ctr + CTR_CLAIM, 1u);
-    // Completion of a stream unit: its partial and a release-increment of the
-    // sequence's counter go out at once, but the returned count (is this the
-    // sequence's last unit?) is read only after the next unit, so the warp
-    // does not stall on the atomic. The check is always made before the warp
-    // waits or takes other work.
-    int dprev_b = -1;            // sequence of the unit whose count is pending
-    unsigned dprev_old = 0u;     // that count (lane kSig)
+    q.ns = 0u;
+    if (l == 0) q.ns = atomicAdd(a.ctr + CTR_CLAIM, 1u);
+    // A completed unit's result and a release-increment of its sequence's
+    // counter go out at once, but the returned count (was this the last
+    // unit?) is read only at the next boundary, or after the next stream unit
+    // has published its own completion, so the warp neither stalls on the
+    // atomic nor holds back its next unit's completion behind a finalize. The
+    // finalize or locate it may owe is always done before the warp waits.
+    int due = DUE_NONE;
+    int due_id = 0;           // sequence (stream) or slot (residual)
+    unsigned due_old = 0u;    // the count returned to lane kSig
     for (;;) {
         int kind = 0;
         unsigned unit = 0;
         if (l == 0) kind = next_job(a, q, unit);
         kind = __shfl_sync(kFull, kind, 0);
         unit = __shfl_sync(kFull, unit, 0);
-        if (kind != JOB_STREAM && dprev_b >= 0) {
-            const bool last = __shfl_sync(kFull, dprev_old == per_seq - 1, kSig);
-            if (last) {
+        if (kind != JOB_STREAM && due != DUE_NONE) {
+            const unsigned need = due == DUE_STREAM ? per_seq - 1u : (unsigned)a.nR - 1u;
+            if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
-                finalize<T>(a, dprev_b, l);
+                if (due == DUE_STREAM) finalize<T>(a, due_id, l, wbuf);
+                else locate<T>(a, due_id, l, wbuf);
             }
-            dprev_b = -1;
+            due = DUE_NONE;
         }
         if (kind == JOB_WAIT) {
             if (l == 0) kind = wait_job(a, q, unit);
@@ -714,25 +822,34 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         }
         if (kind == JOB_DONE) break;
         if (kind == JOB_RESIDUAL) {
-            residual_unit<T>(a, unit, l);
+            const ResDone r = residual_unit<T>(a, unit, l);
+            due = DUE_RESIDUAL;
+            due_id = r.slot;
+            due_old = r.old;
             continue;
         }
         const UnitGeo<T> g = unit_geo<T>(a, unit, per_seq);
         // target rows also carry the entropy moment; draft rows do not need it
         const RowAcc s = g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l);
-        if (dprev_b >= 0) {
-            const bool last = __shfl_sync(kFull, dprev_old == per_seq - 1, kSig);
-            if (last) {
-                fence_acquire();
-                finalize<T>(a, dprev_b, l);
-            }
-        }
         const int b = (int)(unit / per_seq);
+        unsigned old = 0u;
         if (l == kSig) {
             a.part[unit] = acc_pack(s);
-            dprev_old = atom_add_release(a.seq_done + b, 1u);
+            old = atom_add_release(a.seq_done + b, 1u);
         }
-        dprev_b = b;
+        // this unit's completion is out; now the previous one, whose count
+        // has had a whole unit to come back
+        if (due != DUE_NONE) {
+            const unsigned need = due == DUE_STREAM ? per_seq - 1u : (unsigned)a.nR - 1u;
+            if (__shfl_sync(kFull, due_old == need, kSig)) {
+                fence_acquire();
+                if (due == DUE_STREAM) finalize<T>(a, due_id, l, wbuf);
+                else locate<T>(a, due_id, l, wbuf);
+            }
+        }
+        due = DUE_STREAM;
+        due_id = b;
+        due_old = old;
     }
 }
 
@@ -754,9 +871,9 @@ static int fail(int code, const char *fmt, ...) {
 }
 
 struct Plan {
-    int nT, TS, nR, nslice;
+    int nT, TS, nR, nslice, sstride;
     unsigned long long units;
-    size_t seq_off, ready_off, done_off, rec_off, utot_off, part_off, slice_off;
+    size_t seq_off, ready_off, done_off, rec_off, part_off, slice_off;
     size_t zero_bytes, bytes;
 };
 
@@ -783,14 +900,16 @@ static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
     p.nT = nT;
     p.TS = TS;
     p.nslice = (V + kSlice - 1) / kSlice;
-    p.nR = (p.nslice + kResSlices - 1) / kResSlices;
+    p.sstride = (p.nslice + 3) & ~3;
+    const int rs = esize == 2 ? res_slices<__nv_bfloat16>() : res_slices<float>();
+    p.nR = (p.nslice + rs - 1) / rs;
 }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace: [header words | seq_done[B] | res_ready[B] | res_done[B]] (zeroed
-// per call) [slot records B | unit totals B*nR | tile partials B*rows*nT |
-// slices B*nslice]
+// per call) [slot records B | tile partials B*rows*nT |
+// slices B*sstride]
 static void plan_workspace(int B, int rows, int V, int esize, Plan &p) {
     plan_tiles(B, rows, V, esize, p);
     p.seq_off = kHeaderWords * sizeof(unsigned);
@@ -798,10 +917,9 @@ static void plan_workspace(int B, int rows, int V, int esize, Plan &p) {
     p.done_off = p.ready_off + (size_t)B * sizeof(unsigned);
     p.zero_bytes = p.done_off + (size_t)B * sizeof(unsigned);
     p.rec_off = align_up(p.zero_bytes, 16);
-    p.utot_off = align_up(p.rec_off + (size_t)B * sizeof(float4), 16);
-    p.part_off = align_up(p.utot_off + (size_t)B * p.nR * sizeof(double), 16);
+    p.part_off = align_up(p.rec_off + (size_t)B * sizeof(float4), 16);
     p.slice_off = align_up(p.part_off + (size_t)B * rows * p.nT * sizeof(float4), 16);
-    p.bytes = align_up(p.slice_off + (size_t)B * p.nslice * sizeof(float), 16);
+    p.bytes = align_up(p.slice_off + (size_t)B * p.sstride * sizeof(float), 16);
     p.units = (unsigned long long)B * rows * p.nT;
 }
 
@@ -853,13 +971,15 @@ static int launch(Args &a, const Plan &p, int dtype, void *ws, void *stream) {
     a.res_ready = reinterpret_cast<unsigned *>(base + p.ready_off);
     a.res_done = reinterpret_cast<unsigned *>(base + p.done_off);
     a.slotrec = reinterpret_cast<float4 *>(base + p.rec_off);
-    a.utot = reinterpret_cast<double *>(base + p.utot_off);
     a.part = reinterpret_cast<float4 *>(base + p.part_off);
     a.slices = reinterpret_cast<float *>(base + p.slice_off);
     a.nT = p.nT;
+    a.gsh = 0;
+    while ((1 << a.gsh) < p.nT && a.gsh < 5) ++a.gsh;
     a.TS = p.TS;
     a.nR = p.nR;
     a.nslice = p.nslice;
+    a.sstride = p.sstride;
     a.units = (unsigned)p.units;
     a.res_units = a.mode == MODE_STOCHASTIC ? (unsigned)a.B * (unsigned)p.nR : 0u;
     a.inv_log_v = (float)(1.0 / std::log((double)a.V));
