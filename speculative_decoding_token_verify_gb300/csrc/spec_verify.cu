@@ -114,14 +114,14 @@ struct Args {
     int nd_rows;             // draft rows streamed per sequence (K or 0)
     int rows;
     int nT;                  // tiles per row
-    int gsh;                 // log2 of the lane-group size that merges one row's partials
     int TS;                  // tile size (elements, multiple of 8)
-    unsigned units;          // B * rows * nT
+    unsigned per_seq;        // stream units per sequence (rows * nT)
+    unsigned units;          // B * per_seq
     int t_vec_ok, d_vec_ok;  // rows start on 16-byte boundaries
     float inv_log_v;         // 1 / ln V
     unsigned *ctr;           // header words
     unsigned *seq_done;      // [B] completed units per sequence
-    float4 *part;            // [B][rows][nT] tile partials
+    float4 *part;            // [B][rows][nT] tile partials, one per stream unit
     unsigned res_units;      // B * nR in stochastic mode, else 0
     int nR;                  // residual units per sequence
     int nslice;              // scan slices per row
@@ -207,22 +207,25 @@ __device__ __forceinline__ double warp_incl_scan_d(double v, int l) {
 template <typename T>
 struct UnitGeo {
     const T *row;
+    int b;            // sequence
     int v0, vb, head, ve, tail;
     unsigned bytes;   // body bytes (a multiple of 16)
     bool target;      // a target row (carries the entropy moment)
 };
 
 template <typename T>
-__device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit, unsigned per_seq) {
+__device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit) {
     UnitGeo<T> g;
-    const int b = (int)(unit / per_seq);
-    const unsigned rem = unit - (unsigned)b * per_seq;
+    const int b = (int)(unit / a.per_seq);
+    const unsigned rem = unit - (unsigned)b * a.per_seq;
     const int r = (int)(rem / (unsigned)a.nT);
     const int t = (int)(rem - (unsigned)r * (unsigned)a.nT);
+    const int TS = a.TS;
+    g.b = b;
     g.target = r < a.nt_rows;
     g.row = g.target ? trow_ptr<T>(a, b, r) : drow_ptr<T>(a, b, r - a.nt_rows);
-    g.v0 = t * a.TS;
-    const int v1 = min(a.V, g.v0 + a.TS);
+    g.v0 = t * TS;
+    const int v1 = min(a.V, g.v0 + TS);
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(g.row + g.v0);
     int head = (int)(((16u - (unsigned)(a0 & 15u)) & 15u) / sizeof(T));
     if (head > v1 - g.v0) head = v1 - g.v0;
@@ -311,13 +314,15 @@ __device__ __forceinline__ RowAcc shfl_acc(const RowAcc &a, int src) {
 
 // Merge the tile partials of every row of sequence b: whole rows at a time
 // are staged in the warp's shared buffer with asynchronous copies (all in
-// flight together, no registers held), then lane j folds target row j and
-// draft row j in tile order. nT <= kStage always (tiles hold >= 4096 of at
-// most 2^20 elements).
+// flight together, no registers held). Each staged row gets L lanes (the
+// largest power of two that fits): lane i of a row folds a contiguous run of
+// its tiles in order, then the L lanes merge by butterfly, a fixed tree. Lane
+// j ends with target row j in tr and draft row j in dr. nT <= kStage always
+// (tiles hold >= 4096 of at most 2^20 elements).
 __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *buf, RowAcc &tr, RowAcc &dr) {
     const int nT = a.nT;
-    const int rc = kStage / nT;                // whole rows per staging pass
-    const float4 *base = a.part + (size_t)b * a.rows * nT;
+    const int rc = min(kStage / nT, 32);       // whole rows per staging pass, one lane each at least
+    const float4 *base = a.part + (size_t)b * a.per_seq;
     const int drow = a.nt_rows + l;            // row index of lane l's draft row
     tr = acc_empty();
     dr = acc_empty();
@@ -327,14 +332,22 @@ __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *
         for (int i = l; i < cnt; i += 32) cp_async16(buf + i, base + (size_t)r0 * nT + i);
         cp_async_wait_all();
         __syncwarp();
-        const bool ht = l < a.nt_rows && l >= r0 && l < r0 + rn;
-        const bool hd = l < a.nd_rows && drow >= r0 && drow < r0 + rn;
-        const float4 *pt = buf + (l - r0) * nT;
-        const float4 *pd = buf + (drow - r0) * nT;
-        for (int t = 0; t < nT; ++t) {
-            if (ht) tr = acc_merge(tr, acc_unpack(pt[t]));
-            if (hd) dr = acc_merge(dr, acc_unpack(pd[t]));
+        int lsh = 0;
+        while (lsh < 5 && (rn << (lsh + 1)) <= 32) ++lsh;
+        const int ri = l >> lsh, sub = l & ((1 << lsh) - 1);
+        const int run = (nT + (1 << lsh) - 1) >> lsh;
+        RowAcc acc = acc_empty();
+        if (ri < rn) {
+            const float4 *pr = buf + ri * nT;
+            const int t1 = min(nT, (sub + 1) * run);
+            for (int t = sub * run; t < t1; ++t) acc = acc_merge(acc, acc_unpack(pr[t]));
         }
+        for (int o = 1; o < (1 << lsh); o <<= 1) acc = acc_merge(acc, shfl_xor_acc(acc, o));
+        // row r0 + i now sits in lane i * L
+        const RowAcc st = shfl_acc(acc, (int)(((unsigned)(l - r0) << lsh) & 31u));
+        const RowAcc sd = shfl_acc(acc, (int)(((unsigned)(drow - r0) << lsh) & 31u));
+        if (l < a.nt_rows && l >= r0 && l < r0 + rn) tr = st;
+        if (l < a.nd_rows && drow >= r0 && drow < r0 + rn) dr = sd;
         __syncwarp();
     }
 }
@@ -485,18 +498,20 @@ __device__ __forceinline__ float staged(const float4 *buf, int i, int cn) {
     return i < cn ? reinterpret_cast<const float *>(buf)[i] : 0.f;
 }
 
-// fp64 sum of lane l's run of the staged chunk, in ascending order
-__device__ __forceinline__ double run_sum(const float4 *buf, int l, int cn) {
-    double seg = 0.0;
+// fp32 sum of lane l's run of the staged chunk, in ascending order (at most
+// kScanPer terms: relative error below 2e-6 of the run, so below 2e-6 of Z)
+__device__ __forceinline__ float run_sum(const float4 *buf, int l, int cn) {
+    float seg = 0.f;
 #pragma unroll 8
-    for (int j = 0; j < kScanPer; ++j) seg += (double)staged(buf, l * kScanPer + j, cn);
+    for (int j = 0; j < kScanPer; ++j) seg += staged(buf, l * kScanPer + j, cn);
     return seg;
 }
 
-// Locate the token of sequence b's draw from its slice sums: Z is their fp64
-// total; the scan picks the slice whose fp64 running sum first exceeds u*Z,
-// then rescans that slice lane by lane with an fp64 prefix. Returns the token,
-// or -1 when Z is not positive (only possible through rounding, or a bad row).
+// Locate the token of sequence b's draw from its slice sums: Z is their total
+// (fp32 within a lane's run, fp64 across runs); the scan picks the slice whose
+// running sum first exceeds u*Z, then rescans that slice lane by lane with an
+// fp64 prefix across lanes. Returns the token, or -1 when Z is not positive
+// (only possible through rounding, or a bad row).
 template <typename T>
 __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l, float4 *buf) {
     const float *ss = a.slices + (size_t)b * a.sstride;
@@ -506,7 +521,7 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
     double Z = 0.0;
     for (int c0 = 0; c0 < n; c0 += kChunk) {
         stage_slices(ss, n, c0, l, buf);
-        Z += warp_sum_d(run_sum(buf, l, n - c0));
+        Z += warp_sum_d((double)run_sum(buf, l, n - c0));
         __syncwarp();
     }
     if (!(Z > 0.0)) return -1;
@@ -519,17 +534,20 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
     for (int c0 = 0; c0 < n; c0 += kChunk) {
         if (n > kChunk) stage_slices(ss, n, c0, l, buf);
         const int cn = n - c0;
-        const double seg = run_sum(buf, l, cn);
-        const double incl = warp_incl_scan_d(seg, l) + P;
-        double c = incl - seg;
+        const float segf = run_sum(buf, l, cn);
+        const double incl = warp_incl_scan_d((double)segf, l) + P;
+        const double excl = incl - (double)segf;
+        // walk the run in fp32, relative to its start
+        const float rel = (float)(target - excl);
+        float c = 0.f;
         int found = -1;
         double Pf = 0.0;
         for (int j = 0; j < kScanPer; ++j) {
-            const double prev = c;
-            c += (double)staged(buf, l * kScanPer + j, cn);
-            if (c > target) {
+            const float prev = c;
+            c += staged(buf, l * kScanPer + j, cn);
+            if (c > rel) {
                 found = c0 + l * kScanPer + j;
-                Pf = prev;
+                Pf = excl + (double)prev;
                 break;
             }
         }
@@ -572,12 +590,13 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
         L = nz ? 31 - __clz(nz) : 0;
     }
     int tok = -1, lastpos = -1;
-    double cc = P2 + ex;
+    const float rel = (float)(target - (P2 + ex));
+    float cc = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if (r[j] > 0.f) lastpos = j;
-        cc += (double)r[j];
-        if (tok < 0 && cc > target) tok = j;
+        cc += r[j];
+        if (tok < 0 && cc > rel) tok = j;
     }
     if (tok < 0) tok = lastpos >= 0 ? lastpos : 0;
     return __shfl_sync(kFull, entry * kSlice + L * 8 + tok, L);
@@ -784,7 +803,6 @@ enum { DUE_NONE = 0, DUE_STREAM = 1, DUE_RESIDUAL = 2 };
 template <typename T>
 __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a) {
     const int l = threadIdx.x & 31;
-    const unsigned per_seq = (unsigned)a.rows * (unsigned)a.nT;
     __shared__ float4 s_stage[NWARP][kStage];   // per-warp staging for finalize and locate
     float4 *const wbuf = s_stage[threadIdx.x >> 5];
     Sched q;
@@ -807,7 +825,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         kind = __shfl_sync(kFull, kind, 0);
         unit = __shfl_sync(kFull, unit, 0);
         if (kind != JOB_STREAM && due != DUE_NONE) {
-            const unsigned need = due == DUE_STREAM ? per_seq - 1u : (unsigned)a.nR - 1u;
+            const unsigned need = due == DUE_STREAM ? a.per_seq - 1u : (unsigned)a.nR - 1u;
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
                 if (due == DUE_STREAM) finalize<T>(a, due_id, l, wbuf);
@@ -828,10 +846,10 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             due_old = r.old;
             continue;
         }
-        const UnitGeo<T> g = unit_geo<T>(a, unit, per_seq);
+        const UnitGeo<T> g = unit_geo<T>(a, unit);
         // target rows also carry the entropy moment; draft rows do not need it
         const RowAcc s = g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l);
-        const int b = (int)(unit / per_seq);
+        const int b = g.b;
         unsigned old = 0u;
         if (l == kSig) {
             a.part[unit] = acc_pack(s);
@@ -840,7 +858,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         // this unit's completion is out; now the previous one, whose count
         // has had a whole unit to come back
         if (due != DUE_NONE) {
-            const unsigned need = due == DUE_STREAM ? per_seq - 1u : (unsigned)a.nR - 1u;
+            const unsigned need = due == DUE_STREAM ? a.per_seq - 1u : (unsigned)a.nR - 1u;
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
                 if (due == DUE_STREAM) finalize<T>(a, due_id, l, wbuf);
@@ -872,7 +890,7 @@ static int fail(int code, const char *fmt, ...) {
 
 struct Plan {
     int nT, TS, nR, nslice, sstride;
-    unsigned long long units;
+    unsigned long long units;       // stream units: B * rows * nT
     size_t seq_off, ready_off, done_off, rec_off, part_off, slice_off;
     size_t zero_bytes, bytes;
 };
@@ -880,25 +898,31 @@ struct Plan {
 #ifndef SV_MIN_TILE
 #define SV_MIN_TILE 4096
 #endif
+// nT tiles of a row of V elements, rounded to a tile size that is a multiple of 8
+static void split_row(int V, long long want, int &nT, int &TS) {
+    if (want < 1) want = 1;
+    TS = (int)((V + want - 1) / want);
+    TS = (TS + 7) & ~7;
+    nT = (V + TS - 1) / TS;
+}
 
 // A stream unit is one warp's share: a tile of at most SV_TILE_BYTES of
 // logits. Small batches split rows further, down to SV_MIN_TILE elements,
 // aiming at ~32K units (about 7 per resident warp of a GB300) so that the
-// queue's tail stays short.
+// queue's tail stays short. (Finer tiles for just the queue's tail were
+// measured and lost: they lengthen the finalize of exactly the sequences
+// that end the launch.)
 static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
     const int ts_max = SV_TILE_BYTES / esize;
-    int nT = (V + ts_max - 1) / ts_max;
     const long long rows_total = (long long)B * rows;
+    long long cap = V / SV_MIN_TILE;
+    if (cap < 1) cap = 1;
+    long long n = (V + ts_max - 1) / ts_max;
     long long want = (32768 + rows_total - 1) / rows_total;
-    const long long cap = V / SV_MIN_TILE;
     if (want > cap) want = cap;
-    if (want > nT) nT = (int)want;
-    if (nT < 1) nT = 1;
-    int TS = (V + nT - 1) / nT;
-    TS = (TS + 7) & ~7;
-    nT = (V + TS - 1) / TS;
-    p.nT = nT;
-    p.TS = TS;
+    if (want > n) n = want;
+    split_row(V, n, p.nT, p.TS);
+    p.units = (unsigned long long)B * rows * p.nT;
     p.nslice = (V + kSlice - 1) / kSlice;
     p.sstride = (p.nslice + 3) & ~3;
     const int rs = esize == 2 ? res_slices<__nv_bfloat16>() : res_slices<float>();
@@ -908,19 +932,22 @@ static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace: [header words | seq_done[B] | res_ready[B] | res_done[B]] (zeroed
-// per call) [slot records B | tile partials B*rows*nT |
-// slices B*sstride]
-static void plan_workspace(int B, int rows, int V, int esize, Plan &p) {
-    plan_tiles(B, rows, V, esize, p);
+// per call) [slot records B | tile partials | slices B*sstride]. The
+// partials hold one slot per stream unit of the largest plan among the row
+// counts the call may stream (`rows_a`, `rows_b`).
+static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan &p) {
+    Plan q;
+    plan_tiles(B, rows_b, V, esize, q);
+    plan_tiles(B, rows_a, V, esize, p);
+    const unsigned long long cap = p.units > q.units ? p.units : q.units;
     p.seq_off = kHeaderWords * sizeof(unsigned);
     p.ready_off = p.seq_off + (size_t)B * sizeof(unsigned);
     p.done_off = p.ready_off + (size_t)B * sizeof(unsigned);
     p.zero_bytes = p.done_off + (size_t)B * sizeof(unsigned);
     p.rec_off = align_up(p.zero_bytes, 16);
     p.part_off = align_up(p.rec_off + (size_t)B * sizeof(float4), 16);
-    p.slice_off = align_up(p.part_off + (size_t)B * rows * p.nT * sizeof(float4), 16);
+    p.slice_off = align_up(p.part_off + (size_t)cap * sizeof(float4), 16);
     p.bytes = align_up(p.slice_off + (size_t)B * p.sstride * sizeof(float), 16);
-    p.units = (unsigned long long)B * rows * p.nT;
 }
 
 struct DevInfo {
@@ -974,9 +1001,8 @@ static int launch(Args &a, const Plan &p, int dtype, void *ws, void *stream) {
     a.part = reinterpret_cast<float4 *>(base + p.part_off);
     a.slices = reinterpret_cast<float *>(base + p.slice_off);
     a.nT = p.nT;
-    a.gsh = 0;
-    while ((1 << a.gsh) < p.nT && a.gsh < 5) ++a.gsh;
     a.TS = p.TS;
+    a.per_seq = (unsigned)a.rows * (unsigned)p.nT;
     a.nR = p.nR;
     a.nslice = p.nslice;
     a.sstride = p.sstride;
@@ -1002,10 +1028,11 @@ static int check_common(int B, int K, int V, int dtype) {
     if (K < 1 || K > SPEC_MAX_K) return fail(SPEC_ERR_UNSUPPORTED, "K must be in [1, %d] (got %d)", SPEC_MAX_K, K);
     if (V < 2 || V > SPEC_MAX_V) return fail(SPEC_ERR_UNSUPPORTED, "V must be in [2, %d] (got %d)", SPEC_MAX_V, V);
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_UNSUPPORTED, "unknown dtype %d", dtype);
-    Plan pl;
-    plan_tiles(B, 2 * K + 1, V, dtype == SPEC_BF16 ? 2 : 4, pl);
-    if ((unsigned long long)B * (2 * K + 1) * (unsigned long long)pl.nT >= (1ull << 31))
-        return fail(SPEC_ERR_UNSUPPORTED, "batch too large (B=%d)", B);
+    for (int rows : {K, K + 1, 2 * K + 1}) {
+        Plan pl;
+        plan_tiles(B, rows, V, dtype == SPEC_BF16 ? 2 : 4, pl);
+        if (pl.units >= (1ull << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large (B=%d)", B);
+    }
     return SPEC_OK;
 }
 
@@ -1048,14 +1075,14 @@ size_t spec_workspace_size(const spec_verify_params *p) {
     if (!p) return 0;
     if (check_common(p->B, p->K, p->V, p->dtype) != SPEC_OK) return 0;
     Plan pl;
-    plan_workspace(p->B, 2 * p->K + 1, p->V, p->dtype == SPEC_BF16 ? 2 : 4, pl);
+    plan_workspace(p->B, 2 * p->K + 1, p->K + 1, p->V, p->dtype == SPEC_BF16 ? 2 : 4, pl);
     return pl.bytes;
 }
 
 size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype) {
     if (check_common(B, K, V, dtype) != SPEC_OK) return 0;
     Plan pl;
-    plan_workspace(B, K, V, dtype == SPEC_BF16 ? 2 : 4, pl);
+    plan_workspace(B, K, K, V, dtype == SPEC_BF16 ? 2 : 4, pl);
     return pl.bytes;
 }
 
@@ -1088,8 +1115,11 @@ int spec_verify(const spec_verify_params *p, const void *target_logits, const vo
         return fail(SPEC_ERR_INVALID_ARG, "logit pointers must be aligned to the element size");
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16u) != 0)
         return fail(SPEC_ERR_INVALID_ARG, "workspace must be a 16-byte aligned device pointer");
+    // the tiling follows the rows actually streamed; the layout has room for
+    // either row count, so spec_workspace_size covers both
+    const int rows = draft_logits ? 2 * p->K + 1 : p->K + 1;
     Plan pl;
-    plan_workspace(p->B, 2 * p->K + 1, p->V, es, pl);
+    plan_workspace(p->B, rows, draft_logits ? p->K + 1 : 2 * p->K + 1, p->V, es, pl);
     if (workspace_bytes < pl.bytes)
         return fail(SPEC_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, pl.bytes);
 
@@ -1118,9 +1148,6 @@ int spec_verify(const spec_verify_params *p, const void *target_logits, const vo
     a.rows = a.nt_rows + a.nd_rows;
     a.t_vec_ok = vec_ok(target_logits, ts, es);
     a.d_vec_ok = draft_logits ? vec_ok(draft_logits, ds, es) : 0;
-    // the tile plan is that of the workspace (2K+1 rows); the streamed row
-    // count may be smaller (no draft rows), which only shortens the queue
-    pl.units = (unsigned long long)p->B * a.rows * pl.nT;
     return launch(a, pl, p->dtype, workspace, stream);
 }
 
@@ -1141,7 +1168,7 @@ int spec_confidence(int32_t B, int32_t K, int32_t V, int32_t dtype, const void *
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16u) != 0)
         return fail(SPEC_ERR_INVALID_ARG, "workspace must be a 16-byte aligned device pointer");
     Plan pl;
-    plan_workspace(B, K, V, es, pl);
+    plan_workspace(B, K, K, V, es, pl);
     if (workspace_bytes < pl.bytes)
         return fail(SPEC_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, pl.bytes);
     Args a;
