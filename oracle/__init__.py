@@ -61,6 +61,10 @@ def _load():
     lib.oracle_estimator_update.argtypes = [i32, i32, P, P, P, dbl, P, P]
     lib.oracle_estimator_update.restype = ctypes.c_int
     lib.oracle_estimator_loss.argtypes = [i32, i32, P, P, P]
+    lib.oracle_irls_accumulate.restype = ctypes.c_int
+    lib.oracle_irls_accumulate.argtypes = [i32, i32, P, P, P, P, P, P]
+    lib.oracle_irls_refit.restype = ctypes.c_int
+    lib.oracle_irls_refit.argtypes = [i32, P, P, P, dbl, P, P]
     lib.oracle_estimator_loss.restype = dbl
     lib.oracle_row_stats.argtypes = [i64, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
     lib.oracle_row_stats.restype = ctypes.c_int
@@ -171,6 +175,40 @@ def estimator_loss(feature, accepted_len, params):
     n = np.ascontiguousarray(accepted_len, dtype=np.int32)
     p = np.ascontiguousarray(params, dtype=np.float64)
     return lib.oracle_estimator_loss(B, K, _ptr(f), _ptr(n), _ptr(p))
+
+
+def irls_zero(K):
+    """An empty IRLS round: (g [K+1], H [K+1, K+1], n [K+1])."""
+    return np.zeros(K + 1), np.zeros((K + 1, K + 1)), np.zeros(K + 1, np.int64)
+
+
+def irls_accumulate(feature, accepted_len, params, state):
+    """Add one decoding step's labels to an IRLS round ``state`` (in place)."""
+    lib = _load()
+    f = np.ascontiguousarray(feature, dtype=np.float64)
+    B, K = f.shape
+    nacc = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    p = np.ascontiguousarray(params, dtype=np.float64)
+    g, H, n = state
+    assert g.shape == (K + 1,) and H.shape == (K + 1, K + 1) and n.shape == (K + 1,)
+    assert g.flags.c_contiguous and H.flags.c_contiguous and n.flags.c_contiguous
+    rc = lib.oracle_irls_accumulate(B, K, _ptr(f), _ptr(nacc), _ptr(p), _ptr(g), _ptr(H), _ptr(n))
+    if rc != 0:
+        raise ValueError("oracle_irls_accumulate rejected its arguments")
+    return state
+
+
+def irls_refit(state, params, damping):
+    """Refit at the end of a round; returns (new_params [K+1], applied step [K+1])."""
+    lib = _load()
+    g, H, n = state
+    K = g.shape[0] - 1
+    p = np.array(params, dtype=np.float64, copy=True)
+    step = np.empty(K + 1, np.float64)
+    rc = lib.oracle_irls_refit(K, _ptr(g), _ptr(H), _ptr(n), float(damping), _ptr(p), _ptr(step))
+    if rc != 0:
+        raise ValueError("oracle_irls_refit rejected its arguments (%d)" % rc)
+    return p, step
 
 
 def row_stats(z, nthreads=1):

@@ -27,7 +27,9 @@
  *
  * Pins: every function here is pinned by tests/test_oracle_pins.py against
  * closed forms, the worked example of [AV] footnote 1, brute force on tiny
- * vocabularies and a Monte Carlo chi-square test of losslessness ([SD]).
+ * vocabularies and a Monte Carlo chi-square test of losslessness ([SD]); the
+ * IRLS refit against finite differences, a library linear solve and the
+ * maximum-likelihood fit of a general-purpose minimiser.
  */
 #include <math.h>
 #include <stdint.h>
@@ -476,6 +478,102 @@ double oracle_estimator_loss(int32_t B, int32_t K, const double *feature, const 
         }
     }
     return N > 0 ? L / (double)N : 0.0;
+}
+
+/* IRLS refit of the acceptance estimator ([AV] "Ajuste de los Coeficientes").
+ * The coefficients stay fixed during a round of decoding steps; each step
+ * adds the gradient and Hessian of the summed log-loss of its eligible labels
+ * (the labelling of oracle_estimator_update) to the round's totals, and the
+ * refit at the end of the round solves H d = g and moves every coefficient by
+ * its step scaled by n / (n + c), n being the labels behind that coefficient.
+ * With x = (f_i, one-hot of position i) the regressors of a label, s =
+ * sigmoid(theta . x), e = s - y and w = s (1 - s):
+ *   g += e x,   H += w x x^T,   n_0 += 1,   n_{1+i} += 1.
+ * g [K+1], H [(K+1)*(K+1)] row-major and n [K+1] are added to (the caller
+ * zeroes them at the start of a round). Labels are visited in ascending
+ * (b, i) order. */
+int oracle_irls_accumulate(int32_t B, int32_t K, const double *feature, const int32_t *accepted_len,
+                           const double *params, double *g, double *H, int64_t *n) {
+    if (B < 0 || K < 1 || !feature || !accepted_len || !params || !g || !H || !n) return -1;
+    const int32_t D = K + 1;
+    double *x = (double *)calloc((size_t)D, sizeof(double));
+    if (!x) return -1;
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t na = accepted_len[b];
+        if (na < 0 || na > K) { free(x); return -1; }
+        int32_t last = na < K ? na : K - 1;
+        for (int32_t i = 0; i <= last; ++i) {
+            double y = i < na ? 1.0 : 0.0;
+            for (int32_t j = 0; j < D; ++j) x[j] = 0.0;
+            x[0] = feature[(size_t)b * K + i];
+            x[1 + i] = 1.0;
+            double z = 0.0;
+            for (int32_t j = 0; j < D; ++j) z += params[j] * x[j];
+            double sg = sigmoid(z);
+            double e = sg - y, w = sg * (1.0 - sg);
+            for (int32_t r = 0; r < D; ++r) {
+                g[r] += e * x[r];
+                for (int32_t c = 0; c < D; ++c) H[(size_t)r * D + c] += w * x[r] * x[c];
+            }
+            n[0] += 1;
+            n[1 + i] += 1;
+        }
+    }
+    free(x);
+    return 0;
+}
+
+/* The refit at the end of a round. Coefficients without labels (n == 0) keep
+ * their value and leave the system. The rest solve H d = g by Gaussian
+ * elimination without pivoting (H is symmetric positive semi-definite),
+ * eliminating the intercepts first and the slope last. Reading where the
+ * pages are silent: if the slope's final pivot is not positive (below 1e-12 of
+ * its diagonal entry, i.e. the slope is not determined by this round's data,
+ * as when every feature is equal within each position) the slope is held
+ * (d_0 = 0) and the intercepts are solved with it fixed. Then every step is
+ * damped, d_k *= n_k / (n_k + c), and params -= d. A round without labels
+ * changes nothing. step_out [K+1] (may be NULL) receives the applied step. */
+int oracle_irls_refit(int32_t K, const double *g, const double *H, const int64_t *n, double damping,
+                      double *params, double *step_out) {
+    if (K < 1 || !g || !H || !n || !params || !(damping >= 0.0)) return -1;
+    const int32_t D = K + 1;
+    double *d = (double *)calloc((size_t)D, sizeof(double));
+    int32_t *ord = (int32_t *)malloc(sizeof(int32_t) * (size_t)D);
+    double *A = (double *)malloc(sizeof(double) * (size_t)D * (size_t)D);
+    double *rhs = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!d || !ord || !A || !rhs) { free(d); free(ord); free(A); free(rhs); return -1; }
+    int32_t m = 0;                                 /* unknowns: labelled intercepts, then the slope */
+    for (int32_t k = 1; k < D; ++k)                /* (an intercept whose labels all saturated, */
+        if (n[k] > 0 && H[(size_t)k * D + k] > 0.0) ord[m++] = k;   /* w = 0, is held too) */
+    if (n[0] > 0) ord[m++] = 0;
+    for (int32_t r = 0; r < m; ++r) {
+        rhs[r] = g[ord[r]];
+        for (int32_t c = 0; c < m; ++c) A[(size_t)r * m + c] = H[(size_t)ord[r] * D + ord[c]];
+    }
+    int32_t msolve = m;
+    for (int32_t p = 0; p < m; ++p) {                /* forward elimination */
+        double piv = A[(size_t)p * m + p];
+        if (ord[p] == 0 && !(piv > 1e-12 * H[0])) { msolve = p; break; }   /* slope held */
+        if (!(piv > 0.0)) { free(d); free(ord); free(A); free(rhs); return -2; }
+        for (int32_t r = p + 1; r < m; ++r) {
+            double f = A[(size_t)r * m + p] / piv;
+            for (int32_t c = p; c < m; ++c) A[(size_t)r * m + c] -= f * A[(size_t)p * m + c];
+            rhs[r] -= f * rhs[p];
+        }
+    }
+    for (int32_t p = msolve - 1; p >= 0; --p) {      /* back substitution */
+        double acc = rhs[p];
+        for (int32_t c = p + 1; c < msolve; ++c) acc -= A[(size_t)p * m + c] * d[ord[c]];
+        d[ord[p]] = acc / A[(size_t)p * m + p];
+    }
+    for (int32_t k = 0; k < D; ++k) {
+        double nk = (double)n[k];
+        double step = nk > 0.0 ? d[k] * (nk / (nk + damping)) : 0.0;
+        params[k] -= step;
+        if (step_out) step_out[k] = step;
+    }
+    free(d); free(ord); free(A); free(rhs);
+    return 0;
 }
 
 /* Row statistics of `rows` rows of V logits each (row r at z + r*stride):
