@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--irls", action="store_true",
+                    help="also time the IRLS refit entry points (spec_irls_*) on this workload's B, K")
     return ap.parse_args()
 
 
@@ -402,11 +404,45 @@ def run_ours(args, w, world, rank, local, pg):
         "e2e": e2e,
         "clocks": clk,
     }
+    if args.irls and w.with_confidence:
+        line["irls"] = time_irls(w, out, est, dev, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def time_irls(w, out, est, dev, stream, round_steps=64, damping=16.0, reps=20):
+    """Device time of the IRLS refit's two calls on this workload's features
+    and labels: one spec_irls_accumulate per decoding step, one
+    spec_irls_refit per round of `round_steps` steps (both CUDA events on the
+    launching stream, after warm-up)."""
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+
+    st = sv.IrlsState(w.K, dev)
+    params = est.clone()
+    for _ in range(3):
+        sv.irls_accumulate(out["feature"], out["accepted_len"], params, st)
+        sv.irls_refit(st, params, damping)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    er = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record(stream)
+        for _ in range(round_steps):
+            sv.irls_accumulate(out["feature"], out["accepted_len"], params, st)
+        ev[i][1].record(stream)
+        er[i][0].record(stream)
+        sv.irls_refit(st, params, damping)
+        er[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    acc_us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3 / round_steps
+    ref_us = statistics.median(a.elapsed_time(b) for a, b in er) * 1e3
+    return {"accumulate_us_per_step": acc_us, "refit_us_per_round": ref_us, "round_steps": round_steps,
+            "damping": damping, "B": w.B, "K": w.K,
+            "note": "launch-bound O(B*K) work; one CTA each"}
 
 
 def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):

@@ -208,6 +208,46 @@ int spec_estimator_update(int32_t B, int32_t K, const float *feature, const int3
                           void *stream);
 
 /*
+ * IRLS refit of the acceptance estimator ([AV] "Ajuste de los Coeficientes").
+ * The coefficients est_params = (omega, beta_1..beta_K) stay fixed over a
+ * round of decoding steps; each step adds the gradient g and Hessian H of
+ * the summed log-loss of its eligible labels (labelled as for
+ * spec_estimator_update) to a device-resident round state; after the
+ * round's last step the refit solves H d = g and moves every coefficient by
+ * d damped by n / (n + damping), n being the labels behind it (the slope:
+ * all of the round's labels; beta_k: the labels at draft position k).
+ * The pages leave the round length N and the constant c open: the caller
+ * chooses them by when it calls spec_irls_refit and with which damping.
+ *
+ * State: spec_irls_state_size(K) bytes of caller-owned device memory, 8-byte
+ * aligned, of 4K+3 doubles: g[0..K] (g[0] the slope, g[1+i] draft position
+ * i), H_ww, H_wb[0..K-1], H_bb[0..K-1], n[0..K] (n[0] all labels, n[1+i]
+ * labels at position i). H is an arrow matrix (one label touches the slope
+ * and one intercept), so these entries are all of it. spec_irls_reset
+ * zeroes it; spec_irls_refit zeroes it after using it.
+ *
+ * Refit readings (the pages are silent): coefficients without labels keep
+ * their value; if after eliminating the intercepts the slope's pivot is at
+ * most 1e-12 of H_ww (the round does not determine the slope), the slope is
+ * held and the intercepts solve with it fixed. A round without labels
+ * changes nothing. step_out [K+1] doubles (optional) receives the applied
+ * step (params -= step).
+ *
+ * feature [B][K] f32 and accepted_len [B] int32 in [0,K] as produced by
+ * spec_verify; est_params [K+1] f32 (read by accumulate, updated by refit).
+ * Precision: each label's sigmoid terms are fp32; every sum and the solve
+ * are fp64. 1 <= K <= 1024; B >= 0. One CTA each, fixed summation order:
+ * the results are bit-reproducible. Asynchronous on `stream`; the status
+ * codes are those of spec_verify.
+ */
+size_t spec_irls_state_size(int32_t K);
+int spec_irls_reset(int32_t K, void *state, void *stream);
+int spec_irls_accumulate(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                         const float *est_params, void *state, void *stream);
+int spec_irls_refit(int32_t K, void *state, float *est_params, double damping, double *step_out,
+                    void *stream);
+
+/*
  * Synchronously read the device status word of a workspace last used by
  * spec_verify or spec_confidence (waits for the device). *status_out gets
  * SPEC_OK or the largest device-side code raised (SPEC_ERR_TIMEOUT,

@@ -213,6 +213,59 @@ def estimator_update(feature: torch.Tensor, accepted_len: torch.Tensor, est_para
     return (grad, cnt) if want_grad else None
 
 
+class IrlsState:
+    """Device-resident state of one IRLS round (spec_irls_*): 4K+3 doubles,
+    zeroed on creation and after every refit."""
+
+    def __init__(self, K: int, device, stream: Optional[torch.cuda.Stream] = None):
+        n = _native.lib().spec_irls_state_size(int(K))
+        if n == 0:
+            raise SpecError(SPEC_ERR_UNSUPPORTED, "IRLS: K must be in [1, 1024]")
+        self.K = int(K)
+        self.device = torch.device(device)
+        self.tensor = torch.empty(n // 8, dtype=torch.float64, device=self.device)
+        self.reset(stream)
+
+    def reset(self, stream: Optional[torch.cuda.Stream] = None):
+        _check(_native.lib().spec_irls_reset(self.K, _ptr(self.tensor), _stream_ptr(stream, self.device)))
+
+    def parts(self):
+        """Views (g [K+1], H_ww [1], H_wb [K], H_bb [K], n [K+1]) of the state."""
+        K, t = self.K, self.tensor
+        return t[:K + 1], t[K + 1:K + 2], t[K + 2:2 * K + 2], t[2 * K + 2:3 * K + 2], t[3 * K + 2:]
+
+
+def irls_accumulate(feature: torch.Tensor, accepted_len: torch.Tensor, est_params: torch.Tensor,
+                    state: IrlsState, stream: Optional[torch.cuda.Stream] = None):
+    """Add one decoding step's labels to an IRLS round (spec_irls_accumulate)."""
+    B, K = feature.shape
+    dev = feature.device
+    if K != state.K or state.device != dev:
+        raise ValueError("irls_accumulate: state does not match K / device")
+    for t, dt_, shp in ((feature, torch.float32, (B, K)), (accepted_len, torch.int32, (B,)),
+                        (est_params, torch.float32, (K + 1,))):
+        if t.dtype != dt_ or tuple(t.shape) != shp or not t.is_contiguous() or t.device != dev:
+            raise ValueError("irls_accumulate: bad tensor (dtype/shape/device/contiguity)")
+    rc = _native.lib().spec_irls_accumulate(B, K, _ptr(feature), _ptr(accepted_len), _ptr(est_params),
+                                            _ptr(state.tensor), _stream_ptr(stream, dev))
+    _check(rc)
+
+
+def irls_refit(state: IrlsState, est_params: torch.Tensor, damping: float, want_step: bool = False,
+               stream: Optional[torch.cuda.Stream] = None):
+    """End an IRLS round: update ``est_params`` in place (spec_irls_refit) and
+    zero the state. Returns the applied step [K+1] (fp64) when ``want_step``."""
+    K, dev = state.K, state.device
+    if est_params.dtype != torch.float32 or tuple(est_params.shape) != (K + 1,) \
+            or not est_params.is_contiguous() or est_params.device != dev:
+        raise ValueError("irls_refit: bad est_params (dtype/shape/device/contiguity)")
+    step = torch.empty(K + 1, dtype=torch.float64, device=dev) if want_step else None
+    rc = _native.lib().spec_irls_refit(K, _ptr(state.tensor), _ptr(est_params), float(damping), _ptr(step),
+                                       _stream_ptr(stream, dev))
+    _check(rc)
+    return step
+
+
 def device_status(workspace_tensor: torch.Tensor) -> int:
     """Synchronously read the status word of a workspace (tests, debugging)."""
     v = ctypes.c_int32(-1)

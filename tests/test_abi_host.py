@@ -182,6 +182,27 @@ def test_confidence_and_estimator_validation(L):
     assert L.spec_get_device_status(None, ctypes.byref(v)) == 1
 
 
+def test_irls_validation(L):
+    P = ctypes.c_void_p
+    assert L.spec_irls_state_size(0) == 0 and L.spec_irls_state_size(1025) == 0
+    assert L.spec_irls_state_size(8) == (4 * 8 + 3) * 8
+    assert L.spec_irls_reset(0, P(_FAKE), None) == 2
+    assert L.spec_irls_reset(4, None, None) == 1
+    assert L.spec_irls_accumulate(4, 0, P(_FAKE), P(_FAKE), P(_FAKE), P(_FAKE), None) == 2
+    assert L.spec_irls_accumulate(-1, 2, P(_FAKE), P(_FAKE), P(_FAKE), P(_FAKE), None) == 1
+    assert L.spec_irls_accumulate(4, 2, None, P(_FAKE), P(_FAKE), P(_FAKE), None) == 1
+    assert L.spec_irls_accumulate(4, 2, P(_FAKE), P(_FAKE), None, P(_FAKE), None) == 1
+    assert L.spec_irls_accumulate(4, 2, P(_FAKE), P(_FAKE), P(_FAKE), None, None) == 1
+    assert L.spec_irls_accumulate(4, 2, P(_FAKE), P(_FAKE), P(_FAKE), P(_FAKE + 4), None) == 1   # misaligned
+    assert L.spec_irls_refit(1025, P(_FAKE), P(_FAKE), 1.0, None, None) == 2
+    assert L.spec_irls_refit(4, None, P(_FAKE), 1.0, None, None) == 1
+    assert L.spec_irls_refit(4, P(_FAKE), None, 1.0, None, None) == 1
+    assert L.spec_irls_refit(4, P(_FAKE), P(_FAKE), -1.0, None, None) == 1
+    assert L.spec_irls_refit(4, P(_FAKE), P(_FAKE), float("nan"), None, None) == 1
+    assert L.spec_irls_refit(4, P(_FAKE), P(_FAKE), float("inf"), None, None) == 1
+    assert L.spec_last_error()
+
+
 def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(_native, "_lib", None)
     monkeypatch.setattr(_native, "LIB_PATH", "/nonexistent/libspecverify.so")
