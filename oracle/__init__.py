@@ -54,15 +54,17 @@ def _load():
     P = ctypes.c_void_p
     i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
     lib.oracle_verify.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.c_int, P, i64, P, i64,
-                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
+                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_confidence.argtypes = [i32, i32, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
     lib.oracle_confidence.restype = ctypes.c_int
-    lib.oracle_estimator_update.argtypes = [i32, i32, P, P, P, dbl, P, P]
+    lib.oracle_estimator_update.argtypes = [i32, i32, P, P, P, P, dbl, P, P]
     lib.oracle_estimator_update.restype = ctypes.c_int
-    lib.oracle_estimator_loss.argtypes = [i32, i32, P, P, P]
+    lib.oracle_estimator_loss.argtypes = [i32, i32, P, P, P, P]
     lib.oracle_irls_accumulate.restype = ctypes.c_int
-    lib.oracle_irls_accumulate.argtypes = [i32, i32, P, P, P, P, P, P]
+    lib.oracle_irls_accumulate.argtypes = [i32, i32, P, P, P, P, P, P, P]
+    lib.oracle_av_budget.restype = ctypes.c_int
+    lib.oracle_av_budget.argtypes = [i32, i32, P, P, P, P, P, P, P, P]
     lib.oracle_irls_refit.restype = ctypes.c_int
     lib.oracle_irls_refit.argtypes = [i32, P, P, P, dbl, P, P]
     lib.oracle_estimator_loss.restype = dbl
@@ -86,9 +88,10 @@ def _logits(z):
 
 
 def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_params=None,
-           nthreads=1, want_cdf=False):
+           nthreads=1, want_cdf=False, draft_len=None):
     """Verify B sequences. zt [B,K+1,V], zd [B,K,V] or None, x [B,K] int32,
-    u [B,K+1] float32 or None.
+    u [B,K+1] float32 or None, draft_len [B] int32 in [0, K] or None (drafts
+    submitted for verification per sequence; None: all K).
 
     Returns a dict of numpy arrays: out_tokens [B,K+1] int32, accepted_len [B],
     pos_stats [B,K+1,4] (lse_t, h_t, log_ratio, f), feature [B,K], conf [B,K]
@@ -121,13 +124,16 @@ def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_param
         flags=np.empty(B, np.int32),
     )
     cdf = np.full((B, V), np.nan) if want_cdf else None
+    if draft_len is not None:
+        draft_len = np.ascontiguousarray(draft_len, dtype=np.int32)
+        assert draft_len.shape == (B,)
     rc = lib.oracle_verify(B, K, V, dt, mode, _ptr(zt), V, _ptr(zd), V, _ptr(x), _ptr(u),
                            float(fly_theta), int(fly_window), _ptr(est),
                            _ptr(out["out_tokens"]), _ptr(out["accepted_len"]),
                            _ptr(out["pos_stats"]), _ptr(out["conf"]) if est is not None else None,
                            _ptr(out["feature"]) if zd is not None else None,
                            _ptr(out["margin_acc"]), _ptr(out["margin_cdf"]), _ptr(cdf),
-                           _ptr(out["flags"]), int(nthreads))
+                           _ptr(out["flags"]), _ptr(draft_len), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     out["margin"] = np.minimum(out["margin_acc"], out["margin_cdf"])
@@ -152,29 +158,38 @@ def confidence(zd, est_params=None, nthreads=1):
     return feat, conf, flags
 
 
-def estimator_update(feature, accepted_len, params, lr):
+def _draft_len(draft_len, B):
+    if draft_len is None:
+        return None
+    d = np.ascontiguousarray(draft_len, dtype=np.int32)
+    assert d.shape == (B,)
+    return d
+
+
+def estimator_update(feature, accepted_len, params, lr, draft_len=None):
     """One gradient step; returns (new_params [K+1], grad [K+1], counts [K+1])."""
     lib = _load()
     f = np.ascontiguousarray(feature, dtype=np.float64)
     B, K = f.shape
     n = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    dl = _draft_len(draft_len, B)
     p = np.array(params, dtype=np.float64, copy=True)
     assert p.shape == (K + 1,)
     g = np.empty(K + 1, np.float64)
     c = np.empty(K + 1, np.int64)
-    rc = lib.oracle_estimator_update(B, K, _ptr(f), _ptr(n), _ptr(p), float(lr), _ptr(g), _ptr(c))
+    rc = lib.oracle_estimator_update(B, K, _ptr(f), _ptr(n), _ptr(dl), _ptr(p), float(lr), _ptr(g), _ptr(c))
     if rc != 0:
         raise ValueError("oracle_estimator_update rejected its arguments")
     return p, g, c
 
 
-def estimator_loss(feature, accepted_len, params):
+def estimator_loss(feature, accepted_len, params, draft_len=None):
     lib = _load()
     f = np.ascontiguousarray(feature, dtype=np.float64)
     B, K = f.shape
     n = np.ascontiguousarray(accepted_len, dtype=np.int32)
     p = np.ascontiguousarray(params, dtype=np.float64)
-    return lib.oracle_estimator_loss(B, K, _ptr(f), _ptr(n), _ptr(p))
+    return lib.oracle_estimator_loss(B, K, _ptr(f), _ptr(n), _ptr(_draft_len(draft_len, B)), _ptr(p))
 
 
 def irls_zero(K):
@@ -182,17 +197,18 @@ def irls_zero(K):
     return np.zeros(K + 1), np.zeros((K + 1, K + 1)), np.zeros(K + 1, np.int64)
 
 
-def irls_accumulate(feature, accepted_len, params, state):
+def irls_accumulate(feature, accepted_len, params, state, draft_len=None):
     """Add one decoding step's labels to an IRLS round ``state`` (in place)."""
     lib = _load()
     f = np.ascontiguousarray(feature, dtype=np.float64)
     B, K = f.shape
     nacc = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    dl = _draft_len(draft_len, B)
     p = np.ascontiguousarray(params, dtype=np.float64)
     g, H, n = state
     assert g.shape == (K + 1,) and H.shape == (K + 1, K + 1) and n.shape == (K + 1,)
     assert g.flags.c_contiguous and H.flags.c_contiguous and n.flags.c_contiguous
-    rc = lib.oracle_irls_accumulate(B, K, _ptr(f), _ptr(nacc), _ptr(p), _ptr(g), _ptr(H), _ptr(n))
+    rc = lib.oracle_irls_accumulate(B, K, _ptr(f), _ptr(nacc), _ptr(dl), _ptr(p), _ptr(g), _ptr(H), _ptr(n))
     if rc != 0:
         raise ValueError("oracle_irls_accumulate rejected its arguments")
     return state
@@ -209,6 +225,28 @@ def irls_refit(state, params, damping):
     if rc != 0:
         raise ValueError("oracle_irls_refit rejected its arguments (%d)" % rc)
     return p, step
+
+
+def av_budget(conf, draft_cost, verify_cost):
+    """Adaptive-verification pruning: returns a dict with draft_len [B] int32,
+    budget (int), survival [B,K] float32, objective [B*K+1] and gap (relative
+    gap between the best and second-best objective)."""
+    lib = _load()
+    c = np.ascontiguousarray(conf, dtype=np.float32)
+    B, K = c.shape
+    dc = np.ascontiguousarray(draft_cost, dtype=np.float32)
+    vc = np.ascontiguousarray(verify_cost, dtype=np.float32)
+    assert dc.shape == (B * K + 1,) and vc.shape == (B * K + 1,)
+    dl = np.empty(B, np.int32)
+    bud = np.zeros(1, np.int32)
+    sv = np.empty((B, K), np.float32)
+    obj = np.empty(B * K + 1, np.float64)
+    gap = np.zeros(1, np.float64)
+    rc = lib.oracle_av_budget(B, K, _ptr(c), _ptr(dc), _ptr(vc), _ptr(dl), _ptr(bud), _ptr(sv), _ptr(obj),
+                              _ptr(gap))
+    if rc != 0:
+        raise ValueError("oracle_av_budget rejected its arguments")
+    return dict(draft_len=dl, budget=int(bud[0]), survival=sv, objective=obj, gap=float(gap[0]))
 
 
 def row_stats(z, nthreads=1):

@@ -167,7 +167,7 @@ static double dmin(double a, double b) { return a < b ? a : b; }
  *  zd: K draft rows (NULL allowed in greedy / FLy mode).
  *  x:  K draft tokens.  u: K+1 uniforms (NULL allowed in greedy / FLy mode).
  * Scratch: p, q, r of V doubles each. */
-static void verify_one(int32_t K, int32_t V, int dtype, int mode,
+static void verify_one(int32_t K, int32_t Kb, int32_t V, int dtype, int mode,
                        const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
                        const int32_t *x, const float *u, double fly_theta, int32_t fly_window,
                        const double *est, int32_t *out_tokens, int32_t *acc_len,
@@ -181,15 +181,25 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
     double mc = INFINITY;      /* margin of the final inverse-CDF draw */
     int fl = 0;
 
-    /* Per-position statistics (written whether or not the position is reached). */
-    for (int32_t j = 0; j <= K; ++j) {
+    /* Per-position statistics (written whether or not the position is reached).
+     * Only the first Kb drafts were submitted for verification (Kb = K unless
+     * the batch was pruned, [AV] "Antecedentes": a subset of the drafts is
+     * verified); target rows after Kb and draft rows from Kb on were never
+     * computed and stay NaN. */
+    if (pos_stats)
+        for (int32_t j = 0; j < 4 * (K + 1); ++j) pos_stats[j] = NAN;
+    for (int32_t j = 0; j < K; ++j) {
+        if (feature) feature[j] = NAN;
+        if (conf) conf[j] = NAN;
+    }
+    for (int32_t j = 0; j <= Kb; ++j) {
         const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
         int ok;
         double lse_t = softmax_row(trow, dtype, V, p, &ok);
         if (!ok) fl |= OR_FLAG_BAD_ROW;
         double h = norm_entropy(p, V);
         double lr = NAN, f = NAN;
-        if (j < K && zd) {
+        if (j < Kb && zd) {
             const void *drow = dbase + (size_t)j * (size_t)d_stride * es;
             int okd;
             double lse_d = softmax_row(drow, dtype, V, q, &okd);
@@ -219,7 +229,7 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
          * iff u_i < min(1, p(x_i)/q(x_i)). [SD] step 4: stop at the first
          * rejection and draw the correction from norm(max(0, p - q)). */
         int rejected = 0;
-        for (int32_t i = 0; i < K; ++i) {
+        for (int32_t i = 0; i < Kb; ++i) {
             const void *trow = tbase + (size_t)i * (size_t)t_stride * es;
             const void *drow = dbase + (size_t)i * (size_t)d_stride * es;
             int ok;
@@ -254,9 +264,10 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
             break;
         }
         if (!rejected) {
-            /* Bonus token after K acceptances (reading: a draw from the target's
-             * row K, standard for rejection-sampling verification). */
-            const void *trow = tbase + (size_t)K * (size_t)t_stride * es;
+            /* Bonus token after Kb acceptances (reading: a draw from the target's
+             * row Kb, standard for rejection-sampling verification; the final
+             * draw always uses u[K]). */
+            const void *trow = tbase + (size_t)Kb * (size_t)t_stride * es;
             int ok;
             softmax_row(trow, dtype, V, p, &ok);
             double Z = 0.0;
@@ -268,21 +279,21 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
         /* Exact match: accept x_i iff it is the target's top prediction
          * ([FLy] section 1; [SD] "Проверка результата", greedy output is
          * reproducible). The correction is the target's argmax at the stop. */
-        n = K;
-        for (int32_t i = 0; i < K; ++i) {
+        n = Kb;
+        for (int32_t i = 0; i < Kb; ++i) {
             const void *trow = tbase + (size_t)i * (size_t)t_stride * es;
             int32_t a = argmax_row(trow, dtype, V);
             if (x[i] != a) { n = i; token = a; break; }
         }
-        if (n == K) token = argmax_row(tbase + (size_t)K * (size_t)t_stride * es, dtype, V);
+        if (n == Kb) token = argmax_row(tbase + (size_t)Kb * (size_t)t_stride * es, dtype, V);
     } else {
         /* [FLy] 2.A: a deviation at j (x_j differs from the target's argmax)
          * is rejected at once when the target's normalised entropy h_j < theta;
          * when h_j >= theta it is deferred: accepted if none of the next W draft
          * positions deviates, rejected retroactively if one does, and rejected
          * conservatively if the window does not fit inside the draft. */
-        n = K;
-        for (int32_t j = 0; j < K; ++j) {
+        n = Kb;
+        for (int32_t j = 0; j < Kb; ++j) {
             const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
             int32_t a = argmax_row(trow, dtype, V);
             if (x[j] == a) continue;               /* no deviation: accept j */
@@ -293,7 +304,7 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
             int reject;
             if (h < fly_theta) {
                 reject = 1;                        /* confident target */
-            } else if (j + fly_window > K - 1) {
+            } else if (j + fly_window > Kb - 1) {
                 reject = 1;                        /* window past the draft end */
             } else {
                 reject = 0;
@@ -304,7 +315,7 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
             }
             if (reject) { n = j; token = a; break; }
         }
-        if (n == K) token = argmax_row(tbase + (size_t)K * (size_t)t_stride * es, dtype, V);
+        if (n == Kb) token = argmax_row(tbase + (size_t)Kb * (size_t)t_stride * es, dtype, V);
     }
 
     /* Writeback ([SD] step 4): the accepted prefix, then the correction or
@@ -329,7 +340,10 @@ static void verify_one(int32_t K, int32_t V, int dtype, int mode,
  *    token's interval, in units of Z (stochastic mode; +inf otherwise),
  *  cdf [B][V] or NULL: normalised running sum of the final draw's weights
  *    (stochastic mode; untouched otherwise),
- *  flags [B] or NULL (OR_FLAG_* bits).
+ *  flags [B] or NULL (OR_FLAG_* bits),
+ *  draft_len [B] or NULL: drafts submitted for verification per sequence,
+ *    in [0, K] (NULL: all K). Sequence b verifies drafts 0..draft_len[b]-1
+ *    against target rows 0..draft_len[b]; the rest of its outputs are NaN/-1.
  * nthreads > 0 sets the OpenMP thread count. Returns 0, or -1 on bad args. */
 int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
@@ -337,8 +351,11 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const double *est, int32_t *out_tokens, int32_t *accepted_len,
                   double *pos_stats, double *conf, double *feature,
                   double *margin_acc, double *margin_cdf, double *cdf, int32_t *flags,
-                  int nthreads) {
+                  const int32_t *draft_len, int nthreads) {
     if (B < 0 || K < 1 || V < 2 || !zt || !x || !out_tokens || !accepted_len) return -1;
+    if (draft_len)
+        for (int32_t b = 0; b < B; ++b)
+            if (draft_len[b] < 0 || draft_len[b] > K) return -1;
     if (mode == OR_STOCHASTIC && (!zd || !u)) return -1;
     if (t_stride <= 0) t_stride = V;
     if (d_stride <= 0) d_stride = V;
@@ -356,7 +373,7 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
 #pragma omp for schedule(static)
             for (int32_t b = 0; b < B; ++b) {
                 int fl = 0;
-                verify_one(K, V, dtype, mode,
+                verify_one(K, draft_len ? draft_len[b] : K, V, dtype, mode,
                            (const char *)zt + (size_t)b * (size_t)(K + 1) * (size_t)t_stride * es, t_stride,
                            zd ? (const char *)zd + (size_t)b * (size_t)K * (size_t)d_stride * es : NULL, d_stride,
                            x + (size_t)b * K, u ? u + (size_t)b * (K + 1) : NULL, fly_theta, fly_window,
@@ -418,7 +435,9 @@ int oracle_confidence(int32_t B, int32_t K, int32_t V, int dtype, const void *zd
  * Coeficientes").
  * Labels: only drafts up to and including the first rejection are eligible;
  * y_i = 1 for i < n_acc, y_{n_acc} = 0 when n_acc < K, later positions carry
- * no label.
+ * no label. With pruned verification (draft_len, NULL = K for all) only the
+ * K_b verified drafts of sequence b can carry a label: y_{n_acc} = 0 only
+ * when n_acc < K_b.
  * Step (reading: the pages solve an IRLS Newton system over N steps; this
  * entry point takes one plain gradient step of size lr on the mean log-loss
  * over the batch's eligible labels):
@@ -429,15 +448,17 @@ int oracle_confidence(int32_t B, int32_t K, int32_t V, int dtype, const void *zd
  * (count_out[0] = N, count_out[k] = labels at draft position k-1) may be NULL.
  * The loss is accumulated in ascending (b, i) order. */
 int oracle_estimator_update(int32_t B, int32_t K, const double *feature, const int32_t *accepted_len,
-                            double *params, double lr, double *grad_out, int64_t *count_out) {
+                            const int32_t *draft_len, double *params, double lr, double *grad_out,
+                            int64_t *count_out) {
     if (B < 0 || K < 1 || !feature || !accepted_len || !params) return -1;
     double *g = (double *)calloc((size_t)K + 1, sizeof(double));
     int64_t *cnt = (int64_t *)calloc((size_t)K + 1, sizeof(int64_t));
     if (!g || !cnt) { free(g); free(cnt); return -1; }
     for (int32_t b = 0; b < B; ++b) {
         int32_t n = accepted_len[b];
-        if (n < 0 || n > K) { free(g); free(cnt); return -1; }
-        int32_t last = n < K ? n : K - 1;    /* last eligible position */
+        int32_t kb = draft_len ? draft_len[b] : K;
+        if (kb < 0 || kb > K || n < 0 || n > kb) { free(g); free(cnt); return -1; }
+        int32_t last = n < kb ? n : kb - 1;  /* last eligible (verified) position */
         for (int32_t i = 0; i <= last; ++i) {
             double y = i < n ? 1.0 : 0.0;
             double f = feature[(size_t)b * K + i];
@@ -465,12 +486,13 @@ int oracle_estimator_update(int32_t B, int32_t K, const double *feature, const i
  * the update ([AV] "Otras Características Consideradas": log-loss is the mean
  * negative log-likelihood of the predicted acceptance probability). */
 double oracle_estimator_loss(int32_t B, int32_t K, const double *feature, const int32_t *accepted_len,
-                             const double *params) {
+                             const int32_t *draft_len, const double *params) {
     double L = 0.0;
     int64_t N = 0;
     for (int32_t b = 0; b < B; ++b) {
         int32_t n = accepted_len[b];
-        int32_t last = n < K ? n : K - 1;
+        int32_t kb = draft_len ? draft_len[b] : K;
+        int32_t last = n < kb ? n : kb - 1;
         for (int32_t i = 0; i <= last; ++i) {
             double s = sigmoid(params[0] * feature[(size_t)b * K + i] + params[1 + i]);
             L += i < n ? -log(s) : -log(1.0 - s);
@@ -493,15 +515,16 @@ double oracle_estimator_loss(int32_t B, int32_t K, const double *feature, const 
  * zeroes them at the start of a round). Labels are visited in ascending
  * (b, i) order. */
 int oracle_irls_accumulate(int32_t B, int32_t K, const double *feature, const int32_t *accepted_len,
-                           const double *params, double *g, double *H, int64_t *n) {
+                           const int32_t *draft_len, const double *params, double *g, double *H, int64_t *n) {
     if (B < 0 || K < 1 || !feature || !accepted_len || !params || !g || !H || !n) return -1;
     const int32_t D = K + 1;
     double *x = (double *)calloc((size_t)D, sizeof(double));
     if (!x) return -1;
     for (int32_t b = 0; b < B; ++b) {
         int32_t na = accepted_len[b];
-        if (na < 0 || na > K) { free(x); return -1; }
-        int32_t last = na < K ? na : K - 1;
+        int32_t kb = draft_len ? draft_len[b] : K;
+        if (kb < 0 || kb > K || na < 0 || na > kb) { free(x); return -1; }
+        int32_t last = na < kb ? na : kb - 1;
         for (int32_t i = 0; i <= last; ++i) {
             double y = i < na ? 1.0 : 0.0;
             for (int32_t j = 0; j < D; ++j) x[j] = 0.0;
@@ -573,6 +596,71 @@ int oracle_irls_refit(int32_t K, const double *g, const double *H, const int64_t
         if (step_out) step_out[k] = step;
     }
     free(d); free(ord); free(A); free(rhs);
+    return 0;
+}
+
+/* Adaptive-verification pruning and budget ([AV] "Otras Características
+ * Consideradas": survival is the running product of the confidences along
+ * each sequence's drafts; the drafts are ranked by survival over the whole
+ * batch; the budget maximises the expected emitted tokens, the number of
+ * requests plus the sum of the top-k survivals, divided by the measured cost
+ * of drafting and verifying k tokens; the top `budget` drafts are verified).
+ * Readings: survival is an fp32 running product in ascending position (the
+ * precision that decides the ranking on the GPU too); ties in survival rank
+ * by ascending flat index b*K + i, so each sequence's winners are a prefix
+ * of its drafts; NaN survival ranks last; the objective is fp64 with the
+ * top-k sum taken in rank order; a cost that is not positive makes its k
+ * ineligible; the first k of the maximum wins (k = 0 if none is eligible).
+ * conf [B][K] f32, draft_cost and verify_cost [B*K+1] f32 (k = 0..B*K).
+ * Outputs: draft_len [B], *budget, survival [B][K] f32 (may be NULL),
+ * objective [B*K+1] (may be NULL), *gap (may be NULL): the relative gap
+ * between the best and the second-best objective (a decision is knife-edge
+ * when it is tiny). */
+static const float *g_av_key;
+static int av_cmp(const void *pa, const void *pb) {
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    float ka = g_av_key[a], kb = g_av_key[b];
+    if (ka > kb) return -1;
+    if (ka < kb) return 1;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+int oracle_av_budget(int32_t B, int32_t K, const float *conf, const float *draft_cost, const float *verify_cost,
+                     int32_t *draft_len, int32_t *budget, float *survival, double *objective, double *gap) {
+    if (B < 0 || K < 1 || (B > 0 && !conf) || !draft_cost || !verify_cost || !draft_len || !budget) return -1;
+    const int64_t N = (int64_t)B * K;
+    float *key = (float *)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
+    int32_t *ord = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    double *obj = (double *)malloc(sizeof(double) * (size_t)(N + 1));
+    if (!key || !ord || !obj) { free(key); free(ord); free(obj); return -1; }
+    for (int32_t b = 0; b < B; ++b) {
+        float sv = 1.0f;
+        for (int32_t i = 0; i < K; ++i) {
+            sv = sv * conf[(size_t)b * K + i];
+            if (survival) survival[(size_t)b * K + i] = sv;
+            key[(size_t)b * K + i] = sv == sv ? sv : -1.0f;   /* NaN ranks last */
+        }
+    }
+    for (int64_t j = 0; j < N; ++j) ord[j] = (int32_t)j;
+    g_av_key = key;
+    qsort(ord, (size_t)N, sizeof(int32_t), av_cmp);
+    double S = 0.0, best = -INFINITY, second = -INFINITY;
+    int64_t kbest = 0;
+    for (int64_t k = 0; k <= N; ++k) {
+        if (k > 0) S += key[ord[k - 1]] > 0.0f ? (double)key[ord[k - 1]] : 0.0;
+        double c = (double)draft_cost[k] + (double)verify_cost[k];
+        double o = c > 0.0 ? ((double)B + S) / c : -INFINITY;
+        obj[k] = o;
+        if (o > best) { second = best; best = o; kbest = k; }
+        else if (o > second) second = o;
+    }
+    for (int32_t b = 0; b < B; ++b) draft_len[b] = 0;
+    if (best == -INFINITY) kbest = 0;
+    for (int64_t j = 0; j < kbest; ++j) draft_len[ord[j] / K] += 1;
+    *budget = (int32_t)kbest;
+    if (objective) for (int64_t k = 0; k <= N; ++k) objective[k] = obj[k];
+    if (gap) *gap = (best > -INFINITY && second > -INFINITY) ? (best - second) / fabs(best) : INFINITY;
+    free(key); free(ord); free(obj);
     return 0;
 }
 
