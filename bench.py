@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--av", action="store_true",
+                    help="also time adaptive-verification pruning (spec_av_budget) and the pruned verify")
     ap.add_argument("--irls", action="store_true",
                     help="also time the IRLS refit entry points (spec_irls_*) on this workload's B, K")
     return ap.parse_args()
@@ -406,11 +408,30 @@ def run_ours(args, w, world, rank, local, pg):
     }
     if args.irls and w.with_confidence:
         line["irls"] = time_irls(w, out, est, dev, stream)
+    if args.av and w.with_confidence and w.mode == "stochastic":
+        line["av"] = time_av(w, inp, zd, u, out, est, ws, dev, stream, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def device_us(fn, stream, reps):
+    """Mean device time of fn() in microseconds over `reps` back-to-back
+    calls. A short sleep kernel holds the stream while the host enqueues
+    them, so the events bracket device work, not host issue gaps (these are
+    launch-sized kernels)."""
+    import torch
+
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(20_000_000)          # ~10 ms of device time, bounded
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
 
 
 def time_irls(w, out, est, dev, stream, round_steps=64, damping=16.0, reps=20):
@@ -427,22 +448,50 @@ def time_irls(w, out, est, dev, stream, round_steps=64, damping=16.0, reps=20):
     for _ in range(3):
         sv.irls_accumulate(out["feature"], out["accepted_len"], params, st)
         sv.irls_refit(st, params, damping)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    er = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    for i in range(reps):
-        ev[i][0].record(stream)
-        for _ in range(round_steps):
-            sv.irls_accumulate(out["feature"], out["accepted_len"], params, st)
-        ev[i][1].record(stream)
-        er[i][0].record(stream)
-        sv.irls_refit(st, params, damping)
-        er[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    acc_us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3 / round_steps
-    ref_us = statistics.median(a.elapsed_time(b) for a, b in er) * 1e3
+    acc_us = device_us(lambda: sv.irls_accumulate(out["feature"], out["accepted_len"], params, st), stream,
+                       round_steps)
+    ref_us = device_us(lambda: sv.irls_refit(st, params, damping), stream, reps)
     return {"accumulate_us_per_step": acc_us, "refit_us_per_round": ref_us, "round_steps": round_steps,
             "damping": damping, "B": w.B, "K": w.K,
             "note": "launch-bound O(B*K) work; one CTA each"}
+
+
+def time_av(w, inp, zd, u, out, est, ws, dev, stream, peak, reps=50):
+    """Device time of one adaptive-verification step's two calls: the budget
+    (spec_av_budget on this step's confidences, with a synthetic cost table
+    that grows by a third of a base step per B verified drafts) and the
+    pruned verify it selects (spec_verify_ragged). The pruned verify reads
+    only the rows it verifies: sum_b (2 K_b + 1) V s bytes."""
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+
+    N = w.B * w.K
+    k = torch.arange(N + 1, dtype=torch.float32, device=dev)
+    dcost = 0.01 * k / w.B
+    vcost = 1.0 + 0.05 * k / w.B
+    # confidences from a calibrated estimator (slope 0.5, intercepts 1.5, in
+    # the range the pages report for fitted pairs) on this step's draft rows
+    est_av = torch.tensor([0.5] + [1.5] * w.K, dtype=torch.float32, device=dev)
+    _, conf = sv.confidence(zd, est_av)
+    bud = sv.av_budget(conf, dcost, vcost)
+    for _ in range(3):
+        sv.av_budget(conf, dcost, vcost, stream=None)
+        sv.verify(inp["zt"], zd, inp["x"], u, mode=w.mode, est_params=est, out=dict(out), workspace=ws,
+                  want_feature=True, want_conf=True, draft_len=bud["draft_len"])
+    budget_us = device_us(lambda: sv.av_budget(conf, dcost, vcost), stream, reps)
+    o2 = dict(out)
+    v_ms = device_us(lambda: sv.verify(inp["zt"], zd, inp["x"], u, mode=w.mode, est_params=est, out=o2,
+                                       workspace=ws, want_feature=True, want_conf=True,
+                                       draft_len=bud["draft_len"]), stream, reps) / 1e3
+    dl = bud["draft_len"].cpu()
+    es = 2 if w.dtype == "bf16" else 4
+    pruned_bytes = int(((2 * dl.long() + 1) * w.V * es).sum())
+    return {"budget": int(bud["budget"].item()), "drafts": N, "mean_draft_len": float(dl.float().mean()),
+            "budget_us": budget_us,
+            "pruned_verify_ms": v_ms, "pruned_bytes": pruned_bytes,
+            "pruned_frac": pruned_bytes / (v_ms / 1e3) / 1e9 / peak,
+            "cost_table": "draft 0.01 k/B, verify 1 + 0.05 k/B (synthetic)", "est": "omega 0.5, beta 1.5"}
 
 
 def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):

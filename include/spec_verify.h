@@ -208,6 +208,61 @@ int spec_estimator_update(int32_t B, int32_t K, const float *feature, const int3
                           void *stream);
 
 /*
+ * Adaptive-verification pruning and budget ([AV] "Antecedentes", "Otras
+ * Características Consideradas"). Before the target model runs, decide which
+ * drafts to verify: survival[b][i] = conf[b][0] * ... * conf[b][i] (fp32
+ * running product); the B*K drafts are ranked by survival (ties by the flat
+ * index b*K+i, NaN last); verifying the top k is expected to emit
+ * B + (sum of the top k survivals) tokens at cost draft_cost[k] +
+ * verify_cost[k]; *budget = the k in 0..B*K maximising that ratio (the
+ * first maximum; k with a cost that is not positive is ineligible; 0 if
+ * none is eligible). Each sequence's winners are a prefix of its drafts:
+ * draft_len[b] of them, the input of spec_verify_ragged.
+ * Precision: the top-k sums are exact (each survival rounded to a multiple
+ * of 2^-32, summed as integers); the ratio is fp32 with each step correctly
+ * rounded: objective_k = (float)(B*2^32 + S_k) / (float)(draft_cost[k] +
+ * verify_cost[k]) * 2^-32. The decision is therefore the same on any
+ * machine that follows these steps.
+ * conf [B][K] f32 in [0,1] (spec_confidence or spec_verify's conf),
+ * draft_cost and verify_cost [B*K+1] f32 (caller-measured tables, k = 0..B*K),
+ * draft_len [B] int32 and budget [1] int32 out; survival [B][K] f32 and
+ * objective [B*K+1] f32 (-inf where ineligible) are optional outputs.
+ * 1 <= B, K and B*K <= 16384 (SPEC_ERR_UNSUPPORTED beyond). One CTA;
+ * bit-reproducible; asynchronous.
+ */
+int spec_av_budget(int32_t B, int32_t K, const float *conf, const float *draft_cost, const float *verify_cost,
+                   int32_t *draft_len, int32_t *budget, float *survival, float *objective, void *stream);
+
+/*
+ * spec_verify for a pruned batch: sequence b submitted only its first
+ * draft_len[b] drafts for verification ([AV]: a subset of the drafts is
+ * verified; the target ran with variable-length sequences). draft_len [B]
+ * int32 on the device, each clamped to [0, K]. Sequence b verifies drafts
+ * 0..kb-1 against target rows 0..kb (kb = draft_len[b]); after kb acceptances
+ * the bonus token comes from target row kb; the final draw still uses
+ * uniforms[b][K]; FLy's window must fit inside kb. Rows never verified are
+ * not read: their pos_stats, feature and conf entries are NaN and their
+ * out_tokens -1. Layouts, workspace and status codes are spec_verify's (the
+ * logit tensors keep their [B][K+1][V] / [B][K][V] layout).
+ */
+int spec_verify_ragged(const spec_verify_params *params, const void *target_logits, const void *draft_logits,
+                       const int32_t *draft_tokens, const int32_t *draft_len, const float *uniforms,
+                       int32_t *out_tokens, int32_t *accepted_len, float *pos_stats, const float *est_params,
+                       float *feature, float *conf, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_estimator_update and spec_irls_accumulate for a pruned batch: only
+ * verified drafts carry labels, so with kb = draft_len[b] the label at
+ * position n_acc (y = 0) exists only when n_acc < kb, and positions >= kb
+ * carry none. accepted_len[b] must lie in [0, kb].
+ */
+int spec_estimator_update_ragged(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                                 const int32_t *draft_len, float *est_params, float lr, float *grad_out,
+                                 int32_t *count_out, void *stream);
+int spec_irls_accumulate_ragged(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                                const int32_t *draft_len, const float *est_params, void *state, void *stream);
+
+/*
  * IRLS refit of the acceptance estimator ([AV] "Ajuste de los Coeficientes").
  * The coefficients est_params = (omega, beta_1..beta_K) stay fixed over a
  * round of decoding steps; each step adds the gradient g and Hessian H of

@@ -240,7 +240,7 @@ def av_budget(conf, draft_cost, verify_cost):
     dl = np.empty(B, np.int32)
     bud = np.zeros(1, np.int32)
     sv = np.empty((B, K), np.float32)
-    obj = np.empty(B * K + 1, np.float64)
+    obj = np.empty(B * K + 1, np.float32)
     gap = np.zeros(1, np.float64)
     rc = lib.oracle_av_budget(B, K, _ptr(c), _ptr(dc), _ptr(vc), _ptr(dl), _ptr(bud), _ptr(sv), _ptr(obj),
                               _ptr(gap))

@@ -608,14 +608,20 @@ int oracle_irls_refit(int32_t K, const double *g, const double *H, const int64_t
  * Readings: survival is an fp32 running product in ascending position (the
  * precision that decides the ranking on the GPU too); ties in survival rank
  * by ascending flat index b*K + i, so each sequence's winners are a prefix
- * of its drafts; NaN survival ranks last; the objective is fp64 with the
- * top-k sum taken in rank order; a cost that is not positive makes its k
+ * * of its drafts; NaN survival ranks last. The top-k sum is kept in fixed
+ * point: each positive survival is rounded to the nearest multiple of 2^-32
+ * and the multiples are added as integers, so S_k is exact and the same in
+ * any order. The decision is taken in fp32 (the pages fix no precision; the
+ * GPU's): num_k = (float)(B * 2^32 + S_k), cost_k = draft_cost[k] +
+ * verify_cost[k] in fp32, objective_k = num_k / cost_k (each step correctly
+ * rounded), reported times 2^-32; a cost that is not positive makes its k
  * ineligible; the first k of the maximum wins (k = 0 if none is eligible).
+ * Every quantity the decision reads is computed identically on any machine,
+ * so the budget needs no knife-edge allowance.
  * conf [B][K] f32, draft_cost and verify_cost [B*K+1] f32 (k = 0..B*K).
  * Outputs: draft_len [B], *budget, survival [B][K] f32 (may be NULL),
- * objective [B*K+1] (may be NULL), *gap (may be NULL): the relative gap
- * between the best and the second-best objective (a decision is knife-edge
- * when it is tiny). */
+ * objective [B*K+1] f32 (may be NULL; -inf where ineligible), *gap (may be
+ * NULL): the relative gap between the best and the second-best objective. */
 static const float *g_av_key;
 static int av_cmp(const void *pa, const void *pb) {
     int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
@@ -626,12 +632,12 @@ static int av_cmp(const void *pa, const void *pb) {
 }
 
 int oracle_av_budget(int32_t B, int32_t K, const float *conf, const float *draft_cost, const float *verify_cost,
-                     int32_t *draft_len, int32_t *budget, float *survival, double *objective, double *gap) {
+                     int32_t *draft_len, int32_t *budget, float *survival, float *objective, double *gap) {
     if (B < 0 || K < 1 || (B > 0 && !conf) || !draft_cost || !verify_cost || !draft_len || !budget) return -1;
     const int64_t N = (int64_t)B * K;
     float *key = (float *)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
     int32_t *ord = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
-    double *obj = (double *)malloc(sizeof(double) * (size_t)(N + 1));
+    float *obj = (float *)malloc(sizeof(float) * (size_t)(N + 1));
     if (!key || !ord || !obj) { free(key); free(ord); free(obj); return -1; }
     for (int32_t b = 0; b < B; ++b) {
         float sv = 1.0f;
@@ -644,12 +650,15 @@ int oracle_av_budget(int32_t B, int32_t K, const float *conf, const float *draft
     for (int64_t j = 0; j < N; ++j) ord[j] = (int32_t)j;
     g_av_key = key;
     qsort(ord, (size_t)N, sizeof(int32_t), av_cmp);
-    double S = 0.0, best = -INFINITY, second = -INFINITY;
+    uint64_t S = 0;                            /* sum of the top k, in units of 2^-32 */
+    float best = -INFINITY, second = -INFINITY;
     int64_t kbest = 0;
     for (int64_t k = 0; k <= N; ++k) {
-        if (k > 0) S += key[ord[k - 1]] > 0.0f ? (double)key[ord[k - 1]] : 0.0;
-        double c = (double)draft_cost[k] + (double)verify_cost[k];
-        double o = c > 0.0 ? ((double)B + S) / c : -INFINITY;
+        if (k > 0 && key[ord[k - 1]] > 0.0f) S += (uint64_t)llrint((double)key[ord[k - 1]] * 4294967296.0);
+        volatile float c = draft_cost[k] + verify_cost[k];          /* fp32 add, no contraction */
+        volatile float num = (float)((uint64_t)B * 4294967296ull + S);
+        volatile float q = num / c;
+        float o = c > 0.0f ? q * (1.0f / 4294967296.0f) : -INFINITY;
         obj[k] = o;
         if (o > best) { second = best; best = o; kbest = k; }
         else if (o > second) second = o;
@@ -659,7 +668,7 @@ int oracle_av_budget(int32_t B, int32_t K, const float *conf, const float *draft
     for (int64_t j = 0; j < kbest; ++j) draft_len[ord[j] / K] += 1;
     *budget = (int32_t)kbest;
     if (objective) for (int64_t k = 0; k <= N; ++k) objective[k] = obj[k];
-    if (gap) *gap = (best > -INFINITY && second > -INFINITY) ? (best - second) / fabs(best) : INFINITY;
+    if (gap) *gap = (best > -INFINITY && second > -INFINITY) ? ((double)best - second) / fabs((double)best) : INFINITY;
     free(key); free(ord); free(obj);
     return 0;
 }

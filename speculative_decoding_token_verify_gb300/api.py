@@ -114,11 +114,13 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
            fly_theta: float = 0.3, fly_window: int = 6, est_params: Optional[torch.Tensor] = None,
            want_pos_stats: bool = False, want_feature: bool = False, want_conf: bool = False,
            out: Optional[dict] = None, workspace: Optional[Workspace] = None,
-           stream: Optional[torch.cuda.Stream] = None) -> dict:
-    """Run spec_verify. Returns a dict with ``out_tokens`` [B,K+1] int32 and
-    ``accepted_len`` [B] int32, plus ``pos_stats`` [B,K+1,4], ``feature`` [B,K]
-    and ``conf`` [B,K] (float32) when requested. ``out`` may supply
-    preallocated output tensors under the same keys."""
+           stream: Optional[torch.cuda.Stream] = None, draft_len: Optional[torch.Tensor] = None) -> dict:
+    """Run spec_verify (spec_verify_ragged when ``draft_len`` [B] int32 gives
+    the drafts verified per sequence of a pruned batch). Returns a dict with
+    ``out_tokens`` [B,K+1] int32 and ``accepted_len`` [B] int32, plus
+    ``pos_stats`` [B,K+1,4], ``feature`` [B,K] and ``conf`` [B,K] (float32)
+    when requested. ``out`` may supply preallocated output tensors under the
+    same keys."""
     zt = target_logits
     if not zt.is_cuda:
         raise ValueError("target_logits must be a CUDA tensor")
@@ -144,6 +146,10 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
     if est_params is not None:
         if est_params.dtype != torch.float32 or est_params.numel() != K + 1 or est_params.device != dev:
             raise ValueError("est_params must be a float32 [K+1] tensor on the logits' device")
+    if draft_len is not None:
+        if (draft_len.dtype != torch.int32 or tuple(draft_len.shape) != (B,) or not draft_len.is_contiguous()
+                or draft_len.device != dev):
+            raise ValueError("draft_len must be a contiguous int32 [B] tensor on the logits' device")
     o = dict(out or {})
     if "out_tokens" not in o:
         o["out_tokens"] = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
@@ -161,10 +167,17 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
     if nbytes == 0:
         raise SpecError(SPEC_ERR_INVALID_ARG, _native.last_error())
     ws = _ws_for(workspace, nbytes, dev)
-    rc = L.spec_verify(ctypes.byref(p), _ptr(zt), _ptr(draft_logits), _ptr(x), _ptr(uniforms),
-                       _ptr(o["out_tokens"]), _ptr(o["accepted_len"]), _ptr(o.get("pos_stats")),
-                       _ptr(est_params), _ptr(o.get("feature")), _ptr(o.get("conf")),
-                       _ptr(ws), ctypes.c_size_t(ws.numel()), _stream_ptr(stream, dev))
+    if draft_len is None:
+        rc = L.spec_verify(ctypes.byref(p), _ptr(zt), _ptr(draft_logits), _ptr(x), _ptr(uniforms),
+                           _ptr(o["out_tokens"]), _ptr(o["accepted_len"]), _ptr(o.get("pos_stats")),
+                           _ptr(est_params), _ptr(o.get("feature")), _ptr(o.get("conf")),
+                           _ptr(ws), ctypes.c_size_t(ws.numel()), _stream_ptr(stream, dev))
+    else:
+        rc = L.spec_verify_ragged(ctypes.byref(p), _ptr(zt), _ptr(draft_logits), _ptr(x), _ptr(draft_len),
+                                  _ptr(uniforms), _ptr(o["out_tokens"]), _ptr(o["accepted_len"]),
+                                  _ptr(o.get("pos_stats")), _ptr(est_params), _ptr(o.get("feature")),
+                                  _ptr(o.get("conf")), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                  _stream_ptr(stream, dev))
     _check(rc)
     o["_workspace"] = ws
     return o
@@ -194,9 +207,11 @@ def confidence(draft_logits: torch.Tensor, est_params: Optional[torch.Tensor] = 
 
 
 def estimator_update(feature: torch.Tensor, accepted_len: torch.Tensor, est_params: torch.Tensor,
-                     lr: float, want_grad: bool = False, stream: Optional[torch.cuda.Stream] = None):
-    """Run spec_estimator_update in place on ``est_params``. Returns
-    (grad [K+1], counts [K+1]) when ``want_grad``, else None."""
+                     lr: float, want_grad: bool = False, stream: Optional[torch.cuda.Stream] = None,
+                     draft_len: Optional[torch.Tensor] = None):
+    """Run spec_estimator_update (spec_estimator_update_ragged with
+    ``draft_len``) in place on ``est_params``. Returns (grad [K+1], counts
+    [K+1]) when ``want_grad``, else None."""
     B, K = feature.shape
     dev = feature.device
     for t, dt_, shp in ((feature, torch.float32, (B, K)), (accepted_len, torch.int32, (B,)),
@@ -207,8 +222,14 @@ def estimator_update(feature: torch.Tensor, accepted_len: torch.Tensor, est_para
     if want_grad:
         grad = torch.empty(K + 1, dtype=torch.float32, device=dev)
         cnt = torch.empty(K + 1, dtype=torch.int32, device=dev)
-    rc = _native.lib().spec_estimator_update(B, K, _ptr(feature), _ptr(accepted_len), _ptr(est_params),
-                                             float(lr), _ptr(grad), _ptr(cnt), _stream_ptr(stream, dev))
+    if draft_len is None:
+        rc = _native.lib().spec_estimator_update(B, K, _ptr(feature), _ptr(accepted_len), _ptr(est_params),
+                                                 float(lr), _ptr(grad), _ptr(cnt), _stream_ptr(stream, dev))
+    else:
+        _check_draft_len(draft_len, B, dev)
+        rc = _native.lib().spec_estimator_update_ragged(B, K, _ptr(feature), _ptr(accepted_len), _ptr(draft_len),
+                                                        _ptr(est_params), float(lr), _ptr(grad), _ptr(cnt),
+                                                        _stream_ptr(stream, dev))
     _check(rc)
     return (grad, cnt) if want_grad else None
 
@@ -235,9 +256,17 @@ class IrlsState:
         return t[:K + 1], t[K + 1:K + 2], t[K + 2:2 * K + 2], t[2 * K + 2:3 * K + 2], t[3 * K + 2:]
 
 
+def _check_draft_len(draft_len, B, dev):
+    if (draft_len.dtype != torch.int32 or tuple(draft_len.shape) != (B,) or not draft_len.is_contiguous()
+            or draft_len.device != dev):
+        raise ValueError("draft_len must be a contiguous int32 [B] tensor on the same device")
+
+
 def irls_accumulate(feature: torch.Tensor, accepted_len: torch.Tensor, est_params: torch.Tensor,
-                    state: IrlsState, stream: Optional[torch.cuda.Stream] = None):
-    """Add one decoding step's labels to an IRLS round (spec_irls_accumulate)."""
+                    state: IrlsState, stream: Optional[torch.cuda.Stream] = None,
+                    draft_len: Optional[torch.Tensor] = None):
+    """Add one decoding step's labels to an IRLS round (spec_irls_accumulate;
+    spec_irls_accumulate_ragged with ``draft_len``)."""
     B, K = feature.shape
     dev = feature.device
     if K != state.K or state.device != dev:
@@ -246,8 +275,14 @@ def irls_accumulate(feature: torch.Tensor, accepted_len: torch.Tensor, est_param
                         (est_params, torch.float32, (K + 1,))):
         if t.dtype != dt_ or tuple(t.shape) != shp or not t.is_contiguous() or t.device != dev:
             raise ValueError("irls_accumulate: bad tensor (dtype/shape/device/contiguity)")
-    rc = _native.lib().spec_irls_accumulate(B, K, _ptr(feature), _ptr(accepted_len), _ptr(est_params),
-                                            _ptr(state.tensor), _stream_ptr(stream, dev))
+    if draft_len is None:
+        rc = _native.lib().spec_irls_accumulate(B, K, _ptr(feature), _ptr(accepted_len), _ptr(est_params),
+                                                _ptr(state.tensor), _stream_ptr(stream, dev))
+    else:
+        _check_draft_len(draft_len, B, dev)
+        rc = _native.lib().spec_irls_accumulate_ragged(B, K, _ptr(feature), _ptr(accepted_len), _ptr(draft_len),
+                                                       _ptr(est_params), _ptr(state.tensor),
+                                                       _stream_ptr(stream, dev))
     _check(rc)
 
 
@@ -264,6 +299,33 @@ def irls_refit(state: IrlsState, est_params: torch.Tensor, damping: float, want_
                                        _stream_ptr(stream, dev))
     _check(rc)
     return step
+
+
+def av_budget(conf: torch.Tensor, draft_cost: torch.Tensor, verify_cost: torch.Tensor,
+              want_survival: bool = False, want_objective: bool = False,
+              stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Adaptive-verification pruning (spec_av_budget). Returns a dict with
+    ``draft_len`` [B] int32 and ``budget`` [1] int32 (device tensors), plus
+    ``survival`` [B,K] float32 and ``objective`` [B*K+1] float32 when asked."""
+    B, K = conf.shape
+    dev = conf.device
+    if conf.dtype != torch.float32 or not conf.is_contiguous() or not conf.is_cuda:
+        raise ValueError("av_budget: conf must be a contiguous float32 CUDA tensor [B, K]")
+    for t in (draft_cost, verify_cost):
+        if (t.dtype != torch.float32 or tuple(t.shape) != (B * K + 1,) or not t.is_contiguous()
+                or t.device != dev):
+            raise ValueError("av_budget: cost tables must be contiguous float32 [B*K+1] on conf's device")
+    o = {"draft_len": torch.empty(B, dtype=torch.int32, device=dev),
+         "budget": torch.empty(1, dtype=torch.int32, device=dev)}
+    if want_survival:
+        o["survival"] = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if want_objective:
+        o["objective"] = torch.empty(B * K + 1, dtype=torch.float32, device=dev)
+    rc = _native.lib().spec_av_budget(B, K, _ptr(conf), _ptr(draft_cost), _ptr(verify_cost), _ptr(o["draft_len"]),
+                                      _ptr(o["budget"]), _ptr(o.get("survival")), _ptr(o.get("objective")),
+                                      _stream_ptr(stream, dev))
+    _check(rc)
+    return o
 
 
 def device_status(workspace_tensor: torch.Tensor) -> int:

@@ -53,6 +53,7 @@ __device__ void block_sum(float &a, int &n, float *fs, int *is) {
 
 __global__ void __launch_bounds__(NT) estimator_kernel(int B, int K, const float *__restrict__ feature,
                                                        const int32_t *__restrict__ acc_len,
+                                                       const int32_t *__restrict__ draft_len,
                                                        float *__restrict__ params, float lr,
                                                        float *__restrict__ grad_out,
                                                        int32_t *__restrict__ count_out) {
@@ -71,7 +72,8 @@ __global__ void __launch_bounds__(NT) estimator_kernel(int B, int K, const float
         int ni = 0;
         for (int b = tid; b < B; b += NT) {
             const int n = acc_len[b];
-            if (i > n || i >= K) continue;          // not labelled
+            const int kb = draft_len ? min(max(draft_len[b], 0), K) : K;
+            if (i > n || i >= kb) continue;         // not labelled (or never verified)
             const float y = i < n ? 1.f : 0.f;
             const float f = feature[(size_t)b * K + i];
             const float e = 1.f / (1.f + expf(-(omega * f + beta))) - y;
@@ -108,9 +110,9 @@ __global__ void __launch_bounds__(NT) estimator_kernel(int B, int K, const float
 // defined in spec_verify.cu: sets the thread-local message read by spec_last_error
 extern "C" int spec_internal_set_error(int code, const char *msg);
 
-extern "C" int spec_estimator_update(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
-                                     float *est_params, float lr, float *grad_out, int32_t *count_out,
-                                     void *stream) {
+static int estimator_impl(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                          const int32_t *draft_len, float *est_params, float lr, float *grad_out,
+                          int32_t *count_out, void *stream) {
     if (B < 0) return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "B must be >= 0");
     if (K < 1 || K > 1024) return spec_internal_set_error(SPEC_ERR_UNSUPPORTED, "K must be in [1, 1024]");
     if (!est_params) return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "est_params is NULL");
@@ -118,8 +120,22 @@ extern "C" int spec_estimator_update(int32_t B, int32_t K, const float *feature,
         return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "feature / accepted_len is NULL");
     spec_internal_set_error(SPEC_OK, "");
     sv_est::estimator_kernel<<<1, sv_est::NT, 0, static_cast<cudaStream_t>(stream)>>>(
-        B, K, feature, accepted_len, est_params, lr, grad_out, count_out);
+        B, K, feature, accepted_len, draft_len, est_params, lr, grad_out, count_out);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return spec_internal_set_error(SPEC_ERR_CUDA, cudaGetErrorString(e));
     return SPEC_OK;
+}
+
+extern "C" int spec_estimator_update(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                                     float *est_params, float lr, float *grad_out, int32_t *count_out,
+                                     void *stream) {
+    return estimator_impl(B, K, feature, accepted_len, nullptr, est_params, lr, grad_out, count_out, stream);
+}
+
+extern "C" int spec_estimator_update_ragged(int32_t B, int32_t K, const float *feature,
+                                            const int32_t *accepted_len, const int32_t *draft_len,
+                                            float *est_params, float lr, float *grad_out, int32_t *count_out,
+                                            void *stream) {
+    if (B > 0 && !draft_len) return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "draft_len is NULL");
+    return estimator_impl(B, K, feature, accepted_len, draft_len, est_params, lr, grad_out, count_out, stream);
 }

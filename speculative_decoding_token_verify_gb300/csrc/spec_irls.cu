@@ -70,6 +70,7 @@ __device__ __forceinline__ void sigmoid_pair(float z, float &s, float &sn) {
 // small fraction of its fp32 rate.
 __global__ void __launch_bounds__(NT) irls_accumulate_kernel(int B, int K, const float *__restrict__ feature,
                                                             const int32_t *__restrict__ acc_len,
+                                                            const int32_t *__restrict__ draft_len,
                                                             const float *__restrict__ params,
                                                             double *__restrict__ state) {
     // per position: sum e, sum w, sum w f, count; and the slope's sum e f, sum w f^2
@@ -88,6 +89,8 @@ __global__ void __launch_bounds__(NT) irls_accumulate_kernel(int B, int K, const
                 const int b = b0 + 32 * j;
                 nb[j] = b < B ? acc_len[b] : -1;
                 fb[j] = b < B ? feature[(size_t)b * K + i] : 0.f;
+                // a draft at or past the verified length carries no label
+                if (draft_len && b < B && i >= min(max(draft_len[b], 0), K)) nb[j] = -1;
             }
             float be = 0.f, bw = 0.f, bwf = 0.f, bef = 0.f, bwff = 0.f, bc = 0.f;
 #pragma unroll
@@ -225,8 +228,10 @@ int spec_irls_reset(int32_t K, void *state, void *stream) {
     return SPEC_OK;
 }
 
-int spec_irls_accumulate(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
-                         const float *est_params, void *state, void *stream) {
+}  // extern "C"
+
+static int irls_accumulate_impl(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                                const int32_t *draft_len, const float *est_params, void *state, void *stream) {
     if (B < 0) return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "B must be >= 0");
     int rc = irls_check_k(K);
     if (rc != SPEC_OK) return rc;
@@ -237,8 +242,21 @@ int spec_irls_accumulate(int32_t B, int32_t K, const float *feature, const int32
         return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "state must be 8-byte aligned");
     spec_internal_set_error(SPEC_OK, "");
     sv_irls::irls_accumulate_kernel<<<1, sv_irls::NT, 0, static_cast<cudaStream_t>(stream)>>>(
-        B, K, feature, accepted_len, est_params, static_cast<double *>(state));
+        B, K, feature, accepted_len, draft_len, est_params, static_cast<double *>(state));
     return launched();
+}
+
+extern "C" {
+
+int spec_irls_accumulate(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                         const float *est_params, void *state, void *stream) {
+    return irls_accumulate_impl(B, K, feature, accepted_len, nullptr, est_params, state, stream);
+}
+
+int spec_irls_accumulate_ragged(int32_t B, int32_t K, const float *feature, const int32_t *accepted_len,
+                                const int32_t *draft_len, const float *est_params, void *state, void *stream) {
+    if (B > 0 && !draft_len) return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "draft_len is NULL");
+    return irls_accumulate_impl(B, K, feature, accepted_len, draft_len, est_params, state, stream);
 }
 
 int spec_irls_refit(int32_t K, void *state, float *est_params, double damping, double *step_out, void *stream) {

@@ -92,7 +92,9 @@ enum { CTR_CLAIM = 0, CTR_STATUS = 32, CTR_RES_ALLOC = 64, CTR_RES_CLAIM = 96, k
 struct Draw {
     float lse_t, lse_d, u;
     int n;
+    bool bonus;   // all verified drafts accepted: the draw is from p_n alone
 };
+
 
 struct Args {
     const void *zt;
@@ -100,6 +102,7 @@ struct Args {
     long long ts;            // target row stride (elements)
     long long ds;            // draft row stride (elements)
     const int32_t *x;
+    const int32_t *draft_len; // [B] drafts verified per sequence (pruned batch), or null: all K
     const float *u;
     const float *est;
     int32_t *out_tokens;
@@ -128,7 +131,7 @@ struct Args {
     int sstride;             // slice sums per sequence in `slices` (nslice rounded up to 4)
     unsigned *res_ready;     // [B] published flag per slot
     unsigned *res_done;      // [B] residual units completed per sequence
-    float4 *slotrec;         // [B] per published slot: (lse_t, lse_d, u, 32*b + n)
+    float4 *slotrec;         // [B] per published slot: (lse_t, lse_d, u, 64*b + 2*n + bonus)
     float *slices;           // [B][sstride] residual mass per slice
 };
 
@@ -160,6 +163,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+
+// drafts verified for sequence b: draft_len[b] clamped to [0, K], or K
+__device__ __forceinline__ int verified(const Args &a, int b) {
+    return a.draft_len ? min(max(__ldg(a.draft_len + b), 0), a.K) : a.K;
+}
 
 __device__ __forceinline__ void raise_status(const Args &a, unsigned code) {
     atomicMax(a.ctr + CTR_STATUS, code);
@@ -208,6 +216,7 @@ template <typename T>
 struct UnitGeo {
     const T *row;
     int b;            // sequence
+    int r;            // row within the sequence (target rows first)
     int v0, vb, head, ve, tail;
     unsigned bytes;   // body bytes (a multiple of 16)
     bool target;      // a target row (carries the entropy moment)
@@ -222,6 +231,7 @@ __device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit) {
     const int t = (int)(rem - (unsigned)r * (unsigned)a.nT);
     const int TS = a.TS;
     g.b = b;
+    g.r = r;
     g.target = r < a.nt_rows;
     g.row = g.target ? trow_ptr<T>(a, b, r) : drow_ptr<T>(a, b, r - a.nt_rows);
     g.v0 = t * TS;
@@ -361,6 +371,9 @@ __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *
 template <typename T>
 __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) {
     const int K = a.K;
+    // a pruned batch verifies drafts 0..kb-1 against target rows 0..kb
+    // ("Verificación Adaptativa sin una cabeza de confianza", "Antecedentes")
+    const int kb = verified(a, b);
     const float nan = __int_as_float(0x7fc00000);
     // loads that do not depend on the row statistics go out first: the draft
     // token, its uniform and the two logits it indexes
@@ -373,7 +386,7 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
     bool bad_tok = false;
     float ui = 0.f, zx = 0.f, qx = 0.f;
     if (draw && l <= K) ui = a.u[(size_t)b * (K + 1) + l];   // lane K: the residual / bonus uniform
-    if (!conf_only && l < K) {
+    if (!conf_only && l < kb) {
         xi = a.x[(size_t)b * K + l];
         bad_tok = xi < 0 || xi >= a.V;
         if (!bad_tok && a.nd_rows > 0) {
@@ -386,42 +399,42 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
     float lse_t = nan, h = nan, lse_d = nan, f = nan, lr = nan;
     int amax_t = -1;
     bool bad_row = false;
-    if (l < a.nt_rows) {
+    if (l < a.nt_rows && l <= kb) {
         bad_row |= !(tr.M > neg_inf());
         const float lp1 = log1pf(tr.R);
         lse_t = tr.M + lp1;
         h = (lp1 - tr.T * kLn2 / (1.f + tr.R)) * a.inv_log_v;
         amax_t = tr.I;
     }
-    if (l < a.nd_rows) {
+    if (l < a.nd_rows && l < kb) {
         bad_row |= !(dr.M > neg_inf());
         lse_d = dr.M + log1pf(dr.R);
         f = dr.R > 0.f ? -logf(dr.R) : kFeatureClamp;
     }
     if (bad_row) raise_status(a, SPEC_ERR_BAD_ROW);
     if (bad_tok) raise_status(a, SPEC_ERR_BAD_TOKEN);
-    if (!conf_only && l < K && a.nd_rows > 0) lr = bad_tok ? neg_inf() : (zx - lse_t) - (qx - lse_d);
-    int n = K;
+    if (!conf_only && l < kb && a.nd_rows > 0) lr = bad_tok ? neg_inf() : (zx - lse_t) - (qx - lse_d);
+    int n = kb;
     if (a.mode == MODE_STOCHASTIC) {
         // "Математика верификации": accept iff u < min(1, p/q); lr = +inf
         // (q(x) = 0 < p(x)) accepts, NaN (p(x) = q(x) = 0) rejects
-        const bool acc = l < K && (lr >= 0.f || ui < ex2(lr * kLog2e));
-        n = min(__ffs(~__ballot_sync(kFull, acc)) - 1, K);
+        const bool acc = l < kb && (lr >= 0.f || ui < ex2(lr * kLog2e));
+        n = min(__ffs(~__ballot_sync(kFull, acc)) - 1, kb);
     } else if (a.mode == MODE_GREEDY) {
-        const bool acc = l < K && !bad_tok && xi == amax_t;
-        n = min(__ffs(~__ballot_sync(kFull, acc)) - 1, K);
+        const bool acc = l < kb && !bad_tok && xi == amax_t;
+        n = min(__ffs(~__ballot_sync(kFull, acc)) - 1, kb);
     } else if (a.mode == MODE_FLY) {
         // "Training-Free Loosely Speculative Decoding", 2.A: a deviation is
         // excused only if h >= theta, the W-window fits in the draft and holds
         // no further deviation; an invalid token is never excused
-        const bool dev = l < K && (bad_tok || xi != amax_t);
-        const bool open = l < K && !bad_tok && h >= a.theta;
+        const bool dev = l < kb && (bad_tok || xi != amax_t);
+        const bool open = l < kb && !bad_tok && h >= a.theta;
         const unsigned dm = __ballot_sync(kFull, dev);
         const unsigned gm = __ballot_sync(kFull, open);
-        n = K;
-        for (int j = 0; j < K; ++j) {
+        n = kb;
+        for (int j = 0; j < kb; ++j) {
             if (!((dm >> j) & 1u)) continue;
-            bool excused = ((gm >> j) & 1u) && (j + a.W <= K - 1);
+            bool excused = ((gm >> j) & 1u) && (j + a.W <= kb - 1);
             if (excused) {
                 const unsigned win = (a.W >= 32) ? kFull : ((1u << a.W) - 1u);
                 excused = ((dm >> (j + 1)) & win) == 0u;
@@ -437,14 +450,14 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         float *ps = a.pos_stats + ((size_t)b * (K + 1) + l) * 4;
         ps[0] = lse_t;
         ps[1] = h;
-        ps[2] = l < K ? lr : nan;
-        ps[3] = l < K ? f : nan;
+        ps[2] = l < kb ? lr : nan;
+        ps[3] = l < kb ? f : nan;
     }
     if (a.feature && l < a.nd_rows) a.feature[(size_t)b * K + l] = f;
     if (a.conf && a.est && l < a.nd_rows) {
         // "Puntuar la Distribución": sigmoid(omega * logit(q_max) + beta_{i+1})
         const float z = a.est[0] * f + a.est[1 + l];
-        a.conf[(size_t)b * K + l] = 1.f / (1.f + expf(-z));
+        a.conf[(size_t)b * K + l] = l < kb ? 1.f / (1.f + expf(-z)) : nan;
     }
     if (a.mode == MODE_CONF) return;
     const float lt_n = __shfl_sync(kFull, lse_t, n);
@@ -458,7 +471,7 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         if (draw) {
             // hand the draw to the residual units of b; the release store
             // orders the record before the flag
-            a.slotrec[slot] = make_float4(lt_n, ld_n, u_draw, __int_as_float(b * 32 + n));
+            a.slotrec[slot] = make_float4(lt_n, ld_n, u_draw, __int_as_float((b << 6) | (n << 1) | (n == kb ? 1 : 0)));
             st_release(a.res_ready + slot, 1u);
         }
     }
@@ -678,12 +691,13 @@ __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T 
 __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
     const float4 rec = __ldcg(a.slotrec + slot);
     const int bits = __float_as_int(rec.w);
-    b = bits >> 5;
+    b = bits >> 6;
     Draw d;
     d.lse_t = rec.x;
     d.lse_d = rec.y;
     d.u = rec.z;
-    d.n = bits & 31;
+    d.n = (bits >> 1) & 31;
+    d.bonus = (bits & 1) != 0;
     return d;
 }
 
@@ -696,7 +710,7 @@ __device__ __noinline__ void locate(const Args &a, int slot, int l, float4 *buf)
     const Draw d = decode_slot(a, slot, b);
     const int K = a.K;
     const T *tr = trow_ptr<T>(a, b, d.n);
-    const T *dr = d.n < K ? drow_ptr<T>(a, b, d.n) : nullptr;
+    const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
     int token = locate_scan<T>(a, b, tr, dr, d, l, buf);
     if (token < 0 && dr != nullptr) {
         for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T>(a, b, s0, tr, nullptr, d, l);
@@ -726,7 +740,7 @@ __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l)
     int b;
     const Draw d = decode_slot(a, slot, b);
     const T *tr = trow_ptr<T>(a, b, d.n);
-    const T *dr = d.n < a.K ? drow_ptr<T>(a, b, d.n) : nullptr;
+    const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
     unit_sums<T>(a, b, t * res_slices<T>(), tr, dr, d, l);
     ResDone r;
     r.slot = slot;
@@ -847,8 +861,15 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             continue;
         }
         const UnitGeo<T> g = unit_geo<T>(a, unit);
+        // rows a pruned batch never verified are not read (their partial is
+        // empty; the unit still counts toward its sequence's completion)
+        bool skip = false;
+        if (a.draft_len) {
+            const int kb = verified(a, g.b);
+            skip = g.target ? g.r > kb : g.r - a.nt_rows >= kb;
+        }
         // target rows also carry the entropy moment; draft rows do not need it
-        const RowAcc s = g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l);
+        const RowAcc s = skip ? acc_empty() : (g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l));
         const int b = g.b;
         unsigned old = 0u;
         if (l == kSig) {
@@ -1086,10 +1107,12 @@ size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t d
     return pl.bytes;
 }
 
-int spec_verify(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
-                const int32_t *draft_tokens, const float *uniforms, int32_t *out_tokens,
-                int32_t *accepted_len, float *pos_stats, const float *est_params, float *feature,
-                float *conf, void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+static int verify_impl(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
+                       const int32_t *draft_tokens, const int32_t *draft_len, const float *uniforms,
+                       int32_t *out_tokens, int32_t *accepted_len, float *pos_stats, const float *est_params,
+                       float *feature, float *conf, void *workspace, size_t workspace_bytes, void *stream) {
     g_err.clear();
     if (!p) return fail(SPEC_ERR_INVALID_ARG, "params is NULL");
     int rc = check_common(p->B, p->K, p->V, p->dtype);
@@ -1130,6 +1153,7 @@ int spec_verify(const spec_verify_params *p, const void *target_logits, const vo
     a.ts = ts;
     a.ds = ds;
     a.x = draft_tokens;
+    a.draft_len = draft_len;
     a.u = uniforms;
     a.est = est_params;
     a.out_tokens = out_tokens;
@@ -1149,6 +1173,28 @@ int spec_verify(const spec_verify_params *p, const void *target_logits, const vo
     a.t_vec_ok = vec_ok(target_logits, ts, es);
     a.d_vec_ok = draft_logits ? vec_ok(draft_logits, ds, es) : 0;
     return launch(a, pl, p->dtype, workspace, stream);
+}
+
+extern "C" {
+
+int spec_verify(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
+                const int32_t *draft_tokens, const float *uniforms, int32_t *out_tokens,
+                int32_t *accepted_len, float *pos_stats, const float *est_params, float *feature,
+                float *conf, void *workspace, size_t workspace_bytes, void *stream) {
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, nullptr, uniforms, out_tokens, accepted_len,
+                       pos_stats, est_params, feature, conf, workspace, workspace_bytes, stream);
+}
+
+int spec_verify_ragged(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
+                       const int32_t *draft_tokens, const int32_t *draft_len, const float *uniforms,
+                       int32_t *out_tokens, int32_t *accepted_len, float *pos_stats, const float *est_params,
+                       float *feature, float *conf, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!draft_len) {
+        g_err = "draft_len is NULL";
+        return SPEC_ERR_INVALID_ARG;
+    }
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, uniforms, out_tokens,
+                       accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes, stream);
 }
 
 int spec_confidence(int32_t B, int32_t K, int32_t V, int32_t dtype, const void *draft_logits,

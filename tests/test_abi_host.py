@@ -203,6 +203,23 @@ def test_irls_validation(L):
     assert L.spec_last_error()
 
 
+def test_av_and_ragged_validation(L):
+    P = ctypes.c_void_p
+    F = P(_FAKE)
+    assert L.spec_av_budget(0, 4, F, F, F, F, F, None, None, None) == 1
+    assert L.spec_av_budget(4, 0, F, F, F, F, F, None, None, None) == 1
+    assert L.spec_av_budget(1024, 17, F, F, F, F, F, None, None, None) == 2      # B*K > 16384
+    assert L.spec_av_budget(4, 4, None, F, F, F, F, None, None, None) == 1
+    assert L.spec_av_budget(4, 4, F, F, F, None, F, None, None, None) == 1
+    assert L.spec_av_budget(4, 4, F, F, F, F, None, None, None, None) == 1
+    p = sv.make_params(4, 2, 1000, 1)
+    assert L.spec_verify_ragged(ctypes.byref(p), F, F, F, None, F, F, F, None, None, None, None, F, 1 << 24,
+                                None) == 1
+    assert L.spec_estimator_update_ragged(4, 2, F, F, None, F, 0.05, None, None, None) == 1
+    assert L.spec_irls_accumulate_ragged(4, 2, F, F, None, F, F, None) == 1
+    assert L.spec_last_error()
+
+
 def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(_native, "_lib", None)
     monkeypatch.setattr(_native, "LIB_PATH", "/nonexistent/libspecverify.so")
