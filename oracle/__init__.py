@@ -63,6 +63,8 @@ def _load():
     lib.oracle_estimator_loss.argtypes = [i32, i32, P, P, P, P]
     lib.oracle_irls_accumulate.restype = ctypes.c_int
     lib.oracle_irls_accumulate.argtypes = [i32, i32, P, P, P, P, P, P, P]
+    lib.oracle_ngram_draft.restype = ctypes.c_int
+    lib.oracle_ngram_draft.argtypes = [i32, i32, P, P, i32, i32, i32, P, P]
     lib.oracle_av_budget.restype = ctypes.c_int
     lib.oracle_av_budget.argtypes = [i32, i32, P, P, P, P, P, P, P, P]
     lib.oracle_irls_refit.restype = ctypes.c_int
@@ -225,6 +227,22 @@ def irls_refit(state, params, damping):
     if rc != 0:
         raise ValueError("oracle_irls_refit rejected its arguments (%d)" % rc)
     return p, step
+
+
+def ngram_draft(ctx, lengths, n_min, n_max, K):
+    """Prompt-lookup drafts: returns (draft_tokens [B,K] int32, -1 padded;
+    draft_len [B] int32)."""
+    lib = _load()
+    c = np.ascontiguousarray(ctx, dtype=np.int32)
+    B, ld = c.shape
+    ln = np.ascontiguousarray(lengths, dtype=np.int32)
+    assert ln.shape == (B,)
+    toks = np.empty((B, K), np.int32)
+    dl = np.empty(B, np.int32)
+    rc = lib.oracle_ngram_draft(B, ld, _ptr(c), _ptr(ln), int(n_min), int(n_max), int(K), _ptr(toks), _ptr(dl))
+    if rc != 0:
+        raise ValueError("oracle_ngram_draft rejected its arguments")
+    return toks, dl
 
 
 def av_budget(conf, draft_cost, verify_cost):

@@ -673,6 +673,47 @@ int oracle_av_budget(int32_t B, int32_t K, const float *conf, const float *draft
     return 0;
 }
 
+/* N-gram (prompt-lookup) drafting ("Speculative Decoding: как черновая модель
+ * ускоряет генерацию LLM без потери качества", section "N-gram (prompt
+ * lookup)"; the FLy page's "Aceleração Multinível" drafts this way): the
+ * drafts are read from the context itself, the tokens that followed an
+ * earlier occurrence of the context's last n tokens. Readings (the pages do
+ * not say): n runs from n_max down to n_min and the first n with a match
+ * wins (the longest match); among its matches the most recent occurrence is
+ * taken (the one that ends last, before the context's end); up to K tokens
+ * that follow it are proposed (fewer if the context ends first); no match
+ * proposes nothing.
+ * ctx [B][ld] int32 (sequence b's context is ctx[b][0 .. len[b]-1]),
+ * draft_tokens [B][K] out (-1 past draft_len), draft_len [B] out.
+ * 1 <= n_min <= n_max; 0 <= len[b] <= ld. */
+int oracle_ngram_draft(int32_t B, int32_t ld, const int32_t *ctx, const int32_t *len, int32_t n_min,
+                       int32_t n_max, int32_t K, int32_t *draft_tokens, int32_t *draft_len) {
+    if (B < 0 || ld < 0 || K < 1 || n_min < 1 || n_max < n_min || !draft_tokens || !draft_len) return -1;
+    if (B > 0 && (!ctx || !len)) return -1;
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t *c = ctx + (size_t)b * ld;
+        const int32_t L = len[b];
+        if (L < 0 || L > ld) return -1;
+        int32_t start = -1;                   /* first proposed token's index */
+        for (int32_t n = n_max; n >= n_min && start < 0; --n) {
+            if (n > L - 1) continue;          /* the query and an earlier copy must fit */
+            for (int32_t e = L - 1; e >= n; --e) {        /* occurrence c[e-n .. e-1], follow-up from e */
+                int32_t t = 0;
+                while (t < n && c[e - n + t] == c[L - n + t]) ++t;
+                if (t == n) { start = e; break; }
+            }
+        }
+        int32_t m = 0;
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t tok = -1;
+            if (start >= 0 && start + k < L) { tok = c[start + k]; ++m; }
+            draft_tokens[(size_t)b * K + k] = tok;
+        }
+        draft_len[b] = m;
+    }
+    return 0;
+}
+
 /* Row statistics of `rows` rows of V logits each (row r at z + r*stride):
  * lse, normalised entropy, argmax, logit(q_max). Any output may be NULL. */
 int oracle_row_stats(int64_t rows, int32_t V, int dtype, const void *z, int64_t stride,
