@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--ngram", action="store_true",
+                    help="also time prompt-lookup drafting (spec_ngram_draft) for this workload's B and K")
     ap.add_argument("--av", action="store_true",
                     help="also time adaptive-verification pruning (spec_av_budget) and the pruned verify")
     ap.add_argument("--irls", action="store_true",
@@ -408,6 +410,8 @@ def run_ours(args, w, world, rank, local, pg):
     }
     if args.irls and w.with_confidence:
         line["irls"] = time_irls(w, out, est, dev, stream)
+    if args.ngram:
+        line["ngram"] = time_ngram(w, dev, stream, args.seed)
     if args.av and w.with_confidence and w.mode == "stochastic":
         line["av"] = time_av(w, inp, zd, u, out, est, ws, dev, stream, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -454,6 +458,29 @@ def time_irls(w, out, est, dev, stream, round_steps=64, damping=16.0, reps=20):
     return {"accumulate_us_per_step": acc_us, "refit_us_per_round": ref_us, "round_steps": round_steps,
             "damping": damping, "B": w.B, "K": w.K,
             "note": "launch-bound O(B*K) work; one CTA each"}
+
+
+def time_ngram(w, dev, stream, seed, ld=4096, reps=50):
+    """Device time of prompt-lookup drafting for this workload's B sequences
+    of `ld` context tokens (synthetic: uniform tokens with a planted repeat
+    of 4..40 tokens in every other sequence), n in [1, 4], K drafts."""
+    import numpy as np
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+
+    rng = np.random.default_rng(seed + 17)
+    ctx = rng.integers(0, w.V, (w.B, ld)).astype(np.int32)
+    for b in range(0, w.B, 2):
+        n = int(rng.integers(4, 41))
+        a = int(rng.integers(0, ld // 2))
+        ctx[b, ld - n:] = ctx[b, a:a + n]
+    c = torch.tensor(ctx, device=dev)
+    ln = torch.full((w.B,), ld, dtype=torch.int32, device=dev)
+    d = sv.ngram_draft(c, ln, 1, 4, w.K)
+    us = device_us(lambda: sv.ngram_draft(c, ln, 1, 4, w.K), stream, reps)
+    return {"us": us, "B": w.B, "context": ld, "n": [1, 4], "K": w.K,
+            "mean_draft_len": float(d["draft_len"].float().mean().item())}
 
 
 def time_av(w, inp, zd, u, out, est, ws, dev, stream, peak, reps=50):

@@ -234,6 +234,24 @@ int spec_av_budget(int32_t B, int32_t K, const float *conf, const float *draft_c
                    int32_t *draft_len, int32_t *budget, float *survival, float *objective, void *stream);
 
 /*
+ * N-gram (prompt-lookup) drafting ([SD] "N-gram (prompt lookup)"; FLy's
+ * "Aceleração Multinível" drafts this way): the drafts of sequence b are the
+ * tokens that followed an earlier occurrence of its context's last n tokens.
+ * n runs from n_max down to n_min and the longest match wins; among its
+ * matches the most recent occurrence (ending last, before the context
+ * does); up to K following tokens are proposed (fewer when the context
+ * ends first); no match proposes none. The drafts carry no distribution, so
+ * they are verified with spec_verify_ragged in greedy or FLy mode, with
+ * draft_len from here.
+ * ctx [B][ld] int32 (sequence b's context is ctx[b][0 .. len[b]-1], len
+ * clamped to [0, ld]), draft_tokens [B][K] int32 out (-1 past the drafts),
+ * draft_len [B] int32 out. 1 <= n_min <= n_max, K >= 1. One warp per
+ * sequence, integer work: exact. Asynchronous on `stream`.
+ */
+int spec_ngram_draft(int32_t B, int32_t ld, const int32_t *ctx, const int32_t *len, int32_t n_min, int32_t n_max,
+                     int32_t K, int32_t *draft_tokens, int32_t *draft_len, void *stream);
+
+/*
  * spec_verify for a pruned batch: sequence b submitted only its first
  * draft_len[b] drafts for verification ([AV]: a subset of the drafts is
  * verified; the target ran with variable-length sequences). draft_len [B]

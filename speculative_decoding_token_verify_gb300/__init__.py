@@ -8,5 +8,6 @@ built, every call raises.
 from ._native import build, lib, LIB_PATH  # noqa: F401
 from .api import (  # noqa: F401
     BF16, F32, FLY, GREEDY, MAX_K, MAX_V, MODES, STOCHASTIC, IrlsState, SpecError, Workspace, av_budget,
-    confidence, device_status, estimator_update, irls_accumulate, irls_refit, make_params, verify, workspace_size,
+    confidence, device_status, estimator_update, irls_accumulate, irls_refit, make_params, ngram_draft, verify,
+    workspace_size,
 )

@@ -18,7 +18,7 @@ _ROOT = os.path.dirname(_PKG)
 _CSRC = os.path.join(_PKG, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
-SOURCES = ("spec_verify.cu", "spec_estimator.cu", "spec_irls.cu", "spec_av.cu")
+SOURCES = ("spec_verify.cu", "spec_estimator.cu", "spec_irls.cu", "spec_av.cu", "spec_ngram.cu")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
@@ -107,6 +107,7 @@ SIGNATURES = {
     "spec_estimator_update_ragged": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "spec_irls_accumulate_ragged": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P, _P]),
     "spec_av_budget": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "spec_ngram_draft": (ctypes.c_int, [_I32, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "spec_irls_state_size": (ctypes.c_size_t, [_I32]),
     "spec_irls_reset": (ctypes.c_int, [_I32, _P, _P]),
     "spec_irls_accumulate": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P]),

@@ -301,6 +301,24 @@ def irls_refit(state: IrlsState, est_params: torch.Tensor, damping: float, want_
     return step
 
 
+def ngram_draft(ctx: torch.Tensor, lengths: torch.Tensor, n_min: int, n_max: int, K: int,
+                stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Prompt-lookup drafts (spec_ngram_draft): returns a dict with
+    ``draft_tokens`` [B,K] int32 (-1 padded) and ``draft_len`` [B] int32."""
+    B, ld = ctx.shape
+    dev = ctx.device
+    if ctx.dtype != torch.int32 or not ctx.is_contiguous() or not ctx.is_cuda:
+        raise ValueError("ngram_draft: ctx must be a contiguous int32 CUDA tensor [B, ld]")
+    if lengths.dtype != torch.int32 or tuple(lengths.shape) != (B,) or lengths.device != dev:
+        raise ValueError("ngram_draft: lengths must be an int32 [B] tensor on ctx's device")
+    o = {"draft_tokens": torch.empty((B, K), dtype=torch.int32, device=dev),
+         "draft_len": torch.empty(B, dtype=torch.int32, device=dev)}
+    rc = _native.lib().spec_ngram_draft(B, ld, _ptr(ctx), _ptr(lengths.contiguous()), int(n_min), int(n_max), int(K),
+                                        _ptr(o["draft_tokens"]), _ptr(o["draft_len"]), _stream_ptr(stream, dev))
+    _check(rc)
+    return o
+
+
 def av_budget(conf: torch.Tensor, draft_cost: torch.Tensor, verify_cost: torch.Tensor,
               want_survival: bool = False, want_objective: bool = False,
               stream: Optional[torch.cuda.Stream] = None) -> dict:

@@ -217,7 +217,13 @@ def test_av_and_ragged_validation(L):
                                 None) == 1
     assert L.spec_estimator_update_ragged(4, 2, F, F, None, F, 0.05, None, None, None) == 1
     assert L.spec_irls_accumulate_ragged(4, 2, F, F, None, F, F, None) == 1
-    assert L.spec_last_error()
+    assert L.spec_ngram_draft(-1, 8, F, F, 1, 2, 4, F, F, None) == 1
+    assert L.spec_ngram_draft(4, 8, F, F, 0, 2, 4, F, F, None) == 1
+    assert L.spec_ngram_draft(4, 8, F, F, 3, 2, 4, F, F, None) == 1
+    assert L.spec_ngram_draft(4, 8, F, F, 1, 2, 0, F, F, None) == 1
+    assert L.spec_ngram_draft(4, 8, None, F, 1, 2, 4, F, F, None) == 1
+    assert L.spec_ngram_draft(0, 8, None, None, 1, 2, 4, None, None, None) == 0
+    assert L.spec_last_error() is not None
 
 
 def test_missing_library_fails_loudly(monkeypatch):
