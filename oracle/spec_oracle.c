@@ -66,10 +66,11 @@ static double logit_at(const void *row, int dtype, int64_t v) {
  * target's and the draft's next-token distributions). Writes p[0..V) and
  * returns lse = m + log(sum). Returns 0 and sets *ok = 0 when no logit is
  * finite. */
-static double softmax_row(const void *row, int dtype, int32_t V, double *p, int *ok) {
+static double softmax_row(const void *row, int dtype, int32_t V, double sc, double *p, int *ok) {
+    /* softmax of sc * z (sc: the inverse sampling temperature, 1 by default) */
     double m = -INFINITY;
     for (int32_t v = 0; v < V; ++v) {
-        double z = logit_at(row, dtype, v);
+        double z = sc * logit_at(row, dtype, v);
         if (z > m) m = z;
     }
     if (!(m > -INFINITY) || isinf(m)) {
@@ -79,7 +80,7 @@ static double softmax_row(const void *row, int dtype, int32_t V, double *p, int 
     }
     double s = 0.0;
     for (int32_t v = 0; v < V; ++v) {
-        p[v] = exp(logit_at(row, dtype, v) - m);
+        p[v] = exp(sc * logit_at(row, dtype, v) - m);
         s += p[v];
     }
     for (int32_t v = 0; v < V; ++v) p[v] /= s;
@@ -167,7 +168,7 @@ static double dmin(double a, double b) { return a < b ? a : b; }
  *  zd: K draft rows (NULL allowed in greedy / FLy mode).
  *  x:  K draft tokens.  u: K+1 uniforms (NULL allowed in greedy / FLy mode).
  * Scratch: p, q, r of V doubles each. */
-static void verify_one(int32_t K, int32_t Kb, int32_t V, int dtype, int mode,
+static void verify_one(int32_t K, int32_t Kb, double sc, int32_t V, int dtype, int mode,
                        const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
                        const int32_t *x, const float *u, double fly_theta, int32_t fly_window,
                        const double *est, int32_t *out_tokens, int32_t *acc_len,
@@ -195,18 +196,18 @@ static void verify_one(int32_t K, int32_t Kb, int32_t V, int dtype, int mode,
     for (int32_t j = 0; j <= Kb; ++j) {
         const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
         int ok;
-        double lse_t = softmax_row(trow, dtype, V, p, &ok);
+        double lse_t = softmax_row(trow, dtype, V, sc, p, &ok);
         if (!ok) fl |= OR_FLAG_BAD_ROW;
         double h = norm_entropy(p, V);
         double lr = NAN, f = NAN;
         if (j < Kb && zd) {
             const void *drow = dbase + (size_t)j * (size_t)d_stride * es;
             int okd;
-            double lse_d = softmax_row(drow, dtype, V, q, &okd);
+            double lse_d = softmax_row(drow, dtype, V, sc, q, &okd);
             if (!okd) fl |= OR_FLAG_BAD_ROW;
             int32_t amax_d = argmax_row(drow, dtype, V);
             f = logit_qmax(q, V, amax_d, &fl);
-            lr = (logit_at(trow, dtype, x[j]) - lse_t) - (logit_at(drow, dtype, x[j]) - lse_d);
+            lr = (sc * logit_at(trow, dtype, x[j]) - lse_t) - (sc * logit_at(drow, dtype, x[j]) - lse_d);
             if (feature) feature[j] = f;
             /* [AV] "Puntuar la Distribución": confidence = sigmoid of the
              * shared slope times logit(q_max) plus the position's intercept;
@@ -233,8 +234,8 @@ static void verify_one(int32_t K, int32_t Kb, int32_t V, int dtype, int mode,
             const void *trow = tbase + (size_t)i * (size_t)t_stride * es;
             const void *drow = dbase + (size_t)i * (size_t)d_stride * es;
             int ok;
-            softmax_row(trow, dtype, V, p, &ok);
-            softmax_row(drow, dtype, V, q, &ok);
+            softmax_row(trow, dtype, V, sc, p, &ok);
+            softmax_row(drow, dtype, V, sc, q, &ok);
             double px = p[x[i]], qx = q[x[i]];
             double acc;
             if (qx > 0.0) {
@@ -269,7 +270,7 @@ static void verify_one(int32_t K, int32_t Kb, int32_t V, int dtype, int mode,
              * draw always uses u[K]). */
             const void *trow = tbase + (size_t)Kb * (size_t)t_stride * es;
             int ok;
-            softmax_row(trow, dtype, V, p, &ok);
+            softmax_row(trow, dtype, V, sc, p, &ok);
             double Z = 0.0;
             for (int32_t v = 0; v < V; ++v) Z += p[v];
             token = inverse_cdf(p, V, Z, (double)u[K], &mc, &fl);
@@ -298,7 +299,7 @@ static void verify_one(int32_t K, int32_t Kb, int32_t V, int dtype, int mode,
             int32_t a = argmax_row(trow, dtype, V);
             if (x[j] == a) continue;               /* no deviation: accept j */
             int ok;
-            softmax_row(trow, dtype, V, p, &ok);
+            softmax_row(trow, dtype, V, sc, p, &ok);
             double h = norm_entropy(p, V);
             mg = dmin(mg, fabs(h - fly_theta));
             int reject;
@@ -343,7 +344,14 @@ static void verify_one(int32_t K, int32_t Kb, int32_t V, int dtype, int mode,
  *  flags [B] or NULL (OR_FLAG_* bits),
  *  draft_len [B] or NULL: drafts submitted for verification per sequence,
  *    in [0, K] (NULL: all K). Sequence b verifies drafts 0..draft_len[b]-1
- *    against target rows 0..draft_len[b]; the rest of its outputs are NaN/-1.
+ *    against target rows 0..draft_len[b]; the rest of its outputs are NaN/-1,
+ *  inv_temp [B] or NULL: per-sequence inverse sampling temperature (> 0).
+ *    Verification then runs on the temperature-processed distributions
+ *    p = softmax(z / T) and q = softmax(y / T) of sequence b ([AV]
+ *    "Benchmarks": the pages serve at a sampling temperature; speculative
+ *    sampling is lossless for whatever p and q it is given). Argmax is
+ *    unchanged; lse, entropy, the log-ratio and logit(q_max) are those of
+ *    the processed distributions. NULL: temperature 1.
  * nthreads > 0 sets the OpenMP thread count. Returns 0, or -1 on bad args. */
 int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
@@ -351,8 +359,11 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const double *est, int32_t *out_tokens, int32_t *accepted_len,
                   double *pos_stats, double *conf, double *feature,
                   double *margin_acc, double *margin_cdf, double *cdf, int32_t *flags,
-                  const int32_t *draft_len, int nthreads) {
+                  const int32_t *draft_len, const float *inv_temp, int nthreads) {
     if (B < 0 || K < 1 || V < 2 || !zt || !x || !out_tokens || !accepted_len) return -1;
+    if (inv_temp)
+        for (int32_t b = 0; b < B; ++b)
+            if (!(inv_temp[b] > 0.0f) || isinf(inv_temp[b])) return -1;
     if (draft_len)
         for (int32_t b = 0; b < B; ++b)
             if (draft_len[b] < 0 || draft_len[b] > K) return -1;
@@ -373,7 +384,7 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
 #pragma omp for schedule(static)
             for (int32_t b = 0; b < B; ++b) {
                 int fl = 0;
-                verify_one(K, draft_len ? draft_len[b] : K, V, dtype, mode,
+                verify_one(K, draft_len ? draft_len[b] : K, inv_temp ? (double)inv_temp[b] : 1.0, V, dtype, mode,
                            (const char *)zt + (size_t)b * (size_t)(K + 1) * (size_t)t_stride * es, t_stride,
                            zd ? (const char *)zd + (size_t)b * (size_t)K * (size_t)d_stride * es : NULL, d_stride,
                            x + (size_t)b * K, u ? u + (size_t)b * (K + 1) : NULL, fly_theta, fly_window,
@@ -417,7 +428,7 @@ int oracle_confidence(int32_t B, int32_t K, int32_t V, int dtype, const void *zd
                 for (int32_t i = 0; i < K; ++i) {
                     const void *drow = (const char *)zd + ((size_t)b * K + i) * (size_t)d_stride * es;
                     int ok;
-                    softmax_row(drow, dtype, V, q, &ok);
+                    softmax_row(drow, dtype, V, 1.0, q, &ok);
                     if (!ok) fl |= OR_FLAG_BAD_ROW;
                     double f = logit_qmax(q, V, argmax_row(drow, dtype, V), &fl);
                     feature[(size_t)b * K + i] = f;
@@ -733,7 +744,7 @@ int oracle_row_stats(int64_t rows, int32_t V, int dtype, const void *z, int64_t 
             for (int64_t r = 0; r < rows; ++r) {
                 const void *row = (const char *)z + (size_t)r * (size_t)stride * es;
                 int ok, fl = 0;
-                double l = softmax_row(row, dtype, V, p, &ok);
+                double l = softmax_row(row, dtype, V, 1.0, p, &ok);
                 int32_t a = argmax_row(row, dtype, V);
                 if (lse) lse[r] = ok ? l : NAN;
                 if (entropy) entropy[r] = ok ? norm_entropy(p, V) : NAN;
