@@ -47,7 +47,7 @@
 #define OR_FLAG_Q_ZERO 1     /* q(x_i) == 0 at a tested position            */
 #define OR_FLAG_Z_ZERO 2     /* residual mass 0 after a reject: fell back to p */
 #define OR_FLAG_CDF_FALLBACK 4 /* no cumulative value exceeded u*Z           */
-#define OR_FLAG_REST_ZERO 8  /* q_max == 1 exactly: logit(q_max) clamped      */
+#define OR_FLAG_REST_ZERO 8  /* logit(q_max) capped at 30 (q_max ~ 1)          */
 #define OR_FLAG_BAD_ROW 16   /* a row with no finite logit                    */
 
 /* logit(q_max) when the complement mass is exactly zero */
@@ -112,16 +112,21 @@ static double norm_entropy(const double *p, int32_t V) {
 
 /* logit(q_max) = ln q_max - ln(sum_{v != argmax} q_v) ([AV] "Puntuar la
  * Distribución": the feature is the log-odds of the draft's most likely
- * token). The complement is summed directly rather than formed as 1 - q_max. */
+ * token). The complement is summed directly rather than formed as 1 - q_max.
+ * Reading: the feature is capped at OR_F_CLAMP (30, q_max within 1e-13 of 1);
+ * the pages give no value for that regime, and the cap keeps the feature
+ * continuous where the complement underflows (fp64 beyond 708, fp32 beyond
+ * 87). Capped values are flagged. */
 static double logit_qmax(const double *q, int32_t V, int32_t amax, int *flags) {
     double rest = 0.0;
     for (int32_t v = 0; v < V; ++v)
         if (v != amax) rest += q[v];
-    if (rest <= 0.0) {
+    const double f = rest > 0.0 ? log(q[amax]) - log(rest) : INFINITY;
+    if (f >= OR_F_CLAMP) {
         *flags |= OR_FLAG_REST_ZERO;
         return OR_F_CLAMP;
     }
-    return log(q[amax]) - log(rest);
+    return f;
 }
 
 /* Inverse-CDF draw from the unnormalised weights r[0..V) with total Z: the

@@ -249,6 +249,15 @@ def test_logit_qmax_clamps_when_complement_vanishes():
     assert fq[0] == 30.0
 
 
+@pytest.mark.parametrize("gap", [5.0, 29.5, 30.5, 100.0, 800.0])
+def test_logit_qmax_is_capped_at_30(gap):
+    # a two-token row (0, -gap): q_max / (1 - q_max) = e^gap exactly, so
+    # logit(q_max) = gap; the reading caps it at 30 (and flags the cap)
+    z = np.array([[0.0, -gap]], np.float32)
+    _, _, _, fq = oracle.row_stats(z)
+    assert abs(fq[0] - min(gap, 30.0)) < 1e-9
+
+
 def test_log_ratio_matches_logsumexp():
     rng = np.random.default_rng(21)
     B, K, V = 8, 3, 500
