@@ -51,6 +51,9 @@ def parse_args():
                     help="also time prompt-lookup drafting (spec_ngram_draft) for this workload's B and K")
     ap.add_argument("--av", action="store_true",
                     help="also time adaptive-verification pruning (spec_av_budget) and the pruned verify")
+    ap.add_argument("--temperature", action="store_true",
+                    help="also time temperature-processed verification (spec_verify_temperature) on this "
+                         "workload, inverse temperatures log-uniform on [0.5, 2]")
     ap.add_argument("--irls", action="store_true",
                     help="also time the IRLS refit entry points (spec_irls_*) on this workload's B, K")
     return ap.parse_args()
@@ -414,6 +417,9 @@ def run_ours(args, w, world, rank, local, pg):
         line["ngram"] = time_ngram(w, dev, stream, args.seed)
     if args.av and w.with_confidence and w.mode == "stochastic":
         line["av"] = time_av(w, inp, zd, u, out, est, ws, dev, stream, peak)
+    if args.temperature:
+        line["temperature"] = time_temperature(w, args.seed, out, est, ws, dev, stream, peak, logit_bytes,
+                                               kern_s * 1e3)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
     if rank == 0:
@@ -519,6 +525,47 @@ def time_av(w, inp, zd, u, out, est, ws, dev, stream, peak, reps=50):
             "pruned_verify_ms": v_ms, "pruned_bytes": pruned_bytes,
             "pruned_frac": pruned_bytes / (v_ms / 1e3) / 1e9 / peak,
             "cost_table": "draft 0.01 k/B, verify 1 + 0.05 k/B (synthetic)", "est": "omega 0.5, beta 1.5"}
+
+
+def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, default_ms, reps=100):
+    """Device time of one verification at per-sequence inverse temperatures
+    (log-uniform on [0.5, 2]; drafts drawn from the processed q), CUDA events
+    on the launching stream over `reps` back-to-back launches; the inputs
+    (same shapes and logits as the main line) are larger than L2."""
+    import statistics as st
+
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+    import workloads
+
+    wt = w.scaled(inv_temp_range=(0.5, 2.0))
+    inp = workloads.make_inputs(wt, seed, dev)
+    with_draft = w.mode == "stochastic" or w.with_confidence
+    zd = inp["zd"] if with_draft else None
+    u = inp["u"] if w.mode == "stochastic" else None
+    o = dict(out)
+
+    def call():
+        sv.verify(inp["zt"], zd, inp["x"], u, mode=w.mode, fly_theta=w.fly_theta, fly_window=w.fly_window,
+                  est_params=est if w.with_confidence else None, out=o, workspace=ws,
+                  want_feature=w.with_confidence, want_conf=w.with_confidence, inv_temperature=inp["inv_temp"])
+
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = st.mean(ms)
+    del inp
+    return {"verify_ms_mean": mean_ms, "verify_ms_median": st.median(ms),
+            "frac": logit_bytes / (mean_ms / 1e3) / 1e9 / peak, "default_verify_ms_mean": default_ms,
+            "inv_temperature": "log-uniform [0.5, 2] per sequence", "kernel": "verify_kernel<T, temperature>"}
 
 
 def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):

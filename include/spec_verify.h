@@ -63,11 +63,14 @@ extern "C" {
 #define SPEC_ERR_TIMEOUT 4       /* device status: a bounded wait gave up   */
 #define SPEC_ERR_BAD_ROW 5       /* device status: a row had no finite logit */
 #define SPEC_ERR_BAD_TOKEN 6     /* device status: a draft token was outside [0,V) */
+#define SPEC_ERR_BAD_TEMPERATURE 7 /* device status: an inverse temperature was out of range */
 
 /* limits */
 #define SPEC_MAX_K 31            /* draft positions per sequence            */
 #define SPEC_MAX_V (1 << 20)     /* vocabulary size                         */
 #define SPEC_STATIC_SCRATCH_BYTES (16u << 20) /* scratch of spec_verify_static */
+#define SPEC_MIN_INV_TEMPERATURE 1.0e-4f  /* inverse temperature range of   */
+#define SPEC_MAX_INV_TEMPERATURE 1.0e4f   /* spec_verify_temperature        */
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
@@ -118,7 +121,8 @@ size_t spec_workspace_size(const spec_verify_params *params);
  *                                 entropy of target row j, log p(x_j) - log q(x_j),
  *                                 logit(q_max) of draft row j); the last two are
  *                                 NaN at j = K and without draft logits.
- *   feature       [B][K] f32 or NULL: logit(q_max) of every draft row.
+ *   feature       [B][K] f32 or NULL: logit(q_max) of every draft row,
+ *                                 capped at 30 (q_max within 1e-13 of 1).
  *   conf          [B][K] f32 or NULL: sigmoid(omega*feature + beta_{i+1});
  *                                 needs est_params and draft_logits.
  * Rules:
@@ -267,6 +271,31 @@ int spec_verify_ragged(const spec_verify_params *params, const void *target_logi
                        const int32_t *draft_tokens, const int32_t *draft_len, const float *uniforms,
                        int32_t *out_tokens, int32_t *accepted_len, float *pos_stats, const float *est_params,
                        float *feature, float *conf, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify at a sampling temperature ([AV] "Benchmarks": the serving
+ * setting samples at a temperature; [SD] "Математика верификации": the rule
+ * is lossless for whatever distributions the two models sample from).
+ * inv_temperature [B] f32 on the device holds s_b = 1/T_b per sequence, in
+ * [SPEC_MIN_INV_TEMPERATURE, SPEC_MAX_INV_TEMPERATURE]. Both models' rows of
+ * sequence b are processed as p = softmax(s_b z), q = softmax(s_b y) before
+ * every use: the acceptance ratio, the residual and bonus draws, the FLy
+ * entropy, logit(q_max) and pos_stats' lse and log-ratio all read the
+ * processed distributions (argmax decisions do not change). The caller draws
+ * the drafts from the processed q. draft_len may be NULL (all K verified) or
+ * as for spec_verify_ragged. A value outside the range (or NaN) runs that
+ * sequence at s = 1 and sets SPEC_ERR_BAD_TEMPERATURE in the status word.
+ * Everything else is spec_verify's. Exponents are formed difference first,
+ * (z - M) s log2e, so that accuracy does not degrade with |s z|; at s = 1
+ * results therefore agree with spec_verify's to a few fp32 roundings, not
+ * bit for bit. An inverse temperature 2^k on z gives the bits of s = 1 on
+ * 2^k z.
+ */
+int spec_verify_temperature(const spec_verify_params *params, const void *target_logits,
+                            const void *draft_logits, const int32_t *draft_tokens, const int32_t *draft_len,
+                            const float *inv_temperature, const float *uniforms, int32_t *out_tokens,
+                            int32_t *accepted_len, float *pos_stats, const float *est_params, float *feature,
+                            float *conf, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * spec_estimator_update and spec_irls_accumulate for a pruned batch: only

@@ -104,6 +104,8 @@ SIGNATURES = {
     "spec_estimator_update": (ctypes.c_int, [_I32, _I32, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "spec_verify_ragged": (ctypes.c_int, [ctypes.POINTER(VerifyParams), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                           _P, _P, ctypes.c_size_t, _P]),
+    "spec_verify_temperature": (ctypes.c_int, [ctypes.POINTER(VerifyParams), _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                               _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "spec_estimator_update_ragged": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "spec_irls_accumulate_ragged": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P, _P]),
     "spec_av_budget": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),

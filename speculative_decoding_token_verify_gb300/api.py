@@ -25,6 +25,7 @@ SPEC_ERR_CUDA = 3
 SPEC_ERR_TIMEOUT = 4
 SPEC_ERR_BAD_ROW = 5
 SPEC_ERR_BAD_TOKEN = 6
+SPEC_ERR_BAD_TEMPERATURE = 7
 MAX_K = 31
 MAX_V = 1 << 20
 
@@ -114,9 +115,11 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
            fly_theta: float = 0.3, fly_window: int = 6, est_params: Optional[torch.Tensor] = None,
            want_pos_stats: bool = False, want_feature: bool = False, want_conf: bool = False,
            out: Optional[dict] = None, workspace: Optional[Workspace] = None,
-           stream: Optional[torch.cuda.Stream] = None, draft_len: Optional[torch.Tensor] = None) -> dict:
+           stream: Optional[torch.cuda.Stream] = None, draft_len: Optional[torch.Tensor] = None,
+           inv_temperature: Optional[torch.Tensor] = None) -> dict:
     """Run spec_verify (spec_verify_ragged when ``draft_len`` [B] int32 gives
-    the drafts verified per sequence of a pruned batch). Returns a dict with
+    the drafts verified per sequence of a pruned batch; spec_verify_temperature
+    when ``inv_temperature`` [B] float32 gives 1/T per sequence). Returns a dict with
     ``out_tokens`` [B,K+1] int32 and ``accepted_len`` [B] int32, plus
     ``pos_stats`` [B,K+1,4], ``feature`` [B,K] and ``conf`` [B,K] (float32)
     when requested. ``out`` may supply preallocated output tensors under the
@@ -150,6 +153,10 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
         if (draft_len.dtype != torch.int32 or tuple(draft_len.shape) != (B,) or not draft_len.is_contiguous()
                 or draft_len.device != dev):
             raise ValueError("draft_len must be a contiguous int32 [B] tensor on the logits' device")
+    if inv_temperature is not None:
+        if (inv_temperature.dtype != torch.float32 or tuple(inv_temperature.shape) != (B,)
+                or not inv_temperature.is_contiguous() or inv_temperature.device != dev):
+            raise ValueError("inv_temperature must be a contiguous float32 [B] tensor on the logits' device")
     o = dict(out or {})
     if "out_tokens" not in o:
         o["out_tokens"] = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
@@ -167,7 +174,13 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
     if nbytes == 0:
         raise SpecError(SPEC_ERR_INVALID_ARG, _native.last_error())
     ws = _ws_for(workspace, nbytes, dev)
-    if draft_len is None:
+    if inv_temperature is not None:
+        rc = L.spec_verify_temperature(ctypes.byref(p), _ptr(zt), _ptr(draft_logits), _ptr(x), _ptr(draft_len),
+                                       _ptr(inv_temperature), _ptr(uniforms), _ptr(o["out_tokens"]),
+                                       _ptr(o["accepted_len"]), _ptr(o.get("pos_stats")), _ptr(est_params),
+                                       _ptr(o.get("feature")), _ptr(o.get("conf")), _ptr(ws),
+                                       ctypes.c_size_t(ws.numel()), _stream_ptr(stream, dev))
+    elif draft_len is None:
         rc = L.spec_verify(ctypes.byref(p), _ptr(zt), _ptr(draft_logits), _ptr(x), _ptr(uniforms),
                            _ptr(o["out_tokens"]), _ptr(o["accepted_len"]), _ptr(o.get("pos_stats")),
                            _ptr(est_params), _ptr(o.get("feature")), _ptr(o.get("conf")),

@@ -21,6 +21,20 @@
 // Two accumulators merge associatively (winner = larger M, then lower I);
 // every reduction in this library runs in a fixed order, so results are
 // bit-reproducible.
+//
+// Temperature. With an inverse temperature s > 0 the distributions are
+// softmax(s z) ("Speculative Decoding: ...", "Математика верификации" holds
+// for any pair of distributions the two models sample from). M and I stay in
+// raw logit units (s does not move the argmax); R and T are sums over the
+// processed exponents y_v = (z_v - M) s log2e. Every function below takes the
+// exponent scale sL = s log2e (default log2e, s = 1); then lse = s M + ln(1+R)
+// and h and logit(q_max) keep their formulas. With kSub the exponents are
+// formed difference first, (z - ref) sL, instead of z sL - ref sL: the
+// latter rounds ref sL once per reference, an offset shared by every term
+// whose size grows with |s ref| (6e-5 at s = 100 and logits near 10), while
+// z - ref is exact near the maximum (Sterbenz). The temperature variant uses
+// kSub; at s = 1 with ordinary logits the fused form is as accurate and one
+// instruction shorter.
 #pragma once
 
 #include <cstdint>
@@ -34,7 +48,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // lower clamp of exponents (log2 units): 2^-200 is 0 in fp32 and keeps
 // 0 * y finite for masked (-inf) logits
 constexpr float kYMin = -200.0f;
-// logit(q_max) when the complement mass R is exactly zero
+// cap of logit(q_max) = -ln R (q_max within 1e-13 of 1; also R = 0). Every
+// term of a complement R >= e^-30 over at most 2^20 tokens that matters is
+// a normal fp32 number, so the cap is exact under flush-to-zero arithmetic.
 constexpr float kFeatureClamp = 30.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
@@ -63,13 +79,13 @@ __device__ __forceinline__ RowAcc acc_empty() {
 }
 
 // a (+) b. Symmetric: merge(a, b) and merge(b, a) give identical bits.
-__device__ __forceinline__ RowAcc acc_merge(const RowAcc &a, const RowAcc &b) {
+__device__ __forceinline__ RowAcc acc_merge(const RowAcc &a, const RowAcc &b, float sL = kLog2e) {
     if (b.M == neg_inf()) return a;
     if (a.M == neg_inf()) return b;
     const bool aw = (a.M > b.M) || (a.M == b.M && a.I < b.I);
     RowAcc w = aw ? a : b;
     const RowAcc &l = aw ? b : a;
-    const float d = (l.M - w.M) * kLog2e;   // <= 0
+    const float d = (l.M - w.M) * sL;       // <= 0
     const float al = ex2(d);
     const float sl = 1.f + l.R;             // loser's total mass incl. its max
     w.R = fmaf(al, sl, w.R);
@@ -79,15 +95,15 @@ __device__ __forceinline__ RowAcc acc_merge(const RowAcc &a, const RowAcc &b) {
 
 // Fold E logits z[0..E) with global indices base..base+E-1 (ascending) into s.
 // Entries equal to -inf contribute nothing.
-template <int E>
-__device__ __forceinline__ void acc_chunk(RowAcc &s, const float (&z)[E], int base) {
+template <int E, bool kSub = false>
+__device__ __forceinline__ void acc_chunk(RowAcc &s, const float (&z)[E], int base, float sL = kLog2e) {
     float c = z[0];
 #pragma unroll
     for (int j = 1; j < E; ++j) c = fmaxf(c, z[j]);
     if (c > s.M) {
         // new running maximum: the old maximum joins the complement
         if (s.M != neg_inf()) {
-            const float d = (s.M - c) * kLog2e;
+            const float d = (s.M - c) * sL;
             const float al = ex2(d);
             const float st = 1.f + s.R;
             s.T = al * fmaf(d, st, s.T);
@@ -99,11 +115,11 @@ __device__ __forceinline__ void acc_chunk(RowAcc &s, const float (&z)[E], int ba
         for (int j = E - 1; j >= 0; --j)
             if (z[j] == c) jf = j;
         s.I = base + jf;
-        const float ml = c * kLog2e;
+        const float ml = c * sL;
         float r = 0.f, t = 0.f;
 #pragma unroll
         for (int j = 0; j < E; ++j) {
-            const float y = fmaxf(fmaf(z[j], kLog2e, -ml), kYMin);
+            const float y = fmaxf(kSub ? (z[j] - c) * sL : fmaf(z[j], sL, -ml), kYMin);
             const float e = ex2(y);
             if (j != jf) {
                 r += e;
@@ -113,11 +129,11 @@ __device__ __forceinline__ void acc_chunk(RowAcc &s, const float (&z)[E], int ba
         s.R += r;
         s.T += t;
     } else if (s.M != neg_inf()) {
-        const float ml = s.M * kLog2e;
+        const float ml = s.M * sL;
         float r = 0.f, t = 0.f;
 #pragma unroll
         for (int j = 0; j < E; ++j) {
-            const float y = fmaxf(fmaf(z[j], kLog2e, -ml), kYMin);
+            const float y = fmaxf(kSub ? (z[j] - s.M) * sL : fmaf(z[j], sL, -ml), kYMin);
             const float e = ex2(y);
             r += e;
             t = fmaf(e, y, t);
@@ -137,9 +153,9 @@ __device__ __forceinline__ RowAcc shfl_xor_acc(const RowAcc &a, int o) {
 }
 
 // butterfly: every lane ends with the same merged value
-__device__ __forceinline__ RowAcc warp_merge(RowAcc a) {
+__device__ __forceinline__ RowAcc warp_merge(RowAcc a, float sL = kLog2e) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = acc_merge(a, shfl_xor_acc(a, o));
+    for (int o = 16; o > 0; o >>= 1) a = acc_merge(a, shfl_xor_acc(a, o), sL);
     return a;
 }
 
@@ -213,8 +229,9 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 //
 // Per thread, over the 16-byte chunks of one tile, with a lazy reference mr:
 // exponents are taken relative to mr, which only moves when a chunk max
-// exceeds it by more than kRescale nats (so terms stay below e^8 and the
-// rescale branch is rare after the first chunk). The running max bv and the
+// exceeds it by more than kRescale processed nats, i.e. kRescale / s logit
+// units (so terms stay below e^8 and the rescale branch is rare after the
+// first chunk). The running max bv and the
 // chunk holding it (bk) are tracked per chunk; the mass of that chunk (C) is
 // kept apart from the rest (S), so that the complement mass R never has to be
 // formed as a difference; its bits are kept too, so that stream_finish() can
@@ -228,8 +245,8 @@ constexpr float kMaskF32 = -1.0e30f;
 
 struct StreamAcc {
     float mr;    // reference logit
-    float mrL;   // mr * log2(e)
-    float mrh;   // mr + kRescale (a chunk max above it moves the reference)
+    float mrL;   // mr * sL
+    float mrh;   // mr + rs, rs = kRescale / s (a chunk max above it moves the reference)
     float S;     // sum of 2^{(z - mr) log2e} over chunks other than the best one
     float C;     // the same sum over the best chunk
     float2 T;    // sum of 2^y * y, y = (z - mr) log2e (entropy moment, pairwise)
@@ -238,11 +255,11 @@ struct StreamAcc {
     uint4 bw;    // that chunk's bits, captured by the caller (so finishing needs no reload)
 };
 
-__device__ __forceinline__ StreamAcc stream_init() {
+__device__ __forceinline__ StreamAcc stream_init(float sL = kLog2e, float rs = kRescale) {
     StreamAcc s;
     s.mr = kMaskFloor;
-    s.mrL = kMaskFloor * kLog2e;
-    s.mrh = kMaskFloor + kRescale;
+    s.mrL = kMaskFloor * sL;
+    s.mrh = kMaskFloor + rs;
     s.S = 0.f;
     s.C = 0.f;
     s.T = make_float2(0.f, 0.f);
@@ -252,32 +269,34 @@ __device__ __forceinline__ StreamAcc stream_init() {
     return s;
 }
 
-__device__ __forceinline__ void stream_rescale(StreamAcc &s, float c) {
-    const float d = (s.mr - c) * kLog2e;
+__device__ __forceinline__ void stream_rescale(StreamAcc &s, float c, float sL, float rs) {
+    const float d = (s.mr - c) * sL;
     const float al = ex2(d);
     const float t = al * fmaf(d, s.S + s.C, s.T.x + s.T.y);
     s.T = make_float2(t, 0.f);
     s.S *= al;
     s.C *= al;
     s.mr = c;
-    s.mrL = c * kLog2e;
-    s.mrh = c + kRescale;
+    s.mrL = c * sL;
+    s.mrh = c + rs;
 }
 
 // fold the exponentials of one chunk given as fp32 pairs
-template <int NP, bool kEnt>
-__device__ __forceinline__ void stream_fold(StreamAcc &s, const float2 (&z)[NP], float c, int k) {
-    if (c > s.mrh) stream_rescale(s, c);
+template <int NP, bool kEnt, bool kSub>
+__device__ __forceinline__ void stream_fold(StreamAcc &s, const float2 (&z)[NP], float c, int k, float sL,
+                                            float rs) {
+    if (c > s.mrh) stream_rescale(s, c, sL, rs);
     const bool nb = c > s.bv;
     s.bv = nb ? c : s.bv;
     s.bk = nb ? k : s.bk;
-    const float2 L2 = make_float2(kLog2e, kLog2e);
+    const float2 L2 = make_float2(sL, sL);
     const float2 ml = make_float2(-s.mrL, -s.mrL);
     float2 e[NP];
     float2 y[NP];
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        y[p] = pfma(z[p], L2, ml);
+        if constexpr (kSub) y[p] = pfma(padd(z[p], make_float2(-s.mr, -s.mr)), L2, make_float2(0.f, 0.f));
+        else y[p] = pfma(z[p], L2, ml);
         e[p] = make_float2(ex2(y[p].x), ex2(y[p].y));
     }
     float2 a = e[0];
@@ -292,8 +311,9 @@ __device__ __forceinline__ void stream_fold(StreamAcc &s, const float2 (&z)[NP],
     s.C = nb ? cs : s.C;
 }
 
-template <typename T, bool kEnt>
-__device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k) {
+template <typename T, bool kEnt, bool kSub = false>
+__device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k, float sL = kLog2e,
+                                             float rs = kRescale) {
     if constexpr (sizeof(T) == 2) {
         if constexpr (kEnt) {
             w.x = bmax2(w.x, kMaskBf16x2);
@@ -308,7 +328,7 @@ __device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k) {
         z[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
         z[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
         z[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
-        stream_fold<4, kEnt>(s, z, c, k);
+        stream_fold<4, kEnt, kSub>(s, z, c, k, sL, rs);
     } else {
         float2 z[2];
         z[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
@@ -320,7 +340,7 @@ __device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k) {
             z[1].y = fmaxf(z[1].y, kMaskF32);
         }
         const float c = fmaxf(fmaxf(z[0].x, z[0].y), fmaxf(z[1].x, z[1].y));
-        stream_fold<2, kEnt>(s, z, c, k);
+        stream_fold<2, kEnt, kSub>(s, z, c, k, sL, rs);
     }
 }
 
@@ -391,8 +411,8 @@ __device__ __forceinline__ void load8(const T *row, int v, int V, bool vec_ok, f
 
 // Canonical RowAcc of one thread's streamed chunks; vector 0 of the tile has
 // row index `vb`.
-template <typename T>
-__device__ __forceinline__ RowAcc stream_finish(const StreamAcc &s, int vb) {
+template <typename T, bool kSub = false>
+__device__ __forceinline__ RowAcc stream_finish(const StreamAcc &s, int vb, float sL = kLog2e) {
     constexpr int E = Elem<T>::kPerVec;
     RowAcc a = acc_empty();
     if (!(s.bv > kMaskFloor)) return a;          // nothing unmasked seen
@@ -405,8 +425,8 @@ __device__ __forceinline__ RowAcc stream_finish(const StreamAcc &s, int vb) {
     float crest = 0.f;
 #pragma unroll
     for (int j = 0; j < E; ++j)
-        if (j != jf) crest += ex2(fmaf(z[j], kLog2e, -s.mrL));
-    const float d = (s.mr - s.bv) * kLog2e;      // <= 0: mr is some chunk max <= bv
+        if (j != jf) crest += ex2(kSub ? (z[j] - s.mr) * sL : fmaf(z[j], sL, -s.mrL));
+    const float d = (s.mr - s.bv) * sL;          // <= 0: mr is some chunk max <= bv
     const float al = ex2(d);
     a.M = s.bv;
     a.R = al * (s.S + crest);

@@ -88,9 +88,15 @@ enum { MODE_STOCHASTIC = 0, MODE_GREEDY = 1, MODE_FLY = 2, MODE_CONF = 3 };
 // one L2 slice
 enum { CTR_CLAIM = 0, CTR_STATUS = 32, CTR_RES_ALLOC = 64, CTR_RES_CLAIM = 96, kHeaderWords = 128 };
 
-// what finalise hands to the residual units of a sequence
+// what finalise hands to the residual units of a sequence. At temperature 1
+// the weights are p_v = e^{z_v - lse}. With an inverse temperature s they are
+// p_v = 2^{(z_v - M) sL - A}, sL = s log2e, A = log2(1 + R): z - M is exact
+// where p_v matters (Sterbenz), so p keeps fp32 accuracy at any s, which
+// s z - lse would not once |s M| is large.
 struct Draw {
-    float lse_t, lse_d, u;
+    float lse_t, lse_d;   // temperature variant: A_t, A_d
+    float m_t, m_d, sL;   // temperature variant only
+    float u;
     int n;
     bool bonus;   // all verified drafts accepted: the draw is from p_n alone
 };
@@ -103,6 +109,7 @@ struct Args {
     long long ds;            // draft row stride (elements)
     const int32_t *x;
     const int32_t *draft_len; // [B] drafts verified per sequence (pruned batch), or null: all K
+    const float *inv_temp;    // [B] inverse temperature s per sequence (temperature variant only)
     const float *u;
     const float *est;
     int32_t *out_tokens;
@@ -131,7 +138,9 @@ struct Args {
     int sstride;             // slice sums per sequence in `slices` (nslice rounded up to 4)
     unsigned *res_ready;     // [B] published flag per slot
     unsigned *res_done;      // [B] residual units completed per sequence
-    float4 *slotrec;         // [B] per published slot: (lse_t, lse_d, u, 64*b + 2*n + bonus)
+    float4 *slotrec;         // per published slot: (lse_t, lse_d, u, 64*b + 2*n + bonus); the
+                             // temperature variant uses two entries per slot, (A_t, A_d, u, bits)
+                             // and (M_t, M_d, sL, 0)
     float *slices;           // [B][sstride] residual mass per slice
 };
 
@@ -171,6 +180,17 @@ __device__ __forceinline__ int verified(const Args &a, int b) {
 
 __device__ __forceinline__ void raise_status(const Args &a, unsigned code) {
     atomicMax(a.ctr + CTR_STATUS, code);
+}
+
+// inverse temperature of sequence b; outside [SPEC_MIN_INV_TEMPERATURE,
+// SPEC_MAX_INV_TEMPERATURE] (or NaN) the sequence runs at s = 1, and its
+// finalize raises SPEC_ERR_BAD_TEMPERATURE
+__device__ __forceinline__ bool temp_ok(float s) {
+    return s >= SPEC_MIN_INV_TEMPERATURE && s <= SPEC_MAX_INV_TEMPERATURE;
+}
+__device__ __forceinline__ float seq_inv_temp(const Args &a, int b) {
+    const float s = __ldg(a.inv_temp + b);
+    return temp_ok(s) ? s : 1.f;
 }
 
 template <typename T>
@@ -250,20 +270,23 @@ __device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit) {
 }
 
 // Fold one unit. Returns the warp-merged accumulator (identical in every lane).
-template <typename T, bool kEnt>
-__device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l) {
+// sL, rs: exponent scale and rescale margin (log2e and kRescale at s = 1);
+// kSub: difference-first exponents (the temperature variant).
+template <typename T, bool kEnt, bool kSub = false>
+__device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float sL = kLog2e,
+                                               float rs = kRescale) {
     RowAcc hs = acc_empty(), ts = acc_empty();
     if (l < g.head) {
         float z[1] = {Elem<T>::load(g.row + g.v0 + l)};
-        acc_chunk<1>(hs, z, g.v0 + l);
+        acc_chunk<1, kSub>(hs, z, g.v0 + l, sL);
     }
     if (l < g.tail) {
         float z[1] = {Elem<T>::load(g.row + g.ve + l)};
-        acc_chunk<1>(ts, z, g.ve + l);
+        acc_chunk<1, kSub>(ts, z, g.ve + l, sL);
     }
     const uint4 *vp = reinterpret_cast<const uint4 *>(g.row + g.vb);
     const int nvec = (int)(g.bytes / 16u);
-    StreamAcc s = stream_init();
+    StreamAcc s = stream_init(sL, rs);
     int k = l;
     for (; k + (kUnroll - 1) * 32 < nvec; k += kUnroll * 32) {
         uint4 w[kUnroll];
@@ -271,38 +294,46 @@ __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l) {
         for (int q = 0; q < kUnroll; ++q) w[q] = ldg_stream(vp + k + q * 32);
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
-            stream_chunk<T, kEnt>(s, w[q], k + q * 32);
+            stream_chunk<T, kEnt, kSub>(s, w[q], k + q * 32, sL, rs);
             // keep the bits of the lane's best chunk (no reload when finishing)
             if (s.bk == k + q * 32) s.bw = w[q];
         }
     }
     for (; k < nvec; k += 32) {
         const uint4 w = ldg_stream(vp + k);
-        stream_chunk<T, kEnt>(s, w, k);
+        stream_chunk<T, kEnt, kSub>(s, w, k, sL, rs);
         if (s.bk == k) s.bw = w;
     }
-    const RowAcc vs = stream_finish<T>(s, g.vb);
-    return warp_merge(acc_merge(acc_merge(hs, vs), ts));
+    const RowAcc vs = stream_finish<T, kSub>(s, g.vb, sL);
+    return warp_merge(acc_merge(acc_merge(hs, vs, sL), ts, sL), sL);
+}
+
+// one probability of the draw's distributions (see Draw)
+template <bool kTemp>
+__device__ __forceinline__ float prob_t(const Draw &d, float z) {
+    if constexpr (kTemp) return ex2(fmaf(z - d.m_t, d.sL, -d.lse_t));
+    else return ex2((z - d.lse_t) * kLog2e);
+}
+template <bool kTemp>
+__device__ __forceinline__ float prob_d(const Draw &d, float z) {
+    if constexpr (kTemp) return ex2(fmaf(z - d.m_d, d.sL, -d.lse_d));
+    else return ex2((z - d.lse_d) * kLog2e);
 }
 
 // r_v = max(0, p_v - q_v) (or p_v without a draft row) for v..v+7, fp32.
-template <typename T>
+template <typename T, bool kTemp>
 __device__ __forceinline__ void resid8(const T *trow, const T *drow, int v, int V, bool tv, bool dv,
-                                       float lse_t, float lse_d, float (&r)[8]) {
+                                       const Draw &d, float (&r)[8]) {
     float zt[8];
     load8<T>(trow, v, V, tv, zt);
     if (drow) {
         float zd[8];
         load8<T>(drow, v, V, dv, zd);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float p = ex2((zt[j] - lse_t) * kLog2e);
-            const float q = ex2((zd[j] - lse_d) * kLog2e);
-            r[j] = fmaxf(p - q, 0.f);
-        }
+        for (int j = 0; j < 8; ++j) r[j] = fmaxf(prob_t<kTemp>(d, zt[j]) - prob_d<kTemp>(d, zd[j]), 0.f);
     } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) r[j] = ex2((zt[j] - lse_t) * kLog2e);
+        for (int j = 0; j < 8; ++j) r[j] = prob_t<kTemp>(d, zt[j]);
     }
 }
 
@@ -329,7 +360,8 @@ __device__ __forceinline__ RowAcc shfl_acc(const RowAcc &a, int src) {
 // its tiles in order, then the L lanes merge by butterfly, a fixed tree. Lane
 // j ends with target row j in tr and draft row j in dr. nT <= kStage always
 // (tiles hold >= 4096 of at most 2^20 elements).
-__device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *buf, RowAcc &tr, RowAcc &dr) {
+__device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *buf, RowAcc &tr, RowAcc &dr,
+                                           float sL) {
     const int nT = a.nT;
     const int rc = min(kStage / nT, 32);       // whole rows per staging pass, one lane each at least
     const float4 *base = a.part + (size_t)b * a.per_seq;
@@ -350,9 +382,9 @@ __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *
         if (ri < rn) {
             const float4 *pr = buf + ri * nT;
             const int t1 = min(nT, (sub + 1) * run);
-            for (int t = sub * run; t < t1; ++t) acc = acc_merge(acc, acc_unpack(pr[t]));
+            for (int t = sub * run; t < t1; ++t) acc = acc_merge(acc, acc_unpack(pr[t]), sL);
         }
-        for (int o = 1; o < (1 << lsh); o <<= 1) acc = acc_merge(acc, shfl_xor_acc(acc, o));
+        for (int o = 1; o < (1 << lsh); o <<= 1) acc = acc_merge(acc, shfl_xor_acc(acc, o), sL);
         // row r0 + i now sits in lane i * L
         const RowAcc st = shfl_acc(acc, (int)(((unsigned)(l - r0) << lsh) & 31u));
         const RowAcc sd = shfl_acc(acc, (int)(((unsigned)(drow - r0) << lsh) & 31u));
@@ -366,11 +398,19 @@ __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *
 // Finalise sequence b with one warp: the lanes merge the row partials (lane j
 // ends with target row j and draft row j), apply the mode's rule, write the
 // per-position outputs and, in stochastic mode, publish the draw of b for the
-// residual units.
+// residual units. kTemp: the rows are processed at sequence b's inverse
+// temperature s (lse = s M + ln(1+R); the log-ratio is formed from z - M).
 // ---------------------------------------------------------------------------
-template <typename T>
+template <typename T, bool kTemp>
 __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) {
     const int K = a.K;
+    float sc = 1.f;
+    if constexpr (kTemp) {
+        const float s_raw = __ldg(a.inv_temp + b);
+        if (l == 0 && !temp_ok(s_raw)) raise_status(a, SPEC_ERR_BAD_TEMPERATURE);
+        sc = temp_ok(s_raw) ? s_raw : 1.f;
+    }
+    const float sL = kTemp ? sc * kLog2e : kLog2e;
     // a pruned batch verifies drafts 0..kb-1 against target rows 0..kb
     // ("Verificación Adaptativa sin una cabeza de confianza", "Antecedentes")
     const int kb = verified(a, b);
@@ -395,25 +435,32 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         }
     }
     RowAcc tr, dr;
-    merge_rows(a, b, l, buf, tr, dr);
+    merge_rows(a, b, l, buf, tr, dr, sL);
     float lse_t = nan, h = nan, lse_d = nan, f = nan, lr = nan;
+    float lp1_t = nan, lp1_d = nan;   // ln(1 + R) (temperature variant)
     int amax_t = -1;
     bool bad_row = false;
     if (l < a.nt_rows && l <= kb) {
         bad_row |= !(tr.M > neg_inf());
         const float lp1 = log1pf(tr.R);
-        lse_t = tr.M + lp1;
+        lp1_t = lp1;
+        lse_t = kTemp ? fmaf(sc, tr.M, lp1) : tr.M + lp1;
         h = (lp1 - tr.T * kLn2 / (1.f + tr.R)) * a.inv_log_v;
         amax_t = tr.I;
     }
     if (l < a.nd_rows && l < kb) {
         bad_row |= !(dr.M > neg_inf());
-        lse_d = dr.M + log1pf(dr.R);
-        f = dr.R > 0.f ? -logf(dr.R) : kFeatureClamp;
+        lp1_d = log1pf(dr.R);
+        lse_d = kTemp ? fmaf(sc, dr.M, lp1_d) : dr.M + lp1_d;
+        f = fminf(-logf(dr.R), kFeatureClamp);   // capped at 30 (R = 0: +inf -> 30)
     }
     if (bad_row) raise_status(a, SPEC_ERR_BAD_ROW);
     if (bad_tok) raise_status(a, SPEC_ERR_BAD_TOKEN);
-    if (!conf_only && l < kb && a.nd_rows > 0) lr = bad_tok ? neg_inf() : (zx - lse_t) - (qx - lse_d);
+    if (!conf_only && l < kb && a.nd_rows > 0) {
+        if (bad_tok) lr = neg_inf();
+        else if constexpr (kTemp) lr = fmaf(sc, zx - tr.M, -lp1_t) - fmaf(sc, qx - dr.M, -lp1_d);
+        else lr = (zx - lse_t) - (qx - lse_d);
+    }
     int n = kb;
     if (a.mode == MODE_STOCHASTIC) {
         // "Математика верификации": accept iff u < min(1, p/q); lr = +inf
@@ -460,8 +507,14 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         a.conf[(size_t)b * K + l] = l < kb ? 1.f / (1.f + expf(-z)) : nan;
     }
     if (a.mode == MODE_CONF) return;
-    const float lt_n = __shfl_sync(kFull, lse_t, n);
-    const float ld_n = __shfl_sync(kFull, lse_d, n);
+    // the draw's weights: lse (s = 1), or M and A = log2(1 + R) (see Draw)
+    const float lt_n = __shfl_sync(kFull, kTemp ? lp1_t * kLog2e : lse_t, n);
+    const float ld_n = __shfl_sync(kFull, kTemp ? lp1_d * kLog2e : lse_d, n);
+    float mt_n = 0.f, md_n = 0.f;
+    if constexpr (kTemp) {
+        mt_n = __shfl_sync(kFull, tr.M, n);
+        md_n = __shfl_sync(kFull, dr.M, n);
+    }
     const int am_n = __shfl_sync(kFull, amax_t, n);
     const float u_draw = __shfl_sync(kFull, ui, K);
     // K <= 31: lane j writes position j (lane j holds draft token j)
@@ -471,7 +524,13 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         if (draw) {
             // hand the draw to the residual units of b; the release store
             // orders the record before the flag
-            a.slotrec[slot] = make_float4(lt_n, ld_n, u_draw, __int_as_float((b << 6) | (n << 1) | (n == kb ? 1 : 0)));
+            const float4 rec = make_float4(lt_n, ld_n, u_draw, __int_as_float((b << 6) | (n << 1) | (n == kb ? 1 : 0)));
+            if constexpr (kTemp) {
+                a.slotrec[2 * slot] = rec;
+                a.slotrec[2 * slot + 1] = make_float4(mt_n, md_n, sL, 0.f);
+            } else {
+                a.slotrec[slot] = rec;
+            }
             st_release(a.res_ready + slot, 1u);
         }
     }
@@ -489,10 +548,10 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
 
 // Sum of slice s (elements 256s .. 256s+255) of the draw's weights, per lane
 // (8 elements each), in the fixed order every consumer of slice sums uses.
-template <typename T>
+template <typename T, bool kTemp>
 __device__ __forceinline__ float slice_lane_sum(const Args &a, const T *tr, const T *dr, int s, int l,
-                                               float lse_t, float lse_d, float (&r)[8]) {
-    resid8<T>(tr, dr, s * kSlice + l * 8, a.V, a.t_vec_ok != 0, a.d_vec_ok != 0, lse_t, lse_d, r);
+                                               const Draw &d, float (&r)[8]) {
+    resid8<T, kTemp>(tr, dr, s * kSlice + l * 8, a.V, a.t_vec_ok != 0, a.d_vec_ok != 0, d, r);
     return sum8(r);
 }
 
@@ -525,7 +584,7 @@ __device__ __forceinline__ float run_sum(const float4 *buf, int l, int cn) {
 // running sum first exceeds u*Z, then rescans that slice lane by lane with an
 // fp64 prefix across lanes. Returns the token, or -1 when Z is not positive
 // (only possible through rounding, or a bad row).
-template <typename T>
+template <typename T, bool kTemp>
 __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l, float4 *buf) {
     const float *ss = a.slices + (size_t)b * a.sstride;
     const int n = a.nslice;
@@ -591,7 +650,7 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
         P2 = -2.0 * Z - 1.0;
     }
     float r[8];
-    const float s = slice_lane_sum<T>(a, tr, dr, entry, l, d.lse_t, d.lse_d, r);
+    const float s = slice_lane_sum<T, kTemp>(a, tr, dr, entry, l, d, r);
     const double in = warp_incl_scan_d((double)s, l);
     const double ex = in - (double)s;
     const unsigned hit = __ballot_sync(kFull, P2 + in > target);
@@ -618,8 +677,8 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
 // Lane sums of kResBatch whole slices s0 .. of 16-byte aligned rows: every
 // load of the batch is issued before any arithmetic. Same per-lane order as
 // slice_lane_sum.
-template <typename T, bool kDraft>
-__device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int l, float lse_t, float lse_d,
+template <typename T, bool kDraft, bool kTemp>
+__device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int l, const Draw &d,
                                            float (&part)[kResBatch]) {
     constexpr int E = Elem<T>::kPerVec;
     constexpr int NV = 8 / E;   // 16-byte vectors per lane per slice per row
@@ -645,14 +704,11 @@ __device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int
                 float zd[E];
                 Elem<T>::unpack(wd[i][k], zd);
 #pragma unroll
-                for (int j = 0; j < E; ++j) {
-                    const float p = ex2((zt[j] - lse_t) * kLog2e);
-                    const float q = ex2((zd[j] - lse_d) * kLog2e);
-                    r[k * E + j] = fmaxf(p - q, 0.f);
-                }
+                for (int j = 0; j < E; ++j)
+                    r[k * E + j] = fmaxf(prob_t<kTemp>(d, zt[j]) - prob_d<kTemp>(d, zd[j]), 0.f);
             } else {
 #pragma unroll
-                for (int j = 0; j < E; ++j) r[k * E + j] = ex2((zt[j] - lse_t) * kLog2e);
+                for (int j = 0; j < E; ++j) r[k * E + j] = prob_t<kTemp>(d, zt[j]);
             }
         }
         part[i] = sum8(r);
@@ -661,7 +717,7 @@ __device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int
 
 // Slices s0 .. s0 + res_slices<T>() - 1 of the draw's weights (kResBatch slices'
 // loads in flight at a time); lane kSig stores their sums.
-template <typename T>
+template <typename T, bool kTemp>
 __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T *tr, const T *dr, const Draw &d,
                                           int l) {
 #pragma unroll
@@ -669,14 +725,14 @@ __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T 
         float part[kResBatch];
         const bool fast = a.t_vec_ok && (dr == nullptr || a.d_vec_ok) && (s0 + i0 + kResBatch) * kSlice <= a.V;
         if (fast && dr) {
-            batch_fast<T, true>(tr, dr, s0 + i0, l, d.lse_t, d.lse_d, part);
+            batch_fast<T, true, kTemp>(tr, dr, s0 + i0, l, d, part);
         } else if (fast) {
-            batch_fast<T, false>(tr, dr, s0 + i0, l, d.lse_t, d.lse_d, part);
+            batch_fast<T, false, kTemp>(tr, dr, s0 + i0, l, d, part);
         } else {
 #pragma unroll
             for (int i = 0; i < kResBatch; ++i) {
                 float r[8];
-                part[i] = slice_lane_sum<T>(a, tr, dr, s0 + i0 + i, l, d.lse_t, d.lse_d, r);
+                part[i] = slice_lane_sum<T, kTemp>(a, tr, dr, s0 + i0 + i, l, d, r);
             }
         }
 #pragma unroll
@@ -688,14 +744,23 @@ __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T 
     }
 }
 
+template <bool kTemp>
 __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
-    const float4 rec = __ldcg(a.slotrec + slot);
+    const float4 rec = __ldcg(a.slotrec + (kTemp ? 2 * slot : slot));
     const int bits = __float_as_int(rec.w);
     b = bits >> 6;
     Draw d;
     d.lse_t = rec.x;
     d.lse_d = rec.y;
     d.u = rec.z;
+    d.m_t = d.m_d = 0.f;
+    d.sL = kLog2e;
+    if constexpr (kTemp) {
+        const float4 r2 = __ldcg(a.slotrec + 2 * slot + 1);
+        d.m_t = r2.x;
+        d.m_d = r2.y;
+        d.sL = r2.z;
+    }
     d.n = (bits >> 1) & 31;
     d.bonus = (bits & 1) != 0;
     return d;
@@ -704,19 +769,19 @@ __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
 // The last residual unit of the sequence in `slot` completed: locate its
 // token. If the residual mass vanished (only possible through rounding) the
 // warp redraws from p.
-template <typename T>
+template <typename T, bool kTemp>
 __device__ __noinline__ void locate(const Args &a, int slot, int l, float4 *buf) {
     int b;
-    const Draw d = decode_slot(a, slot, b);
+    const Draw d = decode_slot<kTemp>(a, slot, b);
     const int K = a.K;
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
-    int token = locate_scan<T>(a, b, tr, dr, d, l, buf);
+    int token = locate_scan<T, kTemp>(a, b, tr, dr, d, l, buf);
     if (token < 0 && dr != nullptr) {
-        for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T>(a, b, s0, tr, nullptr, d, l);
+        for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T, kTemp>(a, b, s0, tr, nullptr, d, l);
         __threadfence();
         __syncwarp();
-        token = locate_scan<T>(a, b, tr, nullptr, d, l, buf);
+        token = locate_scan<T, kTemp>(a, b, tr, nullptr, d, l, buf);
     }
     if (token < 0) {
         if (l == 0) raise_status(a, SPEC_ERR_BAD_ROW);
@@ -733,15 +798,15 @@ struct ResDone {
     unsigned old;
 };
 
-template <typename T>
+template <typename T, bool kTemp>
 __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l) {
     const int slot = (int)(id / (unsigned)a.nR);
     const int t = (int)(id - (unsigned)slot * (unsigned)a.nR);
     int b;
-    const Draw d = decode_slot(a, slot, b);
+    const Draw d = decode_slot<kTemp>(a, slot, b);
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
-    unit_sums<T>(a, b, t * res_slices<T>(), tr, dr, d, l);
+    unit_sums<T, kTemp>(a, b, t * res_slices<T>(), tr, dr, d, l);
     ResDone r;
     r.slot = slot;
     r.old = 0u;
@@ -814,7 +879,7 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
 // ---------------------------------------------------------------------------
 enum { DUE_NONE = 0, DUE_STREAM = 1, DUE_RESIDUAL = 2 };
 
-template <typename T>
+template <typename T, bool kTemp>
 __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a) {
     const int l = threadIdx.x & 31;
     __shared__ float4 s_stage[NWARP][kStage];   // per-warp staging for finalize and locate
@@ -842,8 +907,8 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             const unsigned need = due == DUE_STREAM ? a.per_seq - 1u : (unsigned)a.nR - 1u;
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
-                if (due == DUE_STREAM) finalize<T>(a, due_id, l, wbuf);
-                else locate<T>(a, due_id, l, wbuf);
+                if (due == DUE_STREAM) finalize<T, kTemp>(a, due_id, l, wbuf);
+                else locate<T, kTemp>(a, due_id, l, wbuf);
             }
             due = DUE_NONE;
         }
@@ -854,7 +919,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         }
         if (kind == JOB_DONE) break;
         if (kind == JOB_RESIDUAL) {
-            const ResDone r = residual_unit<T>(a, unit, l);
+            const ResDone r = residual_unit<T, kTemp>(a, unit, l);
             due = DUE_RESIDUAL;
             due_id = r.slot;
             due_old = r.old;
@@ -869,7 +934,16 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             skip = g.target ? g.r > kb : g.r - a.nt_rows >= kb;
         }
         // target rows also carry the entropy moment; draft rows do not need it
-        const RowAcc s = skip ? acc_empty() : (g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l));
+        RowAcc s;
+        if constexpr (kTemp) {
+            // the sequence's inverse temperature scales every exponent
+            const float sc = seq_inv_temp(a, g.b);
+            const float sL = sc * kLog2e, rs = __fdiv_rn(kRescale, sc);   // exact for powers of two
+            s = skip ? acc_empty()
+                     : (g.target ? unit_consume<T, true, true>(g, l, sL, rs) : unit_consume<T, false, true>(g, l, sL, rs));
+        } else {
+            s = skip ? acc_empty() : (g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l));
+        }
         const int b = g.b;
         unsigned old = 0u;
         if (l == kSig) {
@@ -882,8 +956,8 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             const unsigned need = due == DUE_STREAM ? a.per_seq - 1u : (unsigned)a.nR - 1u;
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
-                if (due == DUE_STREAM) finalize<T>(a, due_id, l, wbuf);
-                else locate<T>(a, due_id, l, wbuf);
+                if (due == DUE_STREAM) finalize<T, kTemp>(a, due_id, l, wbuf);
+                else locate<T, kTemp>(a, due_id, l, wbuf);
             }
         }
         due = DUE_STREAM;
@@ -953,7 +1027,7 @@ static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace: [header words | seq_done[B] | res_ready[B] | res_done[B]] (zeroed
-// per call) [slot records B | tile partials | slices B*sstride]. The
+// per call) [slot records 2B | tile partials | slices B*sstride]. The
 // partials hold one slot per stream unit of the largest plan among the row
 // counts the call may stream (`rows_a`, `rows_b`).
 static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan &p) {
@@ -966,14 +1040,14 @@ static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan
     p.done_off = p.ready_off + (size_t)B * sizeof(unsigned);
     p.zero_bytes = p.done_off + (size_t)B * sizeof(unsigned);
     p.rec_off = align_up(p.zero_bytes, 16);
-    p.part_off = align_up(p.rec_off + (size_t)B * sizeof(float4), 16);
+    p.part_off = align_up(p.rec_off + (size_t)2 * B * sizeof(float4), 16);
     p.slice_off = align_up(p.part_off + (size_t)cap * sizeof(float4), 16);
     p.bytes = align_up(p.slice_off + (size_t)B * p.sstride * sizeof(float), 16);
 }
 
 struct DevInfo {
     int sms = 0;
-    int occ[2] = {0, 0};
+    int occ[2][2] = {{0, 0}, {0, 0}};   // [dtype][temperature variant]
 };
 
 static std::mutex g_dev_mu;
@@ -981,15 +1055,16 @@ static DevInfo g_dev[64];
 
 constexpr size_t kDynSmem = 0;
 
-template <typename T>
+template <typename T, bool kTemp>
 static int occupancy() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<T>, NT, kDynSmem) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<T, kTemp>, NT, kDynSmem) != cudaSuccess)
+        n = 0;
     return n;
 }
 
 // Grid = resident CTAs (SMs x occupancy), at most one warp per unit.
-static int grid_for(int dtype, unsigned long long units, int *grid) {
+static int grid_for(int dtype, bool temp, unsigned long long units, int *grid) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice failed");
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -998,13 +1073,17 @@ static int grid_for(int dtype, unsigned long long units, int *grid) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return fail(SPEC_ERR_CUDA, "cannot query the SM count");
-        d.occ[0] = occupancy<float>();
-        d.occ[1] = occupancy<__nv_bfloat16>();
-        if (d.occ[0] < 1 || d.occ[1] < 1)
-            return fail(SPEC_ERR_CUDA, "the verify kernel cannot be resident (shared memory %zu bytes)", kDynSmem);
+        d.occ[0][0] = occupancy<float, false>();
+        d.occ[1][0] = occupancy<__nv_bfloat16, false>();
+        d.occ[0][1] = occupancy<float, true>();
+        d.occ[1][1] = occupancy<__nv_bfloat16, true>();
+        for (int i = 0; i < 4; ++i)
+            if (d.occ[i >> 1][i & 1] < 1)
+                return fail(SPEC_ERR_CUDA, "the verify kernel cannot be resident (shared memory %zu bytes)",
+                            kDynSmem);
         d.sms = sms;
     }
-    unsigned long long g = (unsigned long long)d.sms * (unsigned long long)d.occ[dtype];
+    unsigned long long g = (unsigned long long)d.sms * (unsigned long long)d.occ[dtype][temp ? 1 : 0];
     const unsigned long long need = (units + NWARP - 1) / NWARP;
     if (g > need) g = need;
     *grid = (int)(g < 1 ? 1 : g);
@@ -1031,14 +1110,19 @@ static int launch(Args &a, const Plan &p, int dtype, void *ws, void *stream) {
     a.res_units = a.mode == MODE_STOCHASTIC ? (unsigned)a.B * (unsigned)p.nR : 0u;
     a.inv_log_v = (float)(1.0 / std::log((double)a.V));
     int grid = 1;
-    int rc = grid_for(dtype, p.units, &grid);
+    const bool temp = a.inv_temp != nullptr;
+    int rc = grid_for(dtype, temp, p.units, &grid);
     if (rc != SPEC_OK) return rc;
     cudaError_t e = cudaMemsetAsync(ws, 0, p.zero_bytes, st);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "workspace reset failed: %s", cudaGetErrorString(e));
-    if (dtype == SPEC_BF16)
-        verify_kernel<__nv_bfloat16><<<grid, NT, kDynSmem, st>>>(a);
+    if (dtype == SPEC_BF16 && temp)
+        verify_kernel<__nv_bfloat16, true><<<grid, NT, kDynSmem, st>>>(a);
+    else if (dtype == SPEC_BF16)
+        verify_kernel<__nv_bfloat16, false><<<grid, NT, kDynSmem, st>>>(a);
+    else if (temp)
+        verify_kernel<float, true><<<grid, NT, kDynSmem, st>>>(a);
     else
-        verify_kernel<float><<<grid, NT, kDynSmem, st>>>(a);
+        verify_kernel<float, false><<<grid, NT, kDynSmem, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return SPEC_OK;
@@ -1110,7 +1194,8 @@ size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t d
 }  // extern "C"
 
 static int verify_impl(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
-                       const int32_t *draft_tokens, const int32_t *draft_len, const float *uniforms,
+                       const int32_t *draft_tokens, const int32_t *draft_len, const float *inv_temp,
+                       const float *uniforms,
                        int32_t *out_tokens, int32_t *accepted_len, float *pos_stats, const float *est_params,
                        float *feature, float *conf, void *workspace, size_t workspace_bytes, void *stream) {
     g_err.clear();
@@ -1154,6 +1239,7 @@ static int verify_impl(const spec_verify_params *p, const void *target_logits, c
     a.ds = ds;
     a.x = draft_tokens;
     a.draft_len = draft_len;
+    a.inv_temp = inv_temp;
     a.u = uniforms;
     a.est = est_params;
     a.out_tokens = out_tokens;
@@ -1181,8 +1267,8 @@ int spec_verify(const spec_verify_params *p, const void *target_logits, const vo
                 const int32_t *draft_tokens, const float *uniforms, int32_t *out_tokens,
                 int32_t *accepted_len, float *pos_stats, const float *est_params, float *feature,
                 float *conf, void *workspace, size_t workspace_bytes, void *stream) {
-    return verify_impl(p, target_logits, draft_logits, draft_tokens, nullptr, uniforms, out_tokens, accepted_len,
-                       pos_stats, est_params, feature, conf, workspace, workspace_bytes, stream);
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, nullptr, nullptr, uniforms, out_tokens,
+                       accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes, stream);
 }
 
 int spec_verify_ragged(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
@@ -1193,8 +1279,22 @@ int spec_verify_ragged(const spec_verify_params *p, const void *target_logits, c
         g_err = "draft_len is NULL";
         return SPEC_ERR_INVALID_ARG;
     }
-    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, uniforms, out_tokens,
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, nullptr, uniforms, out_tokens,
                        accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes, stream);
+}
+
+int spec_verify_temperature(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
+                            const int32_t *draft_tokens, const int32_t *draft_len, const float *inv_temperature,
+                            const float *uniforms, int32_t *out_tokens, int32_t *accepted_len, float *pos_stats,
+                            const float *est_params, float *feature, float *conf, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    if (!inv_temperature) {
+        g_err = "inv_temperature is NULL";
+        return SPEC_ERR_INVALID_ARG;
+    }
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, inv_temperature, uniforms,
+                       out_tokens, accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes,
+                       stream);
 }
 
 int spec_confidence(int32_t B, int32_t K, int32_t V, int32_t dtype, const void *draft_logits,

@@ -28,14 +28,16 @@ def tol_for(dtype) -> float:
     return 2e-3 if dtype in ("bf16", torch.bfloat16) else 1e-5
 
 
-def oracle_run(inp, mode, fly_theta=0.3, fly_window=6, est=None, with_draft=True, nthreads=8, draft_len=None):
+def oracle_run(inp, mode, fly_theta=0.3, fly_window=6, est=None, with_draft=True, nthreads=8, draft_len=None,
+               inv_temp=None):
     zt = workloads.to_numpy_logits(inp["zt"])
     zd = workloads.to_numpy_logits(inp["zd"]) if with_draft else None
     x = inp["x"].cpu().numpy()
     u = inp["u"].cpu().numpy() if mode == oracle.STOCHASTIC else None
     r = oracle.verify(zt, zd, x, u, mode=mode, fly_theta=fly_theta, fly_window=fly_window,
                       est_params=None if est is None else np.asarray(est, np.float64),
-                      nthreads=nthreads, want_cdf=mode == oracle.STOCHASTIC, draft_len=draft_len)
+                      nthreads=nthreads, want_cdf=mode == oracle.STOCHASTIC, draft_len=draft_len,
+                      inv_temp=inv_temp)
     if u is not None:
         r["u_final"] = u[:, -1].astype(np.float64)
     return r

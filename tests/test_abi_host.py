@@ -215,6 +215,13 @@ def test_av_and_ragged_validation(L):
     p = sv.make_params(4, 2, 1000, 1)
     assert L.spec_verify_ragged(ctypes.byref(p), F, F, F, None, F, F, F, None, None, None, None, F, 1 << 24,
                                 None) == 1
+    assert L.spec_verify_temperature(ctypes.byref(p), F, F, F, None, None, F, F, F, None, None, None, None, F,
+                                     1 << 24, None) == 1                         # inv_temperature NULL
+    assert b"inv_temperature" in L.spec_last_error()
+    p.mode = 7
+    assert L.spec_verify_temperature(ctypes.byref(p), F, F, F, None, F, F, F, F, None, None, None, None, F,
+                                     1 << 24, None) == 2                         # unknown mode
+    p.mode = 0
     assert L.spec_estimator_update_ragged(4, 2, F, F, None, F, 0.05, None, None, None) == 1
     assert L.spec_irls_accumulate_ragged(4, 2, F, F, None, F, F, None) == 1
     assert L.spec_ngram_draft(-1, 8, F, F, 1, 2, 4, F, F, None) == 1

@@ -19,6 +19,11 @@ which are not available here. Recipe (per workload, seed ``s``):
   the Gumbel-max identity (argmax of logits plus Gumbel noise), or the draft
   row's argmax for greedy drafting.
 * ``u`` uniforms ``[B, K+1]`` in ``[0, 1)`` from a second generator seeded ``s+1``.
+* ``inv_temp`` (workloads with a sampling temperature only) ``[B]`` float32:
+  a per-sequence inverse temperature, log-uniform on ``[lo, hi]``, from a
+  third generator seeded ``s+2``; the drafts are then drawn from the softmax
+  of the stored draft row times it (the distribution the draft samples from
+  at that temperature).
 
 All values come from ``torch.Generator(device)`` seeded with ``s`` (Philox on
 CUDA, mt19937 on CPU), so a given (workload, seed, device) always yields the
@@ -27,6 +32,7 @@ same bytes.
 from __future__ import annotations
 
 import dataclasses
+import math
 from typing import Optional
 
 import torch
@@ -46,6 +52,8 @@ class Workload:
     temp_range: Optional[tuple] = None   # per-row temperature U(lo, hi)
     # second recipe for sequences b >= B/2 (FLy workload): (sigma, spike)
     upper_half: Optional[tuple] = None
+    # sampling inverse temperature per sequence, log-uniform on (lo, hi)
+    inv_temp_range: Optional[tuple] = None
     draft_tokens: str = "sample"         # "sample" (x ~ q) | "argmax"
     fly_theta: float = 0.3
     fly_window: int = 6
@@ -115,6 +123,13 @@ def make_inputs(w: Workload, seed: int, device="cpu", chunk_rows: int = 1 << 14)
     zt = torch.empty((B, K + 1, V), dtype=dt, device=device)
     zd = torch.empty((B, K, V), dtype=dt, device=device)
     x = torch.empty((B, K), dtype=torch.int32, device=device)
+    s_inv = None
+    if w.inv_temp_range is not None:
+        gs = torch.Generator(device=device)
+        gs.manual_seed(seed + 2)
+        lo, hi = (float(v) for v in w.inv_temp_range)
+        r = torch.rand((B,), generator=gs, device=device, dtype=torch.float64)
+        s_inv = torch.exp(math.log(lo) + (math.log(hi) - math.log(lo)) * r).to(torch.float32)
     seqs_per_chunk = max(1, chunk_rows // (2 * K + 1))
     for b0 in range(0, B, seqs_per_chunk):
         b1 = min(B, b0 + seqs_per_chunk)
@@ -139,6 +154,8 @@ def make_inputs(w: Workload, seed: int, device="cpu", chunk_rows: int = 1 << 14)
         zd[b0:b1] = d.to(dt)
         del t
         dq = zd[b0:b1].float()
+        if s_inv is not None:
+            dq = dq * s_inv[b0:b1].view(n, 1, 1)
         if w.draft_tokens == "argmax":
             x[b0:b1] = dq.argmax(dim=-1).to(torch.int32)
         else:
@@ -149,7 +166,10 @@ def make_inputs(w: Workload, seed: int, device="cpu", chunk_rows: int = 1 << 14)
             del gum
         del d, dq
     u = torch.rand((B, K + 1), generator=gu, device=device, dtype=torch.float32)
-    return dict(zt=zt, zd=zd, x=x, u=u)
+    out = dict(zt=zt, zd=zd, x=x, u=u)
+    if s_inv is not None:
+        out["inv_temp"] = s_inv
+    return out
 
 
 def to_numpy_logits(z: torch.Tensor):
