@@ -54,7 +54,7 @@ def _load():
     P = ctypes.c_void_p
     i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
     lib.oracle_verify.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.c_int, P, i64, P, i64,
-                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
+                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, P, P, P, P, dbl, ctypes.c_int]
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_confidence.argtypes = [i32, i32, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
     lib.oracle_confidence.restype = ctypes.c_int
@@ -90,11 +90,12 @@ def _logits(z):
 
 
 def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_params=None,
-           nthreads=1, want_cdf=False, draft_len=None, inv_temp=None):
+           nthreads=1, want_cdf=False, draft_len=None, inv_temp=None, top_p=1.0):
     """Verify B sequences. zt [B,K+1,V], zd [B,K,V] or None, x [B,K] int32,
     u [B,K+1] float32 or None, draft_len [B] int32 in [0, K] or None (drafts
     submitted for verification per sequence; None: all K), inv_temp [B]
-    float32 > 0 or None (per-sequence inverse sampling temperature).
+    float32 > 0 or None (per-sequence inverse sampling temperature), top_p in
+    (0, 1] (nucleus truncation of every processed row; 1: none).
 
     Returns a dict of numpy arrays: out_tokens [B,K+1] int32, accepted_len [B],
     pos_stats [B,K+1,4] (lse_t, h_t, log_ratio, f), feature [B,K], conf [B,K]
@@ -139,7 +140,7 @@ def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_param
                            _ptr(out["pos_stats"]), _ptr(out["conf"]) if est is not None else None,
                            _ptr(out["feature"]) if zd is not None else None,
                            _ptr(out["margin_acc"]), _ptr(out["margin_cdf"]), _ptr(cdf),
-                           _ptr(out["flags"]), _ptr(draft_len), _ptr(inv_temp), int(nthreads))
+                           _ptr(out["flags"]), _ptr(draft_len), _ptr(inv_temp), float(top_p), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     out["margin"] = np.minimum(out["margin_acc"], out["margin_cdf"])

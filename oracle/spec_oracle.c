@@ -53,6 +53,8 @@
 /* logit(q_max) when the complement mass is exactly zero */
 #define OR_F_CLAMP 30.0
 
+static double dmin(double a, double b) { return a < b ? a : b; }
+
 static double logit_at(const void *row, int dtype, int64_t v) {
     if (dtype == OR_F32) return (double)((const float *)row)[v];
     uint32_t bits = ((uint32_t)((const uint16_t *)row)[v]) << 16;
@@ -86,6 +88,76 @@ static double softmax_row(const void *row, int dtype, int32_t V, double sc, doub
     for (int32_t v = 0; v < V; ++v) p[v] /= s;
     *ok = 1;
     return m + log(s);
+}
+
+/* Top-p (nucleus) truncation of a normalised row p ([AV] "Benchmarks": the
+ * serving setting samples with top-p 0.95; [SD] "Математика верификации":
+ * the rule is lossless for whatever distributions the models sample from).
+ * Reading: the nucleus is every token whose logit is at least z*, the
+ * largest logit value t for which the tokens with logit >= t hold at least
+ * top_p of the mass. Tokens tied at z* are all kept, so the set does not
+ * depend on an order among equal logits. p is zeroed outside the nucleus and
+ * renormalised; the nucleus mass P (before renormalising) is returned, z* in
+ * *zstar, and the distance of top_p to the upper mass on either side of the
+ * boundary in *margin. keys: V entries of scratch. */
+typedef struct {
+    double z;
+    int32_t v;
+} OrKey;
+
+static int key_desc(const void *a, const void *b) {
+    const OrKey *x = (const OrKey *)a, *y = (const OrKey *)b;
+    if (x->z != y->z) return x->z > y->z ? -1 : 1;
+    return x->v < y->v ? -1 : (x->v > y->v ? 1 : 0);
+}
+
+static double nucleus(const void *row, int dtype, int32_t V, double top_p, double *p, OrKey *keys,
+                      double *zstar, double *margin) {
+    for (int32_t v = 0; v < V; ++v) {
+        keys[v].z = logit_at(row, dtype, v);
+        keys[v].v = v;
+    }
+    qsort(keys, (size_t)V, sizeof(OrKey), key_desc);
+    double above = 0.0;   /* mass of logits strictly above the current value */
+    int32_t i = 0;
+    *zstar = keys[0].z;
+    *margin = INFINITY;
+    while (i < V) {
+        int32_t j = i;
+        double g = 0.0;   /* mass of the tokens tied at keys[i].z */
+        while (j < V && keys[j].z == keys[i].z) g += p[keys[j++].v];
+        if (above + g >= top_p || j == V) {
+            *zstar = keys[i].z;
+            *margin = dmin(above + g - top_p, top_p - above);
+            break;
+        }
+        above += g;
+        i = j;
+    }
+    double P = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+        if (logit_at(row, dtype, v) >= *zstar) P += p[v];
+        else p[v] = 0.0;
+    }
+    for (int32_t v = 0; v < V; ++v) p[v] /= P;
+    return P;
+}
+
+/* The distribution a model samples from for one row: softmax of sc*z, then,
+ * with top_p < 1, its nucleus renormalised. Returns the log of its
+ * normaliser (lse of the processed row: lse of sc*z plus ln P) and sets
+ * *zstar (-inf without truncation); *margin takes the smaller of itself and
+ * the nucleus boundary's margin. */
+static double processed_row(const void *row, int dtype, int32_t V, double sc, double top_p, double *p,
+                            OrKey *keys, int *ok, double *zstar, double *margin) {
+    double lse = softmax_row(row, dtype, V, sc, p, ok);
+    *zstar = -INFINITY;
+    if (*ok && top_p < 1.0) {
+        double m;
+        lse += log(nucleus(row, dtype, V, top_p, p, keys, zstar, &m));
+        *margin = dmin(*margin, m);
+    }
+    return lse;
 }
 
 /* Index of the largest logit; ties go to the lowest index (reading: the pages
@@ -166,20 +238,19 @@ static void cumulative(const double *r, int32_t V, double Z, double *c) {
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 
-static double dmin(double a, double b) { return a < b ? a : b; }
 
 /* One sequence of the verification pass.
  *  zt: K+1 target rows, row j at zt + j*t_stride elements.
  *  zd: K draft rows (NULL allowed in greedy / FLy mode).
  *  x:  K draft tokens.  u: K+1 uniforms (NULL allowed in greedy / FLy mode).
  * Scratch: p, q, r of V doubles each. */
-static void verify_one(int32_t K, int32_t Kb, double sc, int32_t V, int dtype, int mode,
+static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V, int dtype, int mode,
                        const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
                        const int32_t *x, const float *u, double fly_theta, int32_t fly_window,
                        const double *est, int32_t *out_tokens, int32_t *acc_len,
                        double *pos_stats, double *conf, double *feature,
                        double *margin_acc, double *margin_cdf, double *cdf_out, int *flags,
-                       double *p, double *q, double *r) {
+                       double *p, double *q, double *r, OrKey *keys) {
     const size_t es = dtype == OR_F32 ? 4 : 2;
     const char *tbase = (const char *)zt;
     const char *dbase = (const char *)zd;
@@ -201,18 +272,21 @@ static void verify_one(int32_t K, int32_t Kb, double sc, int32_t V, int dtype, i
     for (int32_t j = 0; j <= Kb; ++j) {
         const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
         int ok;
-        double lse_t = softmax_row(trow, dtype, V, sc, p, &ok);
+        double zs_t, zs_d;
+        double lse_t = processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs_t, &mg);
         if (!ok) fl |= OR_FLAG_BAD_ROW;
         double h = norm_entropy(p, V);
         double lr = NAN, f = NAN;
         if (j < Kb && zd) {
             const void *drow = dbase + (size_t)j * (size_t)d_stride * es;
             int okd;
-            double lse_d = softmax_row(drow, dtype, V, sc, q, &okd);
+            double lse_d = processed_row(drow, dtype, V, sc, top_p, q, keys, &okd, &zs_d, &mg);
             if (!okd) fl |= OR_FLAG_BAD_ROW;
             int32_t amax_d = argmax_row(drow, dtype, V);
             f = logit_qmax(q, V, amax_d, &fl);
-            lr = (sc * logit_at(trow, dtype, x[j]) - lse_t) - (sc * logit_at(drow, dtype, x[j]) - lse_d);
+            /* ln p(x) - ln q(x); a token outside a nucleus has probability 0 */
+            const double zx = logit_at(trow, dtype, x[j]), qx = logit_at(drow, dtype, x[j]);
+            lr = (zx >= zs_t ? sc * zx - lse_t : -INFINITY) - (qx >= zs_d ? sc * qx - lse_d : -INFINITY);
             if (feature) feature[j] = f;
             /* [AV] "Puntuar la Distribución": confidence = sigmoid of the
              * shared slope times logit(q_max) plus the position's intercept;
@@ -239,8 +313,9 @@ static void verify_one(int32_t K, int32_t Kb, double sc, int32_t V, int dtype, i
             const void *trow = tbase + (size_t)i * (size_t)t_stride * es;
             const void *drow = dbase + (size_t)i * (size_t)d_stride * es;
             int ok;
-            softmax_row(trow, dtype, V, sc, p, &ok);
-            softmax_row(drow, dtype, V, sc, q, &ok);
+            double zs;
+            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mg);
+            processed_row(drow, dtype, V, sc, top_p, q, keys, &ok, &zs, &mg);
             double px = p[x[i]], qx = q[x[i]];
             double acc;
             if (qx > 0.0) {
@@ -275,7 +350,8 @@ static void verify_one(int32_t K, int32_t Kb, double sc, int32_t V, int dtype, i
              * draw always uses u[K]). */
             const void *trow = tbase + (size_t)Kb * (size_t)t_stride * es;
             int ok;
-            softmax_row(trow, dtype, V, sc, p, &ok);
+            double zs;
+            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mg);
             double Z = 0.0;
             for (int32_t v = 0; v < V; ++v) Z += p[v];
             token = inverse_cdf(p, V, Z, (double)u[K], &mc, &fl);
@@ -304,7 +380,8 @@ static void verify_one(int32_t K, int32_t Kb, double sc, int32_t V, int dtype, i
             int32_t a = argmax_row(trow, dtype, V);
             if (x[j] == a) continue;               /* no deviation: accept j */
             int ok;
-            softmax_row(trow, dtype, V, sc, p, &ok);
+            double zs;
+            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mg);
             double h = norm_entropy(p, V);
             mg = dmin(mg, fabs(h - fly_theta));
             int reject;
@@ -357,6 +434,9 @@ static void verify_one(int32_t K, int32_t Kb, double sc, int32_t V, int dtype, i
  *    sampling is lossless for whatever p and q it is given). Argmax is
  *    unchanged; lse, entropy, the log-ratio and logit(q_max) are those of
  *    the processed distributions. NULL: temperature 1.
+ *  top_p in (0, 1]: with top_p < 1 every row's processed distribution is
+ *    further truncated to its nucleus (see nucleus()) and renormalised,
+ *    before every use; the nucleus boundary's margin joins margin_acc.
  * nthreads > 0 sets the OpenMP thread count. Returns 0, or -1 on bad args. */
 int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
@@ -364,8 +444,9 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const double *est, int32_t *out_tokens, int32_t *accepted_len,
                   double *pos_stats, double *conf, double *feature,
                   double *margin_acc, double *margin_cdf, double *cdf, int32_t *flags,
-                  const int32_t *draft_len, const float *inv_temp, int nthreads) {
+                  const int32_t *draft_len, const float *inv_temp, double top_p, int nthreads) {
     if (B < 0 || K < 1 || V < 2 || !zt || !x || !out_tokens || !accepted_len) return -1;
+    if (!(top_p > 0.0 && top_p <= 1.0)) return -1;
     if (inv_temp)
         for (int32_t b = 0; b < B; ++b)
             if (!(inv_temp[b] > 0.0f) || isinf(inv_temp[b])) return -1;
@@ -382,14 +463,16 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
         double *p = (double *)malloc(sizeof(double) * (size_t)V);
         double *q = (double *)malloc(sizeof(double) * (size_t)V);
         double *r = (double *)malloc(sizeof(double) * (size_t)V);
-        if (!p || !q || !r) {
+        OrKey *keys = top_p < 1.0 ? (OrKey *)malloc(sizeof(OrKey) * (size_t)V) : NULL;
+        if (!p || !q || !r || (top_p < 1.0 && !keys)) {
 #pragma omp atomic write
             bad = 1;
         } else {
 #pragma omp for schedule(static)
             for (int32_t b = 0; b < B; ++b) {
                 int fl = 0;
-                verify_one(K, draft_len ? draft_len[b] : K, inv_temp ? (double)inv_temp[b] : 1.0, V, dtype, mode,
+                verify_one(K, draft_len ? draft_len[b] : K, inv_temp ? (double)inv_temp[b] : 1.0, top_p, V, dtype,
+                           mode,
                            (const char *)zt + (size_t)b * (size_t)(K + 1) * (size_t)t_stride * es, t_stride,
                            zd ? (const char *)zd + (size_t)b * (size_t)K * (size_t)d_stride * es : NULL, d_stride,
                            x + (size_t)b * K, u ? u + (size_t)b * (K + 1) : NULL, fly_theta, fly_window,
@@ -398,13 +481,14 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                            conf ? conf + (size_t)b * K : NULL,
                            feature ? feature + (size_t)b * K : NULL,
                            margin_acc ? margin_acc + b : NULL, margin_cdf ? margin_cdf + b : NULL,
-                           cdf ? cdf + (size_t)b * (size_t)V : NULL, &fl, p, q, r);
+                           cdf ? cdf + (size_t)b * (size_t)V : NULL, &fl, p, q, r, keys);
                 if (flags) flags[b] = fl;
             }
         }
         free(p);
         free(q);
         free(r);
+        free(keys);
     }
     return bad ? -1 : 0;
 }
