@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--temperature", action="store_true",
                     help="also time temperature-processed verification (spec_verify_temperature) on this "
                          "workload, inverse temperatures log-uniform on [0.5, 2]")
+    ap.add_argument("--top-p", type=float, default=None, dest="top_p",
+                    help="also time top-p (nucleus) processed verification (spec_verify_top_p) at this top_p "
+                         "on this workload, inverse temperatures log-uniform on [0.5, 2]")
     ap.add_argument("--irls", action="store_true",
                     help="also time the IRLS refit entry points (spec_irls_*) on this workload's B, K")
     return ap.parse_args()
@@ -421,6 +424,9 @@ def run_ours(args, w, world, rank, local, pg):
     if args.temperature:
         line["temperature"] = time_temperature(w, args.seed, out, est, ws, dev, stream, peak, logit_bytes,
                                                kern_s * 1e3)
+    if args.top_p is not None:
+        line["top_p"] = time_temperature(w, args.seed, out, est, ws, dev, stream, peak, logit_bytes,
+                                         kern_s * 1e3, top_p=args.top_p)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
     if rank == 0:
@@ -528,11 +534,13 @@ def time_av(w, inp, zd, u, out, est, ws, dev, stream, peak, reps=50):
             "cost_table": "draft 0.01 k/B, verify 1 + 0.05 k/B (synthetic)", "est": "omega 0.5, beta 1.5"}
 
 
-def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, default_ms, reps=100):
+def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, default_ms, reps=100, top_p=None):
     """Device time of one verification at per-sequence inverse temperatures
-    (log-uniform on [0.5, 2]; drafts drawn from the processed q), CUDA events
-    on the launching stream over `reps` back-to-back launches; the inputs
-    (same shapes and logits as the main line) are larger than L2."""
+    (log-uniform on [0.5, 2]; drafts drawn from the temperature-processed q)
+    and, with top_p, at that top-p (spec_verify_top_p: the nucleus pass and
+    the verification launch), CUDA events on the launching stream over `reps`
+    back-to-back calls; the inputs (same shapes and logits as the main line)
+    are larger than L2."""
     import statistics as st
 
     import torch
@@ -550,7 +558,8 @@ def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, defa
     def call():
         sv.verify(inp["zt"], zd, inp["x"], u, mode=w.mode, fly_theta=w.fly_theta, fly_window=w.fly_window,
                   est_params=est if w.with_confidence else None, out=o, workspace=ws,
-                  want_feature=w.with_confidence, want_conf=w.with_confidence, inv_temperature=inp["inv_temp"])
+                  want_feature=w.with_confidence, want_conf=w.with_confidence, inv_temperature=inp["inv_temp"],
+                  top_p=top_p)
 
     for _ in range(5):
         call()
@@ -564,9 +573,14 @@ def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, defa
     ms = [a.elapsed_time(b) for a, b in ev]
     mean_ms = st.mean(ms)
     del inp
-    return {"verify_ms_mean": mean_ms, "verify_ms_median": st.median(ms),
-            "frac": logit_bytes / (mean_ms / 1e3) / 1e9 / peak, "default_verify_ms_mean": default_ms,
-            "inv_temperature": "log-uniform [0.5, 2] per sequence", "kernel": "verify_kernel<T, 1> (temperature variant)"}
+    res = {"verify_ms_mean": mean_ms, "verify_ms_median": st.median(ms),
+           "frac": logit_bytes / (mean_ms / 1e3) / 1e9 / peak, "default_verify_ms_mean": default_ms,
+           "inv_temperature": "log-uniform [0.5, 2] per sequence",
+           "kernel": "verify_kernel<T, 1> (temperature variant)"}
+    if top_p is not None:
+        res["top_p"] = top_p
+        res["kernel"] = "nucleus_kernel<T> + verify_kernel<T, 1> (precomputed rows)"
+    return res
 
 
 def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):

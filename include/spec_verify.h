@@ -298,6 +298,36 @@ int spec_verify_temperature(const spec_verify_params *params, const void *target
                             float *conf, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spec_verify at a sampling top-p, after an optional temperature ([AV]
+ * "Benchmarks": the serving setting samples with top-p 0.95; [SD]
+ * "Математика верификации": the rule is lossless for the distributions the
+ * models sample from). Every row (target and draft) is processed as
+ * p = softmax(s_b z) restricted to its nucleus and renormalised: the nucleus
+ * is every token whose logit is at least z*, the largest logit value whose
+ * tokens (logit >= z*) hold at least top_p of the row's mass; tokens tied
+ * at z* are all kept. The acceptance ratio, residual and bonus draws, FLy
+ * entropy, logit(q_max) and pos_stats read the processed rows; a token
+ * outside a nucleus has probability 0 there (its log-ratio is -inf, or +inf
+ * when only the draft's nucleus excludes it). The caller draws the drafts
+ * from the processed q.
+ *   top_p            in (0, 1]; 1 is spec_verify_temperature (or spec_verify
+ *                    when inv_temperature is NULL).
+ *   inv_temperature  [B] f32 or NULL (s = 1); as for spec_verify_temperature.
+ *   draft_len        [B] int32 or NULL; as for spec_verify_ragged.
+ * Cost: a nucleus pass precedes the verification launch. A thread-block
+ * cluster holds each row in shared memory for the threshold search: one HBM
+ * read per row, for 16-byte aligned rows of up to 256 KB per 8 CTAs. Other
+ * rows take one CTA per row, re-read from L2. Workspace, layouts and status
+ * codes are spec_verify's. Errors: SPEC_ERR_INVALID_ARG for top_p outside
+ * (0, 1].
+ */
+int spec_verify_top_p(const spec_verify_params *params, const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, const int32_t *draft_len, const float *inv_temperature,
+                      float top_p, const float *uniforms, int32_t *out_tokens, int32_t *accepted_len,
+                      float *pos_stats, const float *est_params, float *feature, float *conf, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
  * spec_estimator_update and spec_irls_accumulate for a pruned batch: only
  * verified drafts carry labels, so with kb = draft_len[b] the label at
  * position n_acc (y = 0) exists only when n_acc < kb, and positions >= kb

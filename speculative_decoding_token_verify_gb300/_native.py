@@ -18,7 +18,7 @@ _ROOT = os.path.dirname(_PKG)
 _CSRC = os.path.join(_PKG, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
-SOURCES = ("spec_verify.cu", "spec_estimator.cu", "spec_irls.cu", "spec_av.cu", "spec_ngram.cu")
+SOURCES = ("spec_verify.cu", "spec_nucleus.cu", "spec_estimator.cu", "spec_irls.cu", "spec_av.cu", "spec_ngram.cu")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
@@ -36,7 +36,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile the CUDA sources (in parallel, one object each) and link the
     shared library next to this file. Returns its path."""
     srcs = [os.path.join(_CSRC, s) for s in SOURCES]
-    deps = srcs + [os.path.join(_CSRC, "spec_device.cuh"), os.path.join(_INCLUDE, "spec_verify.h")]
+    deps = srcs + [os.path.join(_CSRC, "spec_device.cuh"), os.path.join(_CSRC, "spec_nucleus.cuh"),
+            os.path.join(_INCLUDE, "spec_verify.h")]
     if (not force and os.path.exists(LIB_PATH)
             and os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps)):
         return LIB_PATH
@@ -106,6 +107,8 @@ SIGNATURES = {
                                           _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_temperature": (ctypes.c_int, [ctypes.POINTER(VerifyParams), _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "spec_verify_top_p": (ctypes.c_int, [ctypes.POINTER(VerifyParams), _P, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                         _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "spec_estimator_update_ragged": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "spec_irls_accumulate_ragged": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P, _P]),
     "spec_av_budget": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),

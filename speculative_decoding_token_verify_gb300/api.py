@@ -116,10 +116,11 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
            want_pos_stats: bool = False, want_feature: bool = False, want_conf: bool = False,
            out: Optional[dict] = None, workspace: Optional[Workspace] = None,
            stream: Optional[torch.cuda.Stream] = None, draft_len: Optional[torch.Tensor] = None,
-           inv_temperature: Optional[torch.Tensor] = None) -> dict:
+           inv_temperature: Optional[torch.Tensor] = None, top_p: Optional[float] = None) -> dict:
     """Run spec_verify (spec_verify_ragged when ``draft_len`` [B] int32 gives
     the drafts verified per sequence of a pruned batch; spec_verify_temperature
-    when ``inv_temperature`` [B] float32 gives 1/T per sequence). Returns a dict with
+    when ``inv_temperature`` [B] float32 gives 1/T per sequence;
+    spec_verify_top_p when ``top_p`` in (0, 1] is given). Returns a dict with
     ``out_tokens`` [B,K+1] int32 and ``accepted_len`` [B] int32, plus
     ``pos_stats`` [B,K+1,4], ``feature`` [B,K] and ``conf`` [B,K] (float32)
     when requested. ``out`` may supply preallocated output tensors under the
@@ -174,7 +175,13 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
     if nbytes == 0:
         raise SpecError(SPEC_ERR_INVALID_ARG, _native.last_error())
     ws = _ws_for(workspace, nbytes, dev)
-    if inv_temperature is not None:
+    if top_p is not None:
+        rc = L.spec_verify_top_p(ctypes.byref(p), _ptr(zt), _ptr(draft_logits), _ptr(x), _ptr(draft_len),
+                                 _ptr(inv_temperature), ctypes.c_float(top_p), _ptr(uniforms),
+                                 _ptr(o["out_tokens"]), _ptr(o["accepted_len"]), _ptr(o.get("pos_stats")),
+                                 _ptr(est_params), _ptr(o.get("feature")), _ptr(o.get("conf")), _ptr(ws),
+                                 ctypes.c_size_t(ws.numel()), _stream_ptr(stream, dev))
+    elif inv_temperature is not None:
         rc = L.spec_verify_temperature(ctypes.byref(p), _ptr(zt), _ptr(draft_logits), _ptr(x), _ptr(draft_len),
                                        _ptr(inv_temperature), _ptr(uniforms), _ptr(o["out_tokens"]),
                                        _ptr(o["accepted_len"]), _ptr(o.get("pos_stats")), _ptr(est_params),

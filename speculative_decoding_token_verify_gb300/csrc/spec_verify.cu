@@ -36,6 +36,7 @@
 #include <string>
 
 #include "spec_device.cuh"
+#include "spec_nucleus.cuh"
 #include "spec_verify.h"
 
 namespace sv {
@@ -96,6 +97,7 @@ enum { CTR_CLAIM = 0, CTR_STATUS = 32, CTR_RES_ALLOC = 64, CTR_RES_CLAIM = 96, k
 struct Draw {
     float lse_t, lse_d;   // temperature variant: A_t, A_d
     float m_t, m_d, sL;   // temperature variant only
+    float th_t, th_d;     // temperature variant: nucleus thresholds (top-p), else -inf
     float u;
     int n;
     bool bonus;   // all verified drafts accepted: the draw is from p_n alone
@@ -109,7 +111,9 @@ struct Args {
     long long ds;            // draft row stride (elements)
     const int32_t *x;
     const int32_t *draft_len; // [B] drafts verified per sequence (pruned batch), or null: all K
-    const float *inv_temp;    // [B] inverse temperature s per sequence (temperature variant only)
+    const float *inv_temp;    // [B] inverse temperature s per sequence, or null: s = 1 (temperature variant)
+    const float *zth;         // [B][rows] nucleus thresholds (top-p), or null (temperature variant)
+    int pre;                  // row statistics precomputed in `part` (one record per row; top-p)
     const float *u;
     const float *est;
     int32_t *out_tokens;
@@ -189,6 +193,7 @@ __device__ __forceinline__ bool temp_ok(float s) {
     return s >= SPEC_MIN_INV_TEMPERATURE && s <= SPEC_MAX_INV_TEMPERATURE;
 }
 __device__ __forceinline__ float seq_inv_temp(const Args &a, int b) {
+    if (!a.inv_temp) return 1.f;
     const float s = __ldg(a.inv_temp + b);
     return temp_ok(s) ? s : 1.f;
 }
@@ -309,14 +314,15 @@ __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float
 }
 
 // one probability of the draw's distributions (see Draw)
+// (the temperature variant: zero outside the row's nucleus)
 template <bool kTemp>
 __device__ __forceinline__ float prob_t(const Draw &d, float z) {
-    if constexpr (kTemp) return ex2(fmaf(z - d.m_t, d.sL, -d.lse_t));
+    if constexpr (kTemp) return z >= d.th_t ? ex2(fmaf(z - d.m_t, d.sL, -d.lse_t)) : 0.f;
     else return ex2((z - d.lse_t) * kLog2e);
 }
 template <bool kTemp>
 __device__ __forceinline__ float prob_d(const Draw &d, float z) {
-    if constexpr (kTemp) return ex2(fmaf(z - d.m_d, d.sL, -d.lse_d));
+    if constexpr (kTemp) return z >= d.th_d ? ex2(fmaf(z - d.m_d, d.sL, -d.lse_d)) : 0.f;
     else return ex2((z - d.lse_d) * kLog2e);
 }
 
@@ -406,9 +412,11 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
     const int K = a.K;
     float sc = 1.f;
     if constexpr (kTemp) {
-        const float s_raw = __ldg(a.inv_temp + b);
-        if (l == 0 && !temp_ok(s_raw)) raise_status(a, SPEC_ERR_BAD_TEMPERATURE);
-        sc = temp_ok(s_raw) ? s_raw : 1.f;
+        if (a.inv_temp) {
+            const float s_raw = __ldg(a.inv_temp + b);
+            if (l == 0 && !temp_ok(s_raw)) raise_status(a, SPEC_ERR_BAD_TEMPERATURE);
+            sc = temp_ok(s_raw) ? s_raw : 1.f;
+        }
     }
     const float sL = kTemp ? sc * kLog2e : kLog2e;
     // a pruned batch verifies drafts 0..kb-1 against target rows 0..kb
@@ -457,9 +465,16 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
     if (bad_row) raise_status(a, SPEC_ERR_BAD_ROW);
     if (bad_tok) raise_status(a, SPEC_ERR_BAD_TOKEN);
     if (!conf_only && l < kb && a.nd_rows > 0) {
-        if (bad_tok) lr = neg_inf();
-        else if constexpr (kTemp) lr = fmaf(sc, zx - tr.M, -lp1_t) - fmaf(sc, qx - dr.M, -lp1_d);
-        else lr = (zx - lse_t) - (qx - lse_d);
+        if (bad_tok) {
+            lr = neg_inf();
+        } else if constexpr (kTemp) {
+            // a token outside a row's nucleus has probability 0 there
+            const bool in_t = !a.zth || zx >= a.zth[(size_t)b * a.rows + l];
+            const bool in_d = !a.zth || qx >= a.zth[(size_t)b * a.rows + a.nt_rows + l];
+            lr = (in_t ? fmaf(sc, zx - tr.M, -lp1_t) : neg_inf()) - (in_d ? fmaf(sc, qx - dr.M, -lp1_d) : neg_inf());
+        } else {
+            lr = (zx - lse_t) - (qx - lse_d);
+        }
     }
     int n = kb;
     if (a.mode == MODE_STOCHASTIC) {
@@ -755,6 +770,7 @@ __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
     d.u = rec.z;
     d.m_t = d.m_d = 0.f;
     d.sL = kLog2e;
+    d.th_t = d.th_d = neg_inf();
     if constexpr (kTemp) {
         const float4 r2 = __ldcg(a.slotrec + 2 * slot + 1);
         d.m_t = r2.x;
@@ -763,6 +779,12 @@ __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
     }
     d.n = (bits >> 1) & 31;
     d.bonus = (bits & 1) != 0;
+    if constexpr (kTemp) {
+        if (a.zth) {
+            d.th_t = __ldg(a.zth + (size_t)b * a.rows + d.n);
+            if (!d.bonus) d.th_d = __ldg(a.zth + (size_t)b * a.rows + a.nt_rows + d.n);
+        }
+    }
     return d;
 }
 
@@ -934,20 +956,22 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             skip = g.target ? g.r > kb : g.r - a.nt_rows >= kb;
         }
         // target rows also carry the entropy moment; draft rows do not need it
-        RowAcc s;
+        RowAcc s = acc_empty();
         if constexpr (kTemp) {
+          if (!a.pre) {
             // the sequence's inverse temperature scales every exponent
             const float sc = seq_inv_temp(a, g.b);
             const float sL = sc * kLog2e, rs = __fdiv_rn(kRescale, sc);   // exact for powers of two
             s = skip ? acc_empty()
                      : (g.target ? unit_consume<T, true, true>(g, l, sL, rs) : unit_consume<T, false, true>(g, l, sL, rs));
+          }
         } else {
             s = skip ? acc_empty() : (g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l));
         }
         const int b = g.b;
         unsigned old = 0u;
         if (l == kSig) {
-            a.part[unit] = acc_pack(s);
+            if (!(kTemp && a.pre)) a.part[unit] = acc_pack(s);   // a precomputed record stays
             old = atom_add_release(a.seq_done + b, 1u);
         }
         // this unit's completion is out; now the previous one, whose count
@@ -986,7 +1010,7 @@ static int fail(int code, const char *fmt, ...) {
 struct Plan {
     int nT, TS, nR, nslice, sstride;
     unsigned long long units;       // stream units: B * rows * nT
-    size_t seq_off, ready_off, done_off, rec_off, part_off, slice_off;
+    size_t seq_off, ready_off, done_off, rec_off, part_off, slice_off, zth_off;
     size_t zero_bytes, bytes;
 };
 
@@ -1027,7 +1051,8 @@ static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace: [header words | seq_done[B] | res_ready[B] | res_done[B]] (zeroed
-// per call) [slot records 2B | tile partials | slices B*sstride]. The
+// per call) [slot records 2B | tile partials | slices B*sstride | nucleus
+// thresholds B*(2K+1)]. The
 // partials hold one slot per stream unit of the largest plan among the row
 // counts the call may stream (`rows_a`, `rows_b`).
 static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan &p) {
@@ -1042,7 +1067,8 @@ static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan
     p.rec_off = align_up(p.zero_bytes, 16);
     p.part_off = align_up(p.rec_off + (size_t)2 * B * sizeof(float4), 16);
     p.slice_off = align_up(p.part_off + (size_t)cap * sizeof(float4), 16);
-    p.bytes = align_up(p.slice_off + (size_t)B * p.sstride * sizeof(float), 16);
+    p.zth_off = align_up(p.slice_off + (size_t)B * p.sstride * sizeof(float), 16);
+    p.bytes = align_up(p.zth_off + (size_t)B * (size_t)(rows_a > rows_b ? rows_a : rows_b) * sizeof(float), 16);
 }
 
 struct DevInfo {
@@ -1090,9 +1116,17 @@ static int grid_for(int dtype, bool temp, unsigned long long units, int *grid) {
     return SPEC_OK;
 }
 
-static int launch(Args &a, const Plan &p, int dtype, void *ws, void *stream) {
+static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, float top_p = 1.f) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(ws);
+    Plan p = p_in;
+    if (a.pre) {
+        // one unit per row: its statistics come from the nucleus pass
+        p.nT = 1;
+        p.TS = a.V;
+        p.units = (unsigned long long)a.B * (unsigned long long)a.rows;
+        a.zth = reinterpret_cast<float *>(base + p.zth_off);
+    }
     a.ctr = reinterpret_cast<unsigned *>(base);
     a.seq_done = reinterpret_cast<unsigned *>(base + p.seq_off);
     a.res_ready = reinterpret_cast<unsigned *>(base + p.ready_off);
@@ -1110,11 +1144,34 @@ static int launch(Args &a, const Plan &p, int dtype, void *ws, void *stream) {
     a.res_units = a.mode == MODE_STOCHASTIC ? (unsigned)a.B * (unsigned)p.nR : 0u;
     a.inv_log_v = (float)(1.0 / std::log((double)a.V));
     int grid = 1;
-    const bool temp = a.inv_temp != nullptr;
+    const bool temp = a.inv_temp != nullptr || a.pre;
     int rc = grid_for(dtype, temp, p.units, &grid);
     if (rc != SPEC_OK) return rc;
     cudaError_t e = cudaMemsetAsync(ws, 0, p.zero_bytes, st);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "workspace reset failed: %s", cudaGetErrorString(e));
+    if (a.pre) {
+        NucleusArgs n;
+        n.zt = a.zt;
+        n.zd = a.zd;
+        n.ts = a.ts;
+        n.ds = a.ds;
+        n.B = a.B;
+        n.K = a.K;
+        n.V = a.V;
+        n.nt_rows = a.nt_rows;
+        n.nd_rows = a.nd_rows;
+        n.t_vec_ok = a.t_vec_ok;
+        n.d_vec_ok = a.d_vec_ok;
+        n.bf16 = dtype == SPEC_BF16 ? 1 : 0;
+        n.draft_len = a.draft_len;
+        n.inv_temp = a.inv_temp;
+        n.top_p = top_p;
+        n.rec = a.part;
+        n.zth = const_cast<float *>(a.zth);
+        n.status = a.ctr + CTR_STATUS;
+        e = launch_nucleus(n, st);
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "nucleus launch failed: %s", cudaGetErrorString(e));
+    }
     if (dtype == SPEC_BF16 && temp)
         verify_kernel<__nv_bfloat16, true><<<grid, NT, kDynSmem, st>>>(a);
     else if (dtype == SPEC_BF16)
@@ -1195,7 +1252,7 @@ size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t d
 
 static int verify_impl(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
                        const int32_t *draft_tokens, const int32_t *draft_len, const float *inv_temp,
-                       const float *uniforms,
+                       float top_p, const float *uniforms,
                        int32_t *out_tokens, int32_t *accepted_len, float *pos_stats, const float *est_params,
                        float *feature, float *conf, void *workspace, size_t workspace_bytes, void *stream) {
     g_err.clear();
@@ -1240,6 +1297,7 @@ static int verify_impl(const spec_verify_params *p, const void *target_logits, c
     a.x = draft_tokens;
     a.draft_len = draft_len;
     a.inv_temp = inv_temp;
+    a.pre = top_p < 1.f ? 1 : 0;
     a.u = uniforms;
     a.est = est_params;
     a.out_tokens = out_tokens;
@@ -1258,7 +1316,7 @@ static int verify_impl(const spec_verify_params *p, const void *target_logits, c
     a.rows = a.nt_rows + a.nd_rows;
     a.t_vec_ok = vec_ok(target_logits, ts, es);
     a.d_vec_ok = draft_logits ? vec_ok(draft_logits, ds, es) : 0;
-    return launch(a, pl, p->dtype, workspace, stream);
+    return launch(a, pl, p->dtype, workspace, stream, top_p);
 }
 
 extern "C" {
@@ -1267,7 +1325,7 @@ int spec_verify(const spec_verify_params *p, const void *target_logits, const vo
                 const int32_t *draft_tokens, const float *uniforms, int32_t *out_tokens,
                 int32_t *accepted_len, float *pos_stats, const float *est_params, float *feature,
                 float *conf, void *workspace, size_t workspace_bytes, void *stream) {
-    return verify_impl(p, target_logits, draft_logits, draft_tokens, nullptr, nullptr, uniforms, out_tokens,
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, nullptr, nullptr, 1.f, uniforms, out_tokens,
                        accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes, stream);
 }
 
@@ -1279,7 +1337,7 @@ int spec_verify_ragged(const spec_verify_params *p, const void *target_logits, c
         g_err = "draft_len is NULL";
         return SPEC_ERR_INVALID_ARG;
     }
-    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, nullptr, uniforms, out_tokens,
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, nullptr, 1.f, uniforms, out_tokens,
                        accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes, stream);
 }
 
@@ -1292,7 +1350,21 @@ int spec_verify_temperature(const spec_verify_params *p, const void *target_logi
         g_err = "inv_temperature is NULL";
         return SPEC_ERR_INVALID_ARG;
     }
-    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, inv_temperature, uniforms,
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, inv_temperature, 1.f, uniforms,
+                       out_tokens, accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes,
+                       stream);
+}
+
+int spec_verify_top_p(const spec_verify_params *p, const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, const int32_t *draft_len, const float *inv_temperature,
+                      float top_p, const float *uniforms, int32_t *out_tokens, int32_t *accepted_len,
+                      float *pos_stats, const float *est_params, float *feature, float *conf, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    if (!(top_p > 0.f && top_p <= 1.f)) {
+        g_err = "top_p must be in (0, 1]";
+        return SPEC_ERR_INVALID_ARG;
+    }
+    return verify_impl(p, target_logits, draft_logits, draft_tokens, draft_len, inv_temperature, top_p, uniforms,
                        out_tokens, accepted_len, pos_stats, est_params, feature, conf, workspace, workspace_bytes,
                        stream);
 }

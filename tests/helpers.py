@@ -29,7 +29,7 @@ def tol_for(dtype) -> float:
 
 
 def oracle_run(inp, mode, fly_theta=0.3, fly_window=6, est=None, with_draft=True, nthreads=8, draft_len=None,
-               inv_temp=None):
+               inv_temp=None, top_p=1.0):
     zt = workloads.to_numpy_logits(inp["zt"])
     zd = workloads.to_numpy_logits(inp["zd"]) if with_draft else None
     x = inp["x"].cpu().numpy()
@@ -37,7 +37,7 @@ def oracle_run(inp, mode, fly_theta=0.3, fly_window=6, est=None, with_draft=True
     r = oracle.verify(zt, zd, x, u, mode=mode, fly_theta=fly_theta, fly_window=fly_window,
                       est_params=None if est is None else np.asarray(est, np.float64),
                       nthreads=nthreads, want_cdf=mode == oracle.STOCHASTIC, draft_len=draft_len,
-                      inv_temp=inv_temp)
+                      inv_temp=inv_temp, top_p=top_p)
     if u is not None:
         r["u_final"] = u[:, -1].astype(np.float64)
     return r
@@ -64,9 +64,15 @@ def _close_unit(g, r, tol):
 
 
 def compare(gpu: dict, ref: dict, dtype, check_pos_stats=True, check_feature=False,
-            check_conf=False, flag_margin=FLAG_MARGIN, max_flagged_frac=0.02):
+            check_conf=False, flag_margin=FLAG_MARGIN, max_flagged_frac=0.02, doubt_frac=None):
     """Assert parity; returns a summary dict (flagged counts, mismatches, worst
-    float error as a fraction of its tolerance)."""
+    float error as a fraction of its tolerance).
+
+    doubt_frac (top-p): sequences whose nucleus boundary the oracle marks as
+    in doubt (flag FLAG_NUCLEUS) may differ in their floats, since the GPU may
+    place that boundary one tie group off; at most max(1, doubt_frac * the
+    number of such sequences) of them may, and every other sequence must meet
+    the tolerances."""
     tol = tol_for(dtype)
     n_g = gpu["accepted_len"].cpu().numpy()
     t_g = gpu["out_tokens"].cpu().numpy()
@@ -104,20 +110,36 @@ def compare(gpu: dict, ref: dict, dtype, check_pos_stats=True, check_feature=Fal
         f"too many acceptance-flagged sequences: {int(acc_flag.sum())} of {B}")
     summary = dict(B=B, flagged_accept=int(acc_flag.sum()), flagged_cdf=int(cdf_flag.sum()),
                    mismatched=int((pre_bad | tok_diff).sum()), token_diff_flagged=int(tok_diff.sum()))
+    doubt = np.zeros(B, bool)
+    if doubt_frac is not None:
+        doubt = (ref["flags"] & oracle.FLAG_NUCLEUS) != 0
+        summary["nucleus_doubt"] = int(doubt.sum())
+    float_bad_doubt = np.zeros(B, bool)
+
+    def _check(bad, name):
+        per_seq = bad.reshape(B, -1).any(1)
+        assert not (per_seq & ~doubt).any(), f"{name} out of tolerance at {np.argwhere(bad)[:3].tolist()}"
+        float_bad_doubt[:] |= per_seq & doubt
+
     if check_pos_stats:
         ps = gpu["pos_stats"].cpu().numpy()
         rp = ref["pos_stats"]
         for k, (name, fn) in enumerate((("lse", _close_log), ("entropy", _close_unit),
                                         ("log_ratio", _close_log), ("feature", _close_log))):
             bad, worst = fn(ps[..., k], rp[..., k], tol)
-            assert not bad.any(), f"pos_stats[{name}] out of tolerance at {np.argwhere(bad)[:3].tolist()}"
+            _check(bad, f"pos_stats[{name}]")
             summary[f"worst_{name}"] = float(worst)
     if check_feature:
         bad, worst = _close_log(gpu["feature"].cpu().numpy(), ref["feature"], tol)
-        assert not bad.any(), "feature out of tolerance"
+        _check(bad, "feature")
         summary["worst_feature_out"] = float(worst)
     if check_conf:
         bad, worst = _close_unit(gpu["conf"].cpu().numpy(), ref["conf"], tol)
-        assert not bad.any(), "conf out of tolerance"
+        _check(bad, "conf")
         summary["worst_conf"] = float(worst)
+    if doubt_frac is not None:
+        nb = int(float_bad_doubt.sum())
+        summary["nucleus_doubt_float_diff"] = nb
+        assert nb <= max(1, doubt_frac * doubt.sum()), (
+            f"{nb} of {int(doubt.sum())} sequences with a nucleus boundary in doubt differ in their floats")
     return summary

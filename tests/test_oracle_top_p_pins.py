@@ -152,8 +152,40 @@ def test_knife_edge_boundary_is_flagged():
     row = np.log(pr).astype(np.float32)
     pf = special.softmax(row.astype(np.float64))
     zt = np.stack([row, row])
-    r = _one_step(zt, row[None], [0], [0.0, 0.5], top_p=float(pf[0] + 1e-7))
+    # top_p just above the first token's mass: the second token (mass .3,
+    # far above the benign size) may be dropped by a slightly different sum
+    r = _one_step(zt, row[None], [0], [0.0, 0.5], top_p=float(pf[0] * (1 + 1e-7)))
     assert r["margin_acc"][0] < 1e-5
+    # top_p just below the first token's mass: the second may be added
+    r = _one_step(zt, row[None], [0], [0.0, 0.5], top_p=float(pf[0] * (1 - 1e-7)))
+    assert r["margin_acc"][0] < 1e-5
+    # nothing above the argmax: dropping it is impossible, nothing is in doubt
+    r = _one_step(zt, row[None], [0], [0.0, 0.5], top_p=1e-9)
+    assert r["margin_acc"][0] > 1e-3
+
+
+def test_benign_boundary_is_not_flagged_but_a_draft_in_it_is():
+    # a long tail of tiny tied tokens: the group (all 3996 of them, 2.5e-8 of
+    # the mass) is below the benign size, so a boundary in doubt there is not
+    # flagged ...
+    V = 4000
+    row = np.full(V, -25.0, np.float32)
+    row[:4] = [0.0, -0.5, -1.0, -1.5]
+    pf = special.softmax(row.astype(np.float64))
+    top_p = float(pf[:4].sum() + 0.5 * pf[4])           # inside the tied tail group
+    zt = np.stack([row, row])
+    r = _one_step(zt, row[None], [0], [0.0, 0.5], top_p=top_p)
+    assert r["margin_acc"][0] > 1e-3
+    # ... a group of 4 tokens of mass 1.5e-4 each is not benign
+    row2 = row.copy()
+    row2[4:8] = -8.0
+    pf2 = special.softmax(row2.astype(np.float64))
+    tp2 = float(pf2[:4].sum() * (1 + 1e-8))              # the group at -8 is the boundary, in doubt
+    r = _one_step(np.stack([row2, row2]), row2[None], [0], [0.0, 0.5], top_p=tp2)
+    assert r["margin_acc"][0] < 1e-5
+    # ... and a draft token in a group in doubt flags the sequence
+    r = _one_step(np.stack([row2, row2]), row2[None], [5], [0.0, 0.5], top_p=tp2)
+    assert r["margin_acc"][0] == 0.0
 
 
 def test_lossless_under_top_p():
