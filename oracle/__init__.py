@@ -30,6 +30,7 @@ FLAG_Z_ZERO = 2
 FLAG_CDF_FALLBACK = 4
 FLAG_REST_ZERO = 8
 FLAG_BAD_ROW = 16
+FLAG_NUCLEUS = 32
 
 _lib = None
 

@@ -48,6 +48,7 @@
 #define OR_FLAG_Z_ZERO 2     /* residual mass 0 after a reject: fell back to p */
 #define OR_FLAG_CDF_FALLBACK 4 /* no cumulative value exceeded u*Z           */
 #define OR_FLAG_REST_ZERO 8  /* logit(q_max) capped at 30 (q_max ~ 1)          */
+#define OR_FLAG_NUCLEUS 32   /* a nucleus boundary (top-p) is in doubt         */
 #define OR_FLAG_BAD_ROW 16   /* a row with no finite logit                    */
 
 /* logit(q_max) when the complement mass is exactly zero */
@@ -97,9 +98,22 @@ static double softmax_row(const void *row, int dtype, int32_t V, double sc, doub
  * largest logit value t for which the tokens with logit >= t hold at least
  * top_p of the mass. Tokens tied at z* are all kept, so the set does not
  * depend on an order among equal logits. p is zeroed outside the nucleus and
- * renormalised; the nucleus mass P (before renormalising) is returned, z* in
- * *zstar, and the distance of top_p to the upper mass on either side of the
- * boundary in *margin. keys: V entries of scratch. */
+ * renormalised; the nucleus mass P (before renormalising) is returned and z*
+ * in *zstar. keys: V entries of scratch.
+ *
+ * Decision margin. A computation whose cumulative masses carry a relative
+ * error e can place the boundary one tie group off: it can drop the group at
+ * z* when (top_p - above) < e above, or add the next group down when
+ * (P - top_p) < e P ("above" = the mass strictly above z*). Such a
+ * difference is harmless when the group in doubt holds at most
+ * OR_NUC_BENIGN of P (it moves every probability by less than that), unless
+ * a draft token is in it. Reading of the flag (the pages fix no precision):
+ * with e = OR_NUC_REL, *margin is the smaller relative distance when a group
+ * in doubt is above OR_NUC_BENIGN, else +inf; *zamb_hi / *zamb_lo are the
+ * logits of the groups in doubt (NaN: none), for the caller to flag a draft
+ * token there. */
+#define OR_NUC_REL 1e-5
+#define OR_NUC_BENIGN 1e-6
 typedef struct {
     double z;
     int32_t v;
@@ -112,7 +126,7 @@ static int key_desc(const void *a, const void *b) {
 }
 
 static double nucleus(const void *row, int dtype, int32_t V, double top_p, double *p, OrKey *keys,
-                      double *zstar, double *margin) {
+                      double *zstar, double *margin, double *zamb_hi, double *zamb_lo) {
     for (int32_t v = 0; v < V; ++v) {
         keys[v].z = logit_at(row, dtype, v);
         keys[v].v = v;
@@ -122,13 +136,26 @@ static double nucleus(const void *row, int dtype, int32_t V, double top_p, doubl
     int32_t i = 0;
     *zstar = keys[0].z;
     *margin = INFINITY;
+    *zamb_hi = *zamb_lo = NAN;
     while (i < V) {
         int32_t j = i;
         double g = 0.0;   /* mass of the tokens tied at keys[i].z */
         while (j < V && keys[j].z == keys[i].z) g += p[keys[j++].v];
         if (above + g >= top_p || j == V) {
+            const double P = above + g;
             *zstar = keys[i].z;
-            *margin = dmin(above + g - top_p, top_p - above);
+            /* the group at z* may be dropped */
+            if (above > 0.0 && top_p - above < OR_NUC_REL * above) {
+                if (g > OR_NUC_BENIGN * P) *margin = dmin(*margin, (top_p - above) / above);
+                *zamb_hi = keys[i].z;
+            }
+            /* the next group down may be added */
+            if (j < V && P - top_p < OR_NUC_REL * P) {
+                double gn = 0.0;
+                for (int32_t k = j; k < V && keys[k].z == keys[j].z; ++k) gn += p[keys[k].v];
+                if (gn > OR_NUC_BENIGN * P) *margin = dmin(*margin, (P - top_p) / P);
+                *zamb_lo = keys[j].z;
+            }
             break;
         }
         above += g;
@@ -147,15 +174,20 @@ static double nucleus(const void *row, int dtype, int32_t V, double top_p, doubl
  * with top_p < 1, its nucleus renormalised. Returns the log of its
  * normaliser (lse of the processed row: lse of sc*z plus ln P) and sets
  * *zstar (-inf without truncation); *margin takes the smaller of itself and
- * the nucleus boundary's margin. */
+ * the nucleus boundary's margin, which is 0 when the logit of token `xtok`
+ * (-1: none) lies in a tie group whose membership is in doubt. */
 static double processed_row(const void *row, int dtype, int32_t V, double sc, double top_p, double *p,
-                            OrKey *keys, int *ok, double *zstar, double *margin) {
+                            OrKey *keys, int *ok, double *zstar, double *margin, int32_t xtok) {
     double lse = softmax_row(row, dtype, V, sc, p, ok);
     *zstar = -INFINITY;
     if (*ok && top_p < 1.0) {
-        double m;
-        lse += log(nucleus(row, dtype, V, top_p, p, keys, zstar, &m));
+        double m, zh, zl;
+        lse += log(nucleus(row, dtype, V, top_p, p, keys, zstar, &m, &zh, &zl));
         *margin = dmin(*margin, m);
+        if (xtok >= 0 && xtok < V) {
+            const double zx = logit_at(row, dtype, xtok);
+            if (zx == zh || zx == zl) *margin = 0.0;
+        }
     }
     return lse;
 }
@@ -255,6 +287,7 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
     const char *tbase = (const char *)zt;
     const char *dbase = (const char *)zd;
     double mg = INFINITY;      /* acceptance (and FLy gate) margin */
+    double mn = INFINITY;      /* nucleus boundary margin (top-p), folded into mg at the end */
     double mc = INFINITY;      /* margin of the final inverse-CDF draw */
     int fl = 0;
 
@@ -273,14 +306,14 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
         const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
         int ok;
         double zs_t, zs_d;
-        double lse_t = processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs_t, &mg);
+        double lse_t = processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs_t, &mn, j < Kb ? x[j] : -1);
         if (!ok) fl |= OR_FLAG_BAD_ROW;
         double h = norm_entropy(p, V);
         double lr = NAN, f = NAN;
         if (j < Kb && zd) {
             const void *drow = dbase + (size_t)j * (size_t)d_stride * es;
             int okd;
-            double lse_d = processed_row(drow, dtype, V, sc, top_p, q, keys, &okd, &zs_d, &mg);
+            double lse_d = processed_row(drow, dtype, V, sc, top_p, q, keys, &okd, &zs_d, &mn, x[j]);
             if (!okd) fl |= OR_FLAG_BAD_ROW;
             int32_t amax_d = argmax_row(drow, dtype, V);
             f = logit_qmax(q, V, amax_d, &fl);
@@ -314,8 +347,8 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
             const void *drow = dbase + (size_t)i * (size_t)d_stride * es;
             int ok;
             double zs;
-            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mg);
-            processed_row(drow, dtype, V, sc, top_p, q, keys, &ok, &zs, &mg);
+            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mn, x[i]);
+            processed_row(drow, dtype, V, sc, top_p, q, keys, &ok, &zs, &mn, x[i]);
             double px = p[x[i]], qx = q[x[i]];
             double acc;
             if (qx > 0.0) {
@@ -351,7 +384,7 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
             const void *trow = tbase + (size_t)Kb * (size_t)t_stride * es;
             int ok;
             double zs;
-            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mg);
+            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mn, -1);
             double Z = 0.0;
             for (int32_t v = 0; v < V; ++v) Z += p[v];
             token = inverse_cdf(p, V, Z, (double)u[K], &mc, &fl);
@@ -381,7 +414,7 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
             if (x[j] == a) continue;               /* no deviation: accept j */
             int ok;
             double zs;
-            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mg);
+            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mn, -1);
             double h = norm_entropy(p, V);
             mg = dmin(mg, fabs(h - fly_theta));
             int reject;
@@ -407,6 +440,8 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
     for (int32_t j = 0; j < n; ++j) out_tokens[j] = x[j];
     out_tokens[n] = token;
     *acc_len = n;
+    if (mn < INFINITY) fl |= OR_FLAG_NUCLEUS;
+    mg = dmin(mg, mn);
     if (margin_acc) *margin_acc = mg;
     if (margin_cdf) *margin_cdf = mc;
     if (flags) *flags = fl;
@@ -436,7 +471,8 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
  *    the processed distributions. NULL: temperature 1.
  *  top_p in (0, 1]: with top_p < 1 every row's processed distribution is
  *    further truncated to its nucleus (see nucleus()) and renormalised,
- *    before every use; the nucleus boundary's margin joins margin_acc.
+ *    before every use; the nucleus boundary's margin (see nucleus()) joins
+ *    margin_acc.
  * nthreads > 0 sets the OpenMP thread count. Returns 0, or -1 on bad args. */
 int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
