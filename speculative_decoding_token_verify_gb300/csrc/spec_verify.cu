@@ -49,7 +49,7 @@ namespace sv {
 #define SV_MIN_BLOCKS 8
 #endif
 #ifndef SV_TILE_BYTES
-#define SV_TILE_BYTES 32768
+#define SV_TILE_BYTES 65536
 #endif
 // slices per residual unit: 8 KB (bf16) or 32 KB (fp32) of the two rows
 #ifndef SV_RES_SLICES_BF16
@@ -60,6 +60,11 @@ namespace sv {
 #endif
 #ifndef SV_UNROLL
 #define SV_UNROLL 4
+#endif
+// the last SV_LAZY_ROUNDS x (resident warps) stream units are claimed when
+// due instead of one unit ahead
+#ifndef SV_LAZY_ROUNDS
+#define SV_LAZY_ROUNDS 4
 #endif
 
 constexpr int NT = SV_THREADS;         // threads per CTA (independent warps)
@@ -131,6 +136,7 @@ struct Args {
     int TS;                  // tile size (elements, multiple of 8)
     unsigned per_seq;        // stream units per sequence (rows * nT)
     unsigned units;          // B * per_seq
+    unsigned lazy_from;      // stream units from here on are claimed when due, not one ahead
     int t_vec_ok, d_vec_ok;  // rows start on 16-byte boundaries
     float inv_log_v;         // 1 / ln V
     unsigned *ctr;           // header words
@@ -146,6 +152,7 @@ struct Args {
                              // temperature variant uses two entries per slot, (A_t, A_d, u, bits)
                              // and (M_t, M_d, sL, 0)
     float *slices;           // [B][sstride] residual mass per slice
+    float *gx;               // [B][2K] logits at the draft tokens: target rows, then draft rows
 };
 
 __device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
@@ -400,6 +407,26 @@ __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *
     }
 }
 
+// The logits at sequence b's draft tokens, zt[b, i, x_i] and zd[b, i, x_i]
+// for the verified positions i, gathered by the warp that streams b's first
+// unit and published with that unit's completion, so that the finalize of b
+// has no load that waits on another (the token, then the logit it indexes).
+template <typename T>
+__device__ __noinline__ void gather_tokens(const Args &a, int b, int l) {
+    const int K = a.K;
+    if (l < verified(a, b)) {
+        const int xv = __ldg(a.x + (size_t)b * K + l);
+        if (xv >= 0 && xv < a.V) {
+            const float zt = Elem<T>::load(trow_ptr<T>(a, b, l) + xv);
+            const float zd = Elem<T>::load(drow_ptr<T>(a, b, l) + xv);
+            a.gx[(size_t)b * 2 * K + l] = zt;
+            a.gx[(size_t)b * 2 * K + K + l] = zd;
+        }
+    }
+    // orders the lanes' stores before lane kSig's release of the unit
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------------------
 // Finalise sequence b with one warp: the lanes merge the row partials (lane j
 // ends with target row j and draft row j), apply the mode's rule, write the
@@ -436,11 +463,13 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
     if (draw && l <= K) ui = a.u[(size_t)b * (K + 1) + l];   // lane K: the residual / bonus uniform
     if (!conf_only && l < kb) {
         xi = a.x[(size_t)b * K + l];
-        bad_tok = xi < 0 || xi >= a.V;
-        if (!bad_tok && a.nd_rows > 0) {
-            zx = Elem<T>::load(trow_ptr<T>(a, b, l) + xi);
-            qx = Elem<T>::load(drow_ptr<T>(a, b, l) + xi);
+        // gathered by the sequence's first stream unit (gather_tokens); the
+        // entries of an invalid token are never written, nor used
+        if (a.gx) {
+            zx = __ldcg(a.gx + (size_t)b * 2 * K + l);
+            qx = __ldcg(a.gx + (size_t)b * 2 * K + K + l);
         }
+        bad_tok = xi < 0 || xi >= a.V;
     }
     RowAcc tr, dr;
     merge_rows(a, b, l, buf, tr, dr, sL);
@@ -853,21 +882,29 @@ __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l)
 // running warps, which never wait, so every wait ends.
 // ---------------------------------------------------------------------------
 struct Sched {
-    unsigned ns;       // claimed next stream unit (>= units: none left)
+    unsigned ns;       // claimed next stream unit (kLazy: claim when due; >= units: none left)
     unsigned pend;     // claimed residual unit (kNone: none)
 };
 constexpr unsigned kNone = 0xffffffffu;
+constexpr unsigned kLazy = 0xfffffffeu;
 
 enum { JOB_DONE = 0, JOB_STREAM = 1, JOB_RESIDUAL = 2, JOB_WAIT = 3 };
 
 // lane 0: the next job that can start now; JOB_WAIT when no stream unit is
-// left and residual work remains (see wait_job).
+// left and residual work remains (see wait_job). Units are claimed one ahead,
+// which hides the claim's latency, except at the end of the queue: there a
+// unit held by a warp that is still busy (streaming, or finalising a
+// sequence) would wait while other warps run dry, so the last units are
+// claimed only when a warp is free to start one.
 __device__ __forceinline__ int next_job(const Args &a, Sched &q, unsigned &id) {
-    if (q.ns < a.units) {
-        id = q.ns;
-        q.ns = atomicAdd(a.ctr + CTR_CLAIM, 1u);
+    unsigned c = q.ns;
+    if (c == kLazy) c = atomicAdd(a.ctr + CTR_CLAIM, 1u);
+    if (c < a.units) {
+        id = c;
+        q.ns = c < a.lazy_from ? atomicAdd(a.ctr + CTR_CLAIM, 1u) : kLazy;
         return JOB_STREAM;
     }
+    q.ns = c;
     return a.res_units ? JOB_WAIT : JOB_DONE;
 }
 
@@ -948,6 +985,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             continue;
         }
         const UnitGeo<T> g = unit_geo<T>(a, unit);
+        if (a.gx && unit == (unsigned)g.b * a.per_seq) gather_tokens<T>(a, g.b, l);
         // rows a pruned batch never verified are not read (their partial is
         // empty; the unit still counts toward its sequence's completion)
         bool skip = false;
@@ -1010,12 +1048,15 @@ static int fail(int code, const char *fmt, ...) {
 struct Plan {
     int nT, TS, nR, nslice, sstride;
     unsigned long long units;       // stream units: B * rows * nT
-    size_t seq_off, ready_off, done_off, rec_off, part_off, slice_off, zth_off;
+    size_t seq_off, ready_off, done_off, rec_off, part_off, slice_off, zth_off, gx_off;
     size_t zero_bytes, bytes;
 };
 
 #ifndef SV_MIN_TILE
 #define SV_MIN_TILE 4096
+#endif
+#ifndef SV_TARGET_UNITS
+#define SV_TARGET_UNITS 16384
 #endif
 // nT tiles of a row of V elements, rounded to a tile size that is a multiple of 8
 static void split_row(int V, long long want, int &nT, int &TS) {
@@ -1027,17 +1068,20 @@ static void split_row(int V, long long want, int &nT, int &TS) {
 
 // A stream unit is one warp's share: a tile of at most SV_TILE_BYTES of
 // logits. Small batches split rows further, down to SV_MIN_TILE elements,
-// aiming at ~32K units (about 7 per resident warp of a GB300) so that the
-// queue's tail stays short. (Finer tiles for just the queue's tail were
-// measured and lost: they lengthen the finalize of exactly the sequences
-// that end the launch.)
+// aiming at ~SV_TARGET_UNITS units (about 3.4 per resident warp of a GB300).
+// Every unit boundary costs a warp a few microseconds without loads in
+// flight (the partial's release, then the first loads of the next tile), so
+// fewer, larger units stream faster; the queue's tail is kept short by
+// claiming its last units only when a warp is free (see next_job). (Finer
+// tiles for just the queue's tail were measured and lost: they lengthen the
+// finalize of exactly the sequences that end the launch.)
 static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
     const int ts_max = SV_TILE_BYTES / esize;
     const long long rows_total = (long long)B * rows;
     long long cap = V / SV_MIN_TILE;
     if (cap < 1) cap = 1;
     long long n = (V + ts_max - 1) / ts_max;
-    long long want = (32768 + rows_total - 1) / rows_total;
+    long long want = (SV_TARGET_UNITS + rows_total - 1) / rows_total;
     if (want > cap) want = cap;
     if (want > n) n = want;
     split_row(V, n, p.nT, p.TS);
@@ -1052,7 +1096,7 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace: [header words | seq_done[B] | res_ready[B] | res_done[B]] (zeroed
 // per call) [slot records 2B | tile partials | slices B*sstride | nucleus
-// thresholds B*(2K+1)]. The
+// thresholds B*(2K+1) | draft-token logits B*2K (sized B*2*(2K+1))]. The
 // partials hold one slot per stream unit of the largest plan among the row
 // counts the call may stream (`rows_a`, `rows_b`).
 static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan &p) {
@@ -1068,7 +1112,9 @@ static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan
     p.part_off = align_up(p.rec_off + (size_t)2 * B * sizeof(float4), 16);
     p.slice_off = align_up(p.part_off + (size_t)cap * sizeof(float4), 16);
     p.zth_off = align_up(p.slice_off + (size_t)B * p.sstride * sizeof(float), 16);
-    p.bytes = align_up(p.zth_off + (size_t)B * (size_t)(rows_a > rows_b ? rows_a : rows_b) * sizeof(float), 16);
+    const size_t rmax = (size_t)(rows_a > rows_b ? rows_a : rows_b);   // >= K
+    p.gx_off = align_up(p.zth_off + (size_t)B * rmax * sizeof(float), 16);
+    p.bytes = align_up(p.gx_off + (size_t)B * 2 * rmax * sizeof(float), 16);
 }
 
 struct DevInfo {
@@ -1134,6 +1180,8 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     a.slotrec = reinterpret_cast<float4 *>(base + p.rec_off);
     a.part = reinterpret_cast<float4 *>(base + p.part_off);
     a.slices = reinterpret_cast<float *>(base + p.slice_off);
+    // draft-token logits are gathered wherever the finalize forms log-ratios
+    a.gx = (a.mode != MODE_CONF && a.nd_rows > 0) ? reinterpret_cast<float *>(base + p.gx_off) : nullptr;
     a.nT = p.nT;
     a.TS = p.TS;
     a.per_seq = (unsigned)a.rows * (unsigned)p.nT;
@@ -1147,6 +1195,8 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     const bool temp = a.inv_temp != nullptr || a.pre;
     int rc = grid_for(dtype, temp, p.units, &grid);
     if (rc != SPEC_OK) return rc;
+    const unsigned long long lazy = (unsigned long long)SV_LAZY_ROUNDS * (unsigned long long)grid * NWARP;
+    a.lazy_from = p.units > lazy ? (unsigned)(p.units - lazy) : 0u;
     cudaError_t e = cudaMemsetAsync(ws, 0, p.zero_bytes, st);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "workspace reset failed: %s", cudaGetErrorString(e));
     if (a.pre) {
