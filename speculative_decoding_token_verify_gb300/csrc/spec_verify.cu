@@ -135,7 +135,12 @@ struct Args {
     int nT;                  // tiles per row
     int TS;                  // tile size (elements, multiple of 8)
     unsigned per_seq;        // stream units per sequence (rows * nT)
-    unsigned units;          // B * per_seq
+    unsigned units;          // head_units + (B - B1) * per_seq2
+    // the queue's last sequences (b >= B1) stream in smaller tiles (nT2 of
+    // TS2 elements per row), so that the last units of the launch are short
+    int B1, nT2, TS2;
+    unsigned per_seq2;       // rows * nT2
+    unsigned head_units;     // B1 * per_seq
     unsigned lazy_from;      // stream units from here on are claimed when due, not one ahead
     int t_vec_ok, d_vec_ok;  // rows start on 16-byte boundaries
     float inv_log_v;         // 1 / ln V
@@ -182,6 +187,8 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 
 // drafts verified for sequence b: draft_len[b] clamped to [0, K], or K
@@ -254,14 +261,32 @@ struct UnitGeo {
     bool target;      // a target row (carries the entropy moment)
 };
 
+// first stream unit (= partial slot) of sequence b, and its unit count
+__device__ __forceinline__ unsigned seq_base(const Args &a, int b) {
+    return b < a.B1 ? (unsigned)b * a.per_seq : a.head_units + (unsigned)(b - a.B1) * a.per_seq2;
+}
+__device__ __forceinline__ unsigned seq_units(const Args &a, int b) { return b < a.B1 ? a.per_seq : a.per_seq2; }
+
 template <typename T>
 __device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit) {
     UnitGeo<T> g;
-    const int b = (int)(unit / a.per_seq);
-    const unsigned rem = unit - (unsigned)b * a.per_seq;
-    const int r = (int)(rem / (unsigned)a.nT);
-    const int t = (int)(rem - (unsigned)r * (unsigned)a.nT);
-    const int TS = a.TS;
+    int b, nT, TS;
+    unsigned rem;
+    if (unit < a.head_units) {
+        b = (int)(unit / a.per_seq);
+        rem = unit - (unsigned)b * a.per_seq;
+        nT = a.nT;
+        TS = a.TS;
+    } else {
+        const unsigned u = unit - a.head_units;
+        const int bt = (int)(u / a.per_seq2);
+        b = a.B1 + bt;
+        rem = u - (unsigned)bt * a.per_seq2;
+        nT = a.nT2;
+        TS = a.TS2;
+    }
+    const int r = (int)(rem / (unsigned)nT);
+    const int t = (int)(rem - (unsigned)r * (unsigned)nT);
     g.b = b;
     g.r = r;
     g.target = r < a.nt_rows;
@@ -375,9 +400,9 @@ __device__ __forceinline__ RowAcc shfl_acc(const RowAcc &a, int src) {
 // (tiles hold >= 4096 of at most 2^20 elements).
 __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *buf, RowAcc &tr, RowAcc &dr,
                                            float sL) {
-    const int nT = a.nT;
+    const int nT = b < a.B1 ? a.nT : a.nT2;
     const int rc = min(kStage / nT, 32);       // whole rows per staging pass, one lane each at least
-    const float4 *base = a.part + (size_t)b * a.per_seq;
+    const float4 *base = a.part + seq_base(a, b);
     const int drow = a.nt_rows + l;            // row index of lane l's draft row
     tr = acc_empty();
     dr = acc_empty();
@@ -759,11 +784,69 @@ __device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int
     }
 }
 
+// Lane sums of kResBatch whole slices s0 .. that lane l staged in the warp's
+// buffer (entry 64 i + l: target row, 64 i + 32 + l: draft row; each lane
+// reads only what it copied). Same per-lane order as slice_lane_sum.
+template <bool kDraft, bool kTemp>
+__device__ __forceinline__ void batch_staged_bf16(const float4 *buf, int l, const Draw &d,
+                                                  float (&part)[kResBatch]) {
+#pragma unroll
+    for (int i = 0; i < kResBatch; ++i) {
+        const float4 vt = buf[64 * i + l];
+        float zt[8], r[8];
+        Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(&vt), zt);
+        if constexpr (kDraft) {
+            const float4 vd = buf[64 * i + 32 + l];
+            float zd[8];
+            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(&vd), zd);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r[j] = fmaxf(prob_t<kTemp>(d, zt[j]) - prob_d<kTemp>(d, zd[j]), 0.f);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r[j] = prob_t<kTemp>(d, zt[j]);
+        }
+        part[i] = sum8(r);
+    }
+}
+
 // Slices s0 .. s0 + res_slices<T>() - 1 of the draw's weights (kResBatch slices'
-// loads in flight at a time); lane kSig stores their sums.
+// loads in flight at a time); lane kSig stores their sums. For bf16 rows
+// holding a whole unit of two batches, the second batch is copied to the
+// warp's staging buffer while the first is loaded to registers, so the
+// unit costs one memory round trip, not two.
 template <typename T, bool kTemp>
 __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T *tr, const T *dr, const Draw &d,
-                                          int l) {
+                                          int l, float4 *buf) {
+    if constexpr (sizeof(T) == 2 && res_slices<T>() == 2 * kResBatch) {
+        const bool fast = a.t_vec_ok && (dr == nullptr || a.d_vec_ok) && (s0 + 2 * kResBatch) * kSlice <= a.V;
+        if (fast) {
+            const int s1 = s0 + kResBatch;
+#pragma unroll
+            for (int i = 0; i < kResBatch; ++i) {
+                cp_async16(buf + 64 * i + l, tr + (s1 + i) * kSlice + l * 8);
+                if (dr) cp_async16(buf + 64 * i + 32 + l, dr + (s1 + i) * kSlice + l * 8);
+            }
+            cp_async_commit();
+            float part[kResBatch];
+            if (dr) batch_fast<T, true, kTemp>(tr, dr, s0, l, d, part);
+            else batch_fast<T, false, kTemp>(tr, dr, s0, l, d, part);
+#pragma unroll
+            for (int i = 0; i < kResBatch; ++i) {
+                const float sm = warp_sum_f(part[i]);
+                if (l == kSig) a.slices[(size_t)b * a.sstride + s0 + i] = sm;
+            }
+            cp_async_wait();
+            if (dr) batch_staged_bf16<true, kTemp>(buf, l, d, part);
+            else batch_staged_bf16<false, kTemp>(buf, l, d, part);
+#pragma unroll
+            for (int i = 0; i < kResBatch; ++i) {
+                const float sm = warp_sum_f(part[i]);
+                if (l == kSig) a.slices[(size_t)b * a.sstride + s1 + i] = sm;
+            }
+            __syncwarp();   // the buffer is reused by the next staged job
+            return;
+        }
+    }
 #pragma unroll
     for (int i0 = 0; i0 < res_slices<T>(); i0 += kResBatch) {
         float part[kResBatch];
@@ -829,7 +912,7 @@ __device__ __noinline__ void locate(const Args &a, int slot, int l, float4 *buf)
     const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
     int token = locate_scan<T, kTemp>(a, b, tr, dr, d, l, buf);
     if (token < 0 && dr != nullptr) {
-        for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T, kTemp>(a, b, s0, tr, nullptr, d, l);
+        for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T, kTemp>(a, b, s0, tr, nullptr, d, l, buf);
         __threadfence();
         __syncwarp();
         token = locate_scan<T, kTemp>(a, b, tr, nullptr, d, l, buf);
@@ -850,14 +933,14 @@ struct ResDone {
 };
 
 template <typename T, bool kTemp>
-__device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l) {
+__device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l, float4 *buf) {
     const int slot = (int)(id / (unsigned)a.nR);
     const int t = (int)(id - (unsigned)slot * (unsigned)a.nR);
     int b;
     const Draw d = decode_slot<kTemp>(a, slot, b);
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
-    unit_sums<T, kTemp>(a, b, t * res_slices<T>(), tr, dr, d, l);
+    unit_sums<T, kTemp>(a, b, t * res_slices<T>(), tr, dr, d, l, buf);
     ResDone r;
     r.slot = slot;
     r.old = 0u;
@@ -883,7 +966,7 @@ __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l)
 // ---------------------------------------------------------------------------
 struct Sched {
     unsigned ns;       // claimed next stream unit (kLazy: claim when due; >= units: none left)
-    unsigned pend;     // claimed residual unit (kNone: none)
+    unsigned pend;     // claimed residual unit (kNone: none claimed; >= res_units: none left)
 };
 constexpr unsigned kNone = 0xffffffffu;
 constexpr unsigned kLazy = 0xfffffffeu;
@@ -915,14 +998,15 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
     for (unsigned it = 0; it < kSpinLimit; ++it) {
         if (q.pend == kNone) {
             if (ld_relaxed(a.ctr + CTR_RES_CLAIM) >= a.res_units) return JOB_DONE;
-            const unsigned c = atomicAdd(a.ctr + CTR_RES_CLAIM, 1u);
-            if (c >= a.res_units) return JOB_DONE;
-            q.pend = c;
+            q.pend = atomicAdd(a.ctr + CTR_RES_CLAIM, 1u);
         }
+        if (q.pend >= a.res_units) return JOB_DONE;
         if (ld_relaxed(a.res_ready + q.pend / (unsigned)a.nR)) {
             fence_acquire();
             id = q.pend;
-            q.pend = kNone;
+            // the next unit is claimed now; its reply is read only when this
+            // unit is done
+            q.pend = atomicAdd(a.ctr + CTR_RES_CLAIM, 1u);
             return JOB_RESIDUAL;
         }
         __nanosleep(ns);
@@ -963,7 +1047,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         kind = __shfl_sync(kFull, kind, 0);
         unit = __shfl_sync(kFull, unit, 0);
         if (kind != JOB_STREAM && due != DUE_NONE) {
-            const unsigned need = due == DUE_STREAM ? a.per_seq - 1u : (unsigned)a.nR - 1u;
+            const unsigned need = due == DUE_STREAM ? seq_units(a, due_id) - 1u : (unsigned)a.nR - 1u;
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
                 if (due == DUE_STREAM) finalize<T, kTemp>(a, due_id, l, wbuf);
@@ -978,14 +1062,14 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         }
         if (kind == JOB_DONE) break;
         if (kind == JOB_RESIDUAL) {
-            const ResDone r = residual_unit<T, kTemp>(a, unit, l);
+            const ResDone r = residual_unit<T, kTemp>(a, unit, l, wbuf);
             due = DUE_RESIDUAL;
             due_id = r.slot;
             due_old = r.old;
             continue;
         }
         const UnitGeo<T> g = unit_geo<T>(a, unit);
-        if (a.gx && unit == (unsigned)g.b * a.per_seq) gather_tokens<T>(a, g.b, l);
+        if (a.gx && unit == seq_base(a, g.b)) gather_tokens<T>(a, g.b, l);
         // rows a pruned batch never verified are not read (their partial is
         // empty; the unit still counts toward its sequence's completion)
         bool skip = false;
@@ -1015,7 +1099,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         // this unit's completion is out; now the previous one, whose count
         // has had a whole unit to come back
         if (due != DUE_NONE) {
-            const unsigned need = due == DUE_STREAM ? a.per_seq - 1u : (unsigned)a.nR - 1u;
+            const unsigned need = due == DUE_STREAM ? seq_units(a, due_id) - 1u : (unsigned)a.nR - 1u;
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
                 if (due == DUE_STREAM) finalize<T, kTemp>(a, due_id, l, wbuf);
@@ -1047,7 +1131,9 @@ static int fail(int code, const char *fmt, ...) {
 
 struct Plan {
     int nT, TS, nR, nslice, sstride;
-    unsigned long long units;       // stream units: B * rows * nT
+    int B1, nT2, TS2;               // the tail: sequences B1.. stream nT2 tiles of TS2 per row
+    unsigned long long head_units;  // B1 * rows * nT
+    unsigned long long units;       // stream units: head_units + (B - B1) * rows * nT2
     size_t seq_off, ready_off, done_off, rec_off, part_off, slice_off, zth_off, gx_off;
     size_t zero_bytes, bytes;
 };
@@ -1057,6 +1143,15 @@ struct Plan {
 #endif
 #ifndef SV_TARGET_UNITS
 #define SV_TARGET_UNITS 16384
+#endif
+// in stochastic mode the queue's last ~SV_TAIL_BYTES of logits (whole
+// sequences, at most half the batch) stream in tiles of SV_TAIL_TILE_BYTES;
+// 0 turns the tail off
+#ifndef SV_TAIL_BYTES
+#define SV_TAIL_BYTES (80ll << 20)
+#endif
+#ifndef SV_TAIL_TILE_BYTES
+#define SV_TAIL_TILE_BYTES 32768
 #endif
 // nT tiles of a row of V elements, rounded to a tile size that is a multiple of 8
 static void split_row(int V, long long want, int &nT, int &TS) {
@@ -1071,10 +1166,11 @@ static void split_row(int V, long long want, int &nT, int &TS) {
 // aiming at ~SV_TARGET_UNITS units (about 3.4 per resident warp of a GB300).
 // Every unit boundary costs a warp a few microseconds without loads in
 // flight (the partial's release, then the first loads of the next tile), so
-// fewer, larger units stream faster; the queue's tail is kept short by
-// claiming its last units only when a warp is free (see next_job). (Finer
-// tiles for just the queue's tail were measured and lost: they lengthen the
-// finalize of exactly the sequences that end the launch.)
+// fewer, larger units stream faster. The queue's end is kept short in two
+// ways: its last units are claimed only when a warp is free (see next_job),
+// and in stochastic mode its last sequences (the tail) stream in smaller
+// tiles, so that the last unit, and with it the chain of finalize, residual
+// pass and locate of the last sequences, ends sooner.
 static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
     const int ts_max = SV_TILE_BYTES / esize;
     const long long rows_total = (long long)B * rows;
@@ -1085,7 +1181,21 @@ static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
     if (want > cap) want = cap;
     if (want > n) n = want;
     split_row(V, n, p.nT, p.TS);
-    p.units = (unsigned long long)B * rows * p.nT;
+    p.B1 = B;
+    p.nT2 = p.nT;
+    p.TS2 = p.TS;
+    const int ts2 = SV_TAIL_TILE_BYTES / esize;
+    if (SV_TAIL_BYTES > 0 && ts2 >= SV_MIN_TILE && ts2 < p.TS) {
+        const long long seq_bytes = (long long)rows * V * esize;
+        long long nt = (SV_TAIL_BYTES + seq_bytes - 1) / seq_bytes;
+        if (nt > B / 2) nt = B / 2;
+        if (nt > 0) {
+            split_row(V, (V + ts2 - 1) / ts2, p.nT2, p.TS2);
+            p.B1 = B - (int)nt;
+        }
+    }
+    p.head_units = (unsigned long long)p.B1 * rows * p.nT;
+    p.units = p.head_units + (unsigned long long)(B - p.B1) * rows * p.nT2;
     p.nslice = (V + kSlice - 1) / kSlice;
     p.sstride = (p.nslice + 3) & ~3;
     const int rs = esize == 2 ? res_slices<__nv_bfloat16>() : res_slices<float>();
@@ -1171,6 +1281,10 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
         p.nT = 1;
         p.TS = a.V;
         p.units = (unsigned long long)a.B * (unsigned long long)a.rows;
+        p.B1 = a.B;
+        p.nT2 = 1;
+        p.TS2 = a.V;
+        p.head_units = p.units;
         a.zth = reinterpret_cast<float *>(base + p.zth_off);
     }
     a.ctr = reinterpret_cast<unsigned *>(base);
@@ -1182,9 +1296,22 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     a.slices = reinterpret_cast<float *>(base + p.slice_off);
     // draft-token logits are gathered wherever the finalize forms log-ratios
     a.gx = (a.mode != MODE_CONF && a.nd_rows > 0) ? reinterpret_cast<float *>(base + p.gx_off) : nullptr;
+    if (a.mode != MODE_STOCHASTIC && !a.pre) {
+        // short tail units pay off only where a draw (finalize, residual
+        // pass, locate) follows the last unit of the queue
+        p.B1 = a.B;
+        p.nT2 = p.nT;
+        p.TS2 = p.TS;
+        p.head_units = p.units = (unsigned long long)a.B * (unsigned long long)a.rows * (unsigned long long)p.nT;
+    }
     a.nT = p.nT;
     a.TS = p.TS;
     a.per_seq = (unsigned)a.rows * (unsigned)p.nT;
+    a.B1 = p.B1;
+    a.nT2 = p.nT2;
+    a.TS2 = p.TS2;
+    a.per_seq2 = (unsigned)a.rows * (unsigned)p.nT2;
+    a.head_units = (unsigned)p.head_units;
     a.nR = p.nR;
     a.nslice = p.nslice;
     a.sstride = p.sstride;
