@@ -59,6 +59,9 @@ def parse_args():
                          "on this workload, inverse temperatures log-uniform on [0.5, 2]")
     ap.add_argument("--irls", action="store_true",
                     help="also time the IRLS refit entry points (spec_irls_*) on this workload's B, K")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time spec_verify alone at every point of the throughput sweep (B x K x V x dtype, "
+                         "stochastic) and print one JSON line per point instead of the step line")
     return ap.parse_args()
 
 
@@ -583,6 +586,63 @@ def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, defa
     return res
 
 
+def run_sweep(args):
+    """spec_verify alone at every sweep point, inputs resident in HBM: CUDA
+    events around each call on the launching stream; an L2 flush (a write of
+    256 MB) before each call where the logits are under twice the L2 size."""
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_src = measured_hbm_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(0, enabled=not args.no_clocks)
+    clocks.start()
+    lines = []
+    for k, w in enumerate(workloads.sweep()):
+        inp = workloads.make_inputs(w, 2000 + k, dev)
+        ws = sv.Workspace(dev)
+        out = {"out_tokens": torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev),
+               "accepted_len": torch.empty((w.B,), dtype=torch.int32, device=dev)}
+        logit_bytes = w.logit_bytes(True)
+        small = logit_bytes <= 2 * 129e6
+
+        def call():
+            sv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], mode="stochastic", out=out, workspace=ws)
+
+        for _ in range(max(args.warmup, 3)):
+            call()
+        reps = max(10, min(args.steps, 100))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            if small:
+                flush.add_(1)
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = [a.elapsed_time(b) for a, b in ev]
+        mean_s = statistics.mean(ms) / 1e3
+        line = {"metric": METRIC, "workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
+                "ms_mean": mean_s * 1e3, "ms_median": statistics.median(ms),
+                "positions_per_s": w.B * w.K / mean_s, "hbm_gbs": logit_bytes / mean_s / 1e9,
+                "frac": logit_bytes / mean_s / 1e9 / peak, "peak": peak,
+                "algorithmic_bytes": logit_bytes,
+                "l2": "flushed before each call" if small else "inputs larger than L2",
+                "status": sv.device_status(ws.buf)}
+        print(json.dumps(line), flush=True)
+        lines.append(line)
+        del inp, ws, out
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    print(json.dumps({"sweep_points": len(lines), "clocks": clk, "peak_source": peak_src}), flush=True)
+    return 0
+
+
 def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):
     """Same metric through the public API with HOST inputs: every step copies
     its inputs from pinned host memory and reads its results back."""
@@ -631,6 +691,8 @@ def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):
 
 def main():
     args = parse_args()
+    if args.sweep:
+        return run_sweep(args)
     w = get_workload(args)
     world, rank, local, pg = dist_setup(args)
     if world != args.gpus and rank == 0:

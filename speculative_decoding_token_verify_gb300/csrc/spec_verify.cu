@@ -496,6 +496,14 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         }
         bad_tok = xi < 0 || xi >= a.V;
     }
+    // the estimator parameters too (read after the outputs are stored, they
+    // would cost a round trip of their own: the compiler cannot move a load
+    // across stores that may alias it)
+    float e_omega = 0.f, e_beta = 0.f;
+    if (a.conf && a.est && l < a.nd_rows) {
+        e_omega = __ldg(a.est);
+        e_beta = __ldg(a.est + 1 + l);
+    }
     RowAcc tr, dr;
     merge_rows(a, b, l, buf, tr, dr, sL);
     float lse_t = nan, h = nan, lse_d = nan, f = nan, lr = nan;
@@ -562,6 +570,34 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         }
     }
     // per-position outputs
+    if (a.mode != MODE_CONF) {
+        // the draw's weights: lse (s = 1), or M and A = log2(1 + R) (see Draw)
+        const float lt_n = __shfl_sync(kFull, kTemp ? lp1_t * kLog2e : lse_t, n);
+        const float ld_n = __shfl_sync(kFull, kTemp ? lp1_d * kLog2e : lse_d, n);
+        float mt_n = 0.f, md_n = 0.f;
+        if constexpr (kTemp) {
+            mt_n = __shfl_sync(kFull, tr.M, n);
+            md_n = __shfl_sync(kFull, dr.M, n);
+        }
+        const int am_n = __shfl_sync(kFull, amax_t, n);
+        const float u_draw = __shfl_sync(kFull, ui, K);
+        if (draw && l == kSig) {
+            // hand the draw to the residual units of b before any other
+            // output goes out, so that the release waits on the record
+            // alone; the release store orders the record before the flag
+            const float4 rec = make_float4(lt_n, ld_n, u_draw, __int_as_float((b << 6) | (n << 1) | (n == kb ? 1 : 0)));
+            if constexpr (kTemp) {
+                a.slotrec[2 * slot] = rec;
+                a.slotrec[2 * slot + 1] = make_float4(mt_n, md_n, sL, 0.f);
+            } else {
+                a.slotrec[slot] = rec;
+            }
+            st_release(a.res_ready + slot, 1u);
+        }
+        // K <= 31: lane j writes position j (lane j holds draft token j)
+        if (l <= K && !(draw && l == n)) a.out_tokens[(size_t)b * (K + 1) + l] = l < n ? xi : (l == n ? am_n : -1);
+        if (l == kSig) a.acc_len[b] = n;
+    }
     if (a.mode != MODE_CONF && a.pos_stats && l <= K) {
         float *ps = a.pos_stats + ((size_t)b * (K + 1) + l) * 4;
         ps[0] = lse_t;
@@ -572,36 +608,8 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
     if (a.feature && l < a.nd_rows) a.feature[(size_t)b * K + l] = f;
     if (a.conf && a.est && l < a.nd_rows) {
         // "Puntuar la Distribución": sigmoid(omega * logit(q_max) + beta_{i+1})
-        const float z = a.est[0] * f + a.est[1 + l];
+        const float z = e_omega * f + e_beta;
         a.conf[(size_t)b * K + l] = l < kb ? 1.f / (1.f + expf(-z)) : nan;
-    }
-    if (a.mode == MODE_CONF) return;
-    // the draw's weights: lse (s = 1), or M and A = log2(1 + R) (see Draw)
-    const float lt_n = __shfl_sync(kFull, kTemp ? lp1_t * kLog2e : lse_t, n);
-    const float ld_n = __shfl_sync(kFull, kTemp ? lp1_d * kLog2e : lse_d, n);
-    float mt_n = 0.f, md_n = 0.f;
-    if constexpr (kTemp) {
-        mt_n = __shfl_sync(kFull, tr.M, n);
-        md_n = __shfl_sync(kFull, dr.M, n);
-    }
-    const int am_n = __shfl_sync(kFull, amax_t, n);
-    const float u_draw = __shfl_sync(kFull, ui, K);
-    // K <= 31: lane j writes position j (lane j holds draft token j)
-    if (l <= K && !(draw && l == n)) a.out_tokens[(size_t)b * (K + 1) + l] = l < n ? xi : (l == n ? am_n : -1);
-    if (l == kSig) {
-        a.acc_len[b] = n;
-        if (draw) {
-            // hand the draw to the residual units of b; the release store
-            // orders the record before the flag
-            const float4 rec = make_float4(lt_n, ld_n, u_draw, __int_as_float((b << 6) | (n << 1) | (n == kb ? 1 : 0)));
-            if constexpr (kTemp) {
-                a.slotrec[2 * slot] = rec;
-                a.slotrec[2 * slot + 1] = make_float4(mt_n, md_n, sL, 0.f);
-            } else {
-                a.slotrec[slot] = rec;
-            }
-            st_release(a.res_ready + slot, 1u);
-        }
     }
 }
 
@@ -627,10 +635,13 @@ __device__ __forceinline__ float slice_lane_sum(const Args &a, const T *tr, cons
 // Stage slice sums c0 .. c0 + 32*kScanPer - 1 of one sequence (row start
 // 16-byte aligned) in the warp's buffer; lane l then owns the contiguous run
 // l*kScanPer .. of the chunk. Entries past n are not staged and read as 0.
-__device__ __forceinline__ void stage_slices(const float *ss, int n, int c0, int l, float4 *buf) {
+__device__ __forceinline__ void stage_issue(const float *ss, int n, int c0, int l, float4 *buf) {
     const int cn = min(4 * kStage, n - c0);
     const float4 *src = reinterpret_cast<const float4 *>(ss + c0);
     for (int i = l; i < (cn + 3) / 4; i += 32) cp_async16(buf + i, src + i);
+}
+__device__ __forceinline__ void stage_slices(const float *ss, int n, int c0, int l, float4 *buf) {
+    stage_issue(ss, n, c0, l, buf);
     cp_async_wait_all();
     __syncwarp();
 }
@@ -654,14 +665,20 @@ __device__ __forceinline__ float run_sum(const float4 *buf, int l, int cn) {
 // fp64 prefix across lanes. Returns the token, or -1 when Z is not positive
 // (only possible through rounding, or a bad row).
 template <typename T, bool kTemp>
-__device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l, float4 *buf) {
+__device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l, float4 *buf,
+                           bool prestaged = false) {
     const float *ss = a.slices + (size_t)b * a.sstride;
     const int n = a.nslice;
     constexpr int kChunk = 32 * kScanPer;
-    // pass 1: Z
+    // pass 1: Z (the first chunk's copies may already be in flight)
     double Z = 0.0;
     for (int c0 = 0; c0 < n; c0 += kChunk) {
-        stage_slices(ss, n, c0, l, buf);
+        if (c0 == 0 && prestaged) {
+            cp_async_wait_all();
+            __syncwarp();
+        } else {
+            stage_slices(ss, n, c0, l, buf);
+        }
         Z += warp_sum_d((double)run_sum(buf, l, n - c0));
         __syncwarp();
     }
@@ -904,13 +921,17 @@ __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
 // token. If the residual mass vanished (only possible through rounding) the
 // warp redraws from p.
 template <typename T, bool kTemp>
-__device__ __noinline__ void locate(const Args &a, int slot, int l, float4 *buf) {
+__device__ __noinline__ void locate(const Args &a, int slot, int b_known, int l, float4 *buf) {
+    // the sequence is known, so its slice sums are staged while the draw
+    // record is read
+    stage_issue(a.slices + (size_t)b_known * a.sstride, a.nslice, 0, l, buf);
     int b;
     const Draw d = decode_slot<kTemp>(a, slot, b);
     const int K = a.K;
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
-    int token = locate_scan<T, kTemp>(a, b, tr, dr, d, l, buf);
+    if (b != b_known) cp_async_wait_all();   // never (a slot names one sequence): restage safely
+    int token = locate_scan<T, kTemp>(a, b, tr, dr, d, l, buf, b == b_known);
     if (token < 0 && dr != nullptr) {
         for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T, kTemp>(a, b, s0, tr, nullptr, d, l, buf);
         __threadfence();
@@ -929,6 +950,7 @@ __device__ __noinline__ void locate(const Args &a, int slot, int l, float4 *buf)
 // counter; the returned count (lane kSig) says whether this was its last unit.
 struct ResDone {
     int slot;
+    int b;
     unsigned old;
 };
 
@@ -943,6 +965,7 @@ __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l,
     unit_sums<T, kTemp>(a, b, t * res_slices<T>(), tr, dr, d, l, buf);
     ResDone r;
     r.slot = slot;
+    r.b = b;
     r.old = 0u;
     if (l == kSig) r.old = atom_add_release(a.res_done + b, 1u);
     return r;
@@ -1039,6 +1062,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
     // finalize or locate it may owe is always done before the warp waits.
     int due = DUE_NONE;
     int due_id = 0;           // sequence (stream) or slot (residual)
+    int due_b = 0;            // the slot's sequence (residual)
     unsigned due_old = 0u;    // the count returned to lane kSig
     for (;;) {
         int kind = 0;
@@ -1051,7 +1075,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
                 if (due == DUE_STREAM) finalize<T, kTemp>(a, due_id, l, wbuf);
-                else locate<T, kTemp>(a, due_id, l, wbuf);
+                else locate<T, kTemp>(a, due_id, due_b, l, wbuf);
             }
             due = DUE_NONE;
         }
@@ -1065,6 +1089,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             const ResDone r = residual_unit<T, kTemp>(a, unit, l, wbuf);
             due = DUE_RESIDUAL;
             due_id = r.slot;
+            due_b = r.b;
             due_old = r.old;
             continue;
         }
@@ -1103,7 +1128,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             if (__shfl_sync(kFull, due_old == need, kSig)) {
                 fence_acquire();
                 if (due == DUE_STREAM) finalize<T, kTemp>(a, due_id, l, wbuf);
-                else locate<T, kTemp>(a, due_id, l, wbuf);
+                else locate<T, kTemp>(a, due_id, due_b, l, wbuf);
             }
         }
         due = DUE_STREAM;
