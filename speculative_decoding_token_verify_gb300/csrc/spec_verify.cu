@@ -16,7 +16,7 @@
 //  * residual units (published sequence, a run of 256-element slices),
 //    taken once the stream queue is empty: they sum max(0, p - q) (or p for
 //    the bonus draw) per slice of the stop rows. The warp that completes the
-//    last residual unit of b locates the token by an fp64 inverse-CDF scan of
+//    last residual unit of b locates the token by an inverse-CDF scan of
 //    the slice sums and one slice.
 //
 // A warp waits only when the stream queue is empty and residual work is still
@@ -225,21 +225,6 @@ __device__ __forceinline__ const T *drow_ptr(const Args &a, int b, int i) {
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
-
-__device__ __forceinline__ double warp_incl_scan_d(double v, int l) {
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(kFull, v, o);
-        if (l >= o) v += t;
-    }
     return v;
 }
 
@@ -621,7 +606,7 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
 // ---------------------------------------------------------------------------
 
 // Each residual unit stores the fp32 sums of its slices; locate() scans all
-// slice sums of the sequence in fp64, then rescans one slice lane by lane.
+// slice sums of the sequence, then rescans one slice lane by lane.
 
 // Sum of slice s (elements 256s .. 256s+255) of the draw's weights, per lane
 // (8 elements each), in the fixed order every consumer of slice sums uses.
@@ -660,10 +645,29 @@ __device__ __forceinline__ float run_sum(const float4 *buf, int l, int cn) {
 }
 
 // Locate the token of sequence b's draw from its slice sums: Z is their total
-// (fp32 within a lane's run, fp64 across runs); the scan picks the slice whose
-// running sum first exceeds u*Z, then rescans that slice lane by lane with an
-// fp64 prefix across lanes. Returns the token, or -1 when Z is not positive
-// (only possible through rounding, or a bad row).
+// (a lane sums its run of slice sums in order, the runs are added across
+// lanes by a butterfly); the scan picks the slice whose running sum first
+// exceeds u*Z, then rescans that slice lane by lane with a prefix across
+// lanes. Returns the token, or -1 when Z is not positive (only possible
+// through rounding, or a bad row).
+//
+// All of it runs in fp32 (GB300's fp64 rate is a small fraction of fp32,
+// and this scan is on the launch's critical path). Error budget, relative
+// to Z: a slice sum (8 terms per lane, then a 32-lane butterfly) is off by
+// under 12 ulp of itself; a lane's run of at most 32 slice sums, summed in
+// order, by under 31 ulp of the run; a sum or a prefix across 32 lanes by
+// under 5 ulp of the total; u*Z and the differences by 1 ulp each. That is
+// under 60 * 2^-24 = 3.6e-6 in all, within the 1e-5 margin inside which a
+// draw is flagged, so an unflagged token is the exact-arithmetic one.
+__device__ __forceinline__ float warp_incl_scan_f(float v, int l) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(kFull, v, o);
+        if (l >= o) v += t;
+    }
+    return v;
+}
+
 template <typename T, bool kTemp>
 __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l, float4 *buf,
                            bool prestaged = false) {
@@ -671,7 +675,7 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
     const int n = a.nslice;
     constexpr int kChunk = 32 * kScanPer;
     // pass 1: Z (the first chunk's copies may already be in flight)
-    double Z = 0.0;
+    float Z = 0.f;
     for (int c0 = 0; c0 < n; c0 += kChunk) {
         if (c0 == 0 && prestaged) {
             cp_async_wait_all();
@@ -679,33 +683,33 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
         } else {
             stage_slices(ss, n, c0, l, buf);
         }
-        Z += warp_sum_d((double)run_sum(buf, l, n - c0));
+        Z += warp_sum_f(run_sum(buf, l, n - c0));
         __syncwarp();
     }
-    if (!(Z > 0.0)) return -1;
-    const double target = (double)d.u * Z;
+    if (!(Z > 0.f)) return -1;
+    const float target = d.u * Z;
     // pass 2: the first slice whose running sum exceeds the target (a single
     // chunk is still staged)
-    double P = 0.0;   // running sum before the current chunk
+    float P = 0.f;    // running sum before the current chunk
     int entry = -1;
-    double P2 = 0.0;  // running sum before slice `entry`
+    float P2 = 0.f;   // running sum before slice `entry`
     for (int c0 = 0; c0 < n; c0 += kChunk) {
         if (n > kChunk) stage_slices(ss, n, c0, l, buf);
         const int cn = n - c0;
         const float segf = run_sum(buf, l, cn);
-        const double incl = warp_incl_scan_d((double)segf, l) + P;
-        const double excl = incl - (double)segf;
-        // walk the run in fp32, relative to its start
-        const float rel = (float)(target - excl);
+        const float incl = warp_incl_scan_f(segf, l) + P;
+        const float excl = incl - segf;
+        // walk the run, relative to its start
+        const float rel = target - excl;
         float c = 0.f;
         int found = -1;
-        double Pf = 0.0;
+        float Pf = 0.f;
         for (int j = 0; j < kScanPer; ++j) {
             const float prev = c;
             c += staged(buf, l * kScanPer + j, cn);
             if (c > rel) {
                 found = c0 + l * kScanPer + j;
-                Pf = excl + (double)prev;
+                Pf = excl + prev;
                 break;
             }
         }
@@ -733,12 +737,12 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
             if (lm >= 0) entry = c0 + lm;
         }
         if (entry < 0) return -1;
-        P2 = -2.0 * Z - 1.0;
+        P2 = -2.f * Z - 1.f;
     }
     float r[8];
     const float s = slice_lane_sum<T, kTemp>(a, tr, dr, entry, l, d, r);
-    const double in = warp_incl_scan_d((double)s, l);
-    const double ex = in - (double)s;
+    const float in = warp_incl_scan_f(s, l);
+    const float ex = in - s;
     const unsigned hit = __ballot_sync(kFull, P2 + in > target);
     int L;
     if (hit) {
@@ -748,7 +752,7 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
         L = nz ? 31 - __clz(nz) : 0;
     }
     int tok = -1, lastpos = -1;
-    const float rel = (float)(target - (P2 + ex));
+    const float rel = target - (P2 + ex);
     float cc = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
