@@ -92,7 +92,9 @@ def dist_setup(args):
     if world > 1 and args.impl == "ours":
         import torch.distributed as dist
 
-        backend = "nccl" if args.impl == "ours" else "gloo"
+        # NCCL on GPU ranks; SPEC_DIST_BACKEND=gloo runs the same host logic
+        # on CPU ranks (the tests do)
+        backend = os.environ.get("SPEC_DIST_BACKEND", "nccl")
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group(backend=backend)
         pg = dist
@@ -105,6 +107,12 @@ def barrier(pg, device=None):
             pg.barrier(device_ids=[device.index])
         else:
             pg.barrier()
+
+
+def replica_throughput(world: int, steps: int, B: int, K: int, max_ms: float) -> float:
+    """Whole-job verified positions/s of N replicas: every rank verifies its
+    own B x K positions per step, and the slowest rank's time counts."""
+    return world * steps * B * K / (max_ms / 1e3)
 
 
 def max_over_ranks(pg, v: float, device=None) -> float:
@@ -393,8 +401,7 @@ def run_ours(args, w, world, rank, local, pg):
         e2e = run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg)
     clk = clocks.stop()
 
-    n_pos = world * args.steps * w.B * w.K
-    value = n_pos / (total_ms / 1e3)
+    value = replica_throughput(world, args.steps, w.B, w.K, total_ms)
     kern_s = statistics.mean(verify_ms) / 1e3
     peak, peak_src = measured_hbm_peak()
     achieved = logit_bytes / kern_s / 1e9
@@ -707,7 +714,7 @@ def run_e2e(args, w, inp, zd, u, est0, out, ws, dev, stream, step, pg):
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(pg, a.elapsed_time(b), dev)
     world = pg.get_world_size() if pg is not None else 1
-    return {"value": world * steps * w.B * w.K / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": replica_throughput(world, steps, w.B, w.K, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
             "overlap": "step i+1's host-to-device copy overlaps step i's kernels and read-back"}
 
