@@ -1170,6 +1170,11 @@ struct Plan {
 #ifndef SV_MIN_TILE
 #define SV_MIN_TILE 4096
 #endif
+// stream units aimed at: stochastic mode (a draw chain follows the stream),
+// and the other modes (the stream ends the launch)
+#ifndef SV_TARGET_UNITS_DRAW
+#define SV_TARGET_UNITS_DRAW 4096
+#endif
 #ifndef SV_TARGET_UNITS
 #define SV_TARGET_UNITS 16384
 #endif
@@ -1192,21 +1197,25 @@ static void split_row(int V, long long want, int &nT, int &TS) {
 
 // A stream unit is one warp's share: a tile of at most SV_TILE_BYTES of
 // logits. Small batches split rows further, down to SV_MIN_TILE elements,
-// aiming at ~SV_TARGET_UNITS units (about 3.4 per resident warp of a GB300).
-// Every unit boundary costs a warp a few microseconds without loads in
-// flight (the partial's release, then the first loads of the next tile), so
-// fewer, larger units stream faster. The queue's end is kept short in two
-// ways: its last units are claimed only when a warp is free (see next_job),
-// and in stochastic mode its last sequences (the tail) stream in smaller
-// tiles, so that the last unit, and with it the chain of finalize, residual
-// pass and locate of the last sequences, ends sooner.
-static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
+// aiming at ~`target` units. Every unit boundary costs a warp a few
+// microseconds without loads in flight (the partial's release, then the
+// first loads of the next tile), so fewer, larger units stream faster.
+// Where the stream ends the launch (greedy, FLy, confidences) the target is
+// ~SV_TARGET_UNITS (about 3.4 per resident warp of a GB300), which keeps the
+// last units short. In stochastic mode it is ~SV_TARGET_UNITS_DRAW (about
+// one per warp): there the finalize merges fewer partials per row, and the
+// end of the queue is kept short by its tail (the last sequences stream in
+// smaller tiles, so that their draw chain of finalize, residual pass and
+// locate starts sooner). In every mode the last units are claimed only when
+// a warp is free (see next_job).
+static void plan_tiles(int B, int rows, int V, int esize, bool draw, Plan &p) {
     const int ts_max = SV_TILE_BYTES / esize;
     const long long rows_total = (long long)B * rows;
     long long cap = V / SV_MIN_TILE;
     if (cap < 1) cap = 1;
     long long n = (V + ts_max - 1) / ts_max;
-    long long want = (SV_TARGET_UNITS + rows_total - 1) / rows_total;
+    const long long target = draw ? SV_TARGET_UNITS_DRAW : SV_TARGET_UNITS;
+    long long want = (target + rows_total - 1) / rows_total;
     if (want > cap) want = cap;
     if (want > n) n = want;
     split_row(V, n, p.nT, p.TS);
@@ -1214,7 +1223,7 @@ static void plan_tiles(int B, int rows, int V, int esize, Plan &p) {
     p.nT2 = p.nT;
     p.TS2 = p.TS;
     const int ts2 = SV_TAIL_TILE_BYTES / esize;
-    if (SV_TAIL_BYTES > 0 && ts2 >= SV_MIN_TILE && ts2 < p.TS) {
+    if (draw && SV_TAIL_BYTES > 0 && ts2 >= SV_MIN_TILE && ts2 < p.TS) {
         const long long seq_bytes = (long long)rows * V * esize;
         long long nt = (SV_TAIL_BYTES + seq_bytes - 1) / seq_bytes;
         if (nt > B / 2) nt = B / 2;
@@ -1237,12 +1246,17 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // per call) [slot records 2B | tile partials | slices B*sstride | nucleus
 // thresholds B*(2K+1) | draft-token logits B*2K (sized B*2*(2K+1))]. The
 // partials hold one slot per stream unit of the largest plan among the row
-// counts the call may stream (`rows_a`, `rows_b`).
-static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, Plan &p) {
-    Plan q;
-    plan_tiles(B, rows_b, V, esize, q);
-    plan_tiles(B, rows_a, V, esize, p);
-    const unsigned long long cap = p.units > q.units ? p.units : q.units;
+// counts the call may stream (`rows_a`, `rows_b`), in either mode class.
+// The plan returned tiles `rows_a` rows for the mode class `draw`.
+static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, bool draw, Plan &p) {
+    unsigned long long cap = 0;
+    for (int r : {rows_a, rows_b})
+        for (bool d : {false, true}) {
+            Plan q;
+            plan_tiles(B, r, V, esize, d, q);
+            if (q.units > cap) cap = q.units;
+        }
+    plan_tiles(B, rows_a, V, esize, draw, p);
     p.seq_off = kHeaderWords * sizeof(unsigned);
     p.ready_off = p.seq_off + (size_t)B * sizeof(unsigned);
     p.done_off = p.ready_off + (size_t)B * sizeof(unsigned);
@@ -1326,12 +1340,17 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     // draft-token logits are gathered wherever the finalize forms log-ratios
     a.gx = (a.mode != MODE_CONF && a.nd_rows > 0) ? reinterpret_cast<float *>(base + p.gx_off) : nullptr;
     if (a.mode != MODE_STOCHASTIC && !a.pre) {
-        // short tail units pay off only where a draw (finalize, residual
-        // pass, locate) follows the last unit of the queue
-        p.B1 = a.B;
-        p.nT2 = p.nT;
-        p.TS2 = p.TS;
-        p.head_units = p.units = (unsigned long long)a.B * (unsigned long long)a.rows * (unsigned long long)p.nT;
+        // no draw follows the stream: the tiling of that mode class (more,
+        // smaller units, no tail; the workspace has room for either)
+        Plan q;
+        plan_tiles(a.B, a.rows, a.V, dtype == SPEC_BF16 ? 2 : 4, false, q);
+        p.nT = q.nT;
+        p.TS = q.TS;
+        p.B1 = q.B1;
+        p.nT2 = q.nT2;
+        p.TS2 = q.TS2;
+        p.head_units = q.head_units;
+        p.units = q.units;
     }
     a.nT = p.nT;
     a.TS = p.TS;
@@ -1396,11 +1415,12 @@ static int check_common(int B, int K, int V, int dtype) {
     if (K < 1 || K > SPEC_MAX_K) return fail(SPEC_ERR_UNSUPPORTED, "K must be in [1, %d] (got %d)", SPEC_MAX_K, K);
     if (V < 2 || V > SPEC_MAX_V) return fail(SPEC_ERR_UNSUPPORTED, "V must be in [2, %d] (got %d)", SPEC_MAX_V, V);
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_UNSUPPORTED, "unknown dtype %d", dtype);
-    for (int rows : {K, K + 1, 2 * K + 1}) {
-        Plan pl;
-        plan_tiles(B, rows, V, dtype == SPEC_BF16 ? 2 : 4, pl);
-        if (pl.units >= (1ull << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large (B=%d)", B);
-    }
+    for (int rows : {K, K + 1, 2 * K + 1})
+        for (bool draw : {false, true}) {
+            Plan pl;
+            plan_tiles(B, rows, V, dtype == SPEC_BF16 ? 2 : 4, draw, pl);
+            if (pl.units >= (1ull << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large (B=%d)", B);
+        }
     return SPEC_OK;
 }
 
@@ -1443,14 +1463,14 @@ size_t spec_workspace_size(const spec_verify_params *p) {
     if (!p) return 0;
     if (check_common(p->B, p->K, p->V, p->dtype) != SPEC_OK) return 0;
     Plan pl;
-    plan_workspace(p->B, 2 * p->K + 1, p->K + 1, p->V, p->dtype == SPEC_BF16 ? 2 : 4, pl);
+    plan_workspace(p->B, 2 * p->K + 1, p->K + 1, p->V, p->dtype == SPEC_BF16 ? 2 : 4, true, pl);
     return pl.bytes;
 }
 
 size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype) {
     if (check_common(B, K, V, dtype) != SPEC_OK) return 0;
     Plan pl;
-    plan_workspace(B, K, K, V, dtype == SPEC_BF16 ? 2 : 4, pl);
+    plan_workspace(B, K, K, V, dtype == SPEC_BF16 ? 2 : 4, false, pl);
     return pl.bytes;
 }
 
@@ -1490,7 +1510,7 @@ static int verify_impl(const spec_verify_params *p, const void *target_logits, c
     // either row count, so spec_workspace_size covers both
     const int rows = draft_logits ? 2 * p->K + 1 : p->K + 1;
     Plan pl;
-    plan_workspace(p->B, rows, draft_logits ? p->K + 1 : 2 * p->K + 1, p->V, es, pl);
+    plan_workspace(p->B, rows, draft_logits ? p->K + 1 : 2 * p->K + 1, p->V, es, p->mode == SPEC_STOCHASTIC, pl);
     if (workspace_bytes < pl.bytes)
         return fail(SPEC_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, pl.bytes);
 
@@ -1592,7 +1612,7 @@ int spec_confidence(int32_t B, int32_t K, int32_t V, int32_t dtype, const void *
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16u) != 0)
         return fail(SPEC_ERR_INVALID_ARG, "workspace must be a 16-byte aligned device pointer");
     Plan pl;
-    plan_workspace(B, K, K, V, es, pl);
+    plan_workspace(B, K, K, V, es, false, pl);
     if (workspace_bytes < pl.bytes)
         return fail(SPEC_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, pl.bytes);
     Args a;
