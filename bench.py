@@ -59,6 +59,8 @@ def parse_args():
                          "on this workload, inverse temperatures log-uniform on [0.5, 2]")
     ap.add_argument("--irls", action="store_true",
                     help="also time the IRLS refit entry points (spec_irls_*) on this workload's B, K")
+    ap.add_argument("--confidence", action="store_true",
+                    help="also time the draft-only confidence pass (spec_confidence) on this workload's draft rows")
     ap.add_argument("--sweep", action="store_true",
                     help="time spec_verify alone at every point of the throughput sweep (B x K x V x dtype, "
                          "stochastic) and print one JSON line per point instead of the step line")
@@ -437,6 +439,8 @@ def run_ours(args, w, world, rank, local, pg):
     if args.top_p is not None:
         line["top_p"] = time_temperature(w, args.seed, out, est, ws, dev, stream, peak, logit_bytes,
                                          kern_s * 1e3, top_p=args.top_p)
+    if args.confidence and zd is not None:
+        line["confidence"] = time_confidence(w, zd, est, dev, stream, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
     if rank == 0:
@@ -591,6 +595,34 @@ def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, defa
         res["top_p"] = top_p
         res["kernel"] = "nucleus_kernel<T> + verify_kernel<T, 1> (precomputed rows)"
     return res
+
+
+def time_confidence(w, zd, est, dev, stream, peak, reps=100):
+    """Device time of spec_confidence (logit(q_max) features and
+    confidences from the draft rows alone: B*K*V elements read once), CUDA
+    events on the launching stream over back-to-back calls; the draft logits
+    are larger than L2."""
+    import statistics as st
+
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+
+    cws = sv.Workspace(dev)
+    for _ in range(5):
+        sv.confidence(zd, est, workspace=cws)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        sv.confidence(zd, est, workspace=cws)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    nbytes = zd.numel() * zd.element_size()
+    mean_ms = st.mean(ms)
+    return {"ms_mean": mean_ms, "ms_median": st.median(ms), "algorithmic_bytes": nbytes,
+            "frac": nbytes / (mean_ms / 1e3) / 1e9 / peak, "kernel": "verify_kernel<T, 0> (draft rows only)"}
 
 
 def run_sweep(args):

@@ -109,6 +109,26 @@ def test_workloads_full_size(wl):
     print(w.name, s)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_queue_tail_geometry_full_vocab(dt):
+    """64 sequences of the estimator workload at its full vocabulary. In
+    stochastic mode the queue's last ~80 MB of logits (the last 20 sequences
+    here) stream in smaller tiles than the rest: 64 KB tiles, 4 per row for
+    bf16 (8 for fp32), then 32 KB tiles. Every sequence, on both sides of that
+    boundary, must match the oracle, in a full launch and in a ragged
+    (pruned) launch of the same batch."""
+    w = workloads.ESTIMATOR.scaled(B=64, dtype=dt)
+    inp = workloads.make_inputs(w, 4064, DEV)
+    g = _run(inp, "stochastic", est=_est(w.K))
+    r = oracle_run(inp, oracle.STOCHASTIC, nthreads=16, est=np.r_[1.0, np.zeros(w.K)])
+    compare(g, r, w.dtype, check_feature=True, check_conf=True)
+    dl = np.random.default_rng(64).integers(0, w.K + 1, size=w.B).astype(np.int32)
+    g2 = _run(inp, "stochastic", draft_len=torch.tensor(dl, device=DEV))
+    r2 = oracle_run(inp, oracle.STOCHASTIC, nthreads=16, draft_len=dl)
+    compare(g2, r2, w.dtype)
+    assert sv.device_status(g2["_workspace"]) == 0
+
+
 @pytest.mark.parametrize("B,K,V,dt", [(1024, 8, 152064, "f32"), (512, 4, 32000, "bf16"),
                                       (32, 8, 128256, "f32")])
 def test_sweep_points_sampled(B, K, V, dt):
