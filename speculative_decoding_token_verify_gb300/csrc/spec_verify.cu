@@ -61,6 +61,16 @@ namespace sv {
 #ifndef SV_UNROLL
 #define SV_UNROLL 4
 #endif
+// stream through a two-chunk cp.async ring in the warp's staging buffer
+// (the next chunks' loads stay in flight while a chunk is folded):
+// 0 never, 1 always, 2 target rows, 3 in the modes with no draw (greedy,
+// FLy, confidences). Measured: 3 is best. With no draw the stream ends the
+// launch, and keeping loads in flight during the fold paid off (FLy B=128,
+// K=15: 0.1154 against 0.1224 ms). In stochastic mode the ring cost 2-7%
+// (1 or 2), so its rows keep the direct loads.
+#ifndef SV_STREAM_RING
+#define SV_STREAM_RING 3
+#endif
 // the last SV_LAZY_ROUNDS x (resident warps) stream units are claimed when
 // due instead of one unit ahead
 #ifndef SV_LAZY_ROUNDS
@@ -142,6 +152,7 @@ struct Args {
     unsigned per_seq2;       // rows * nT2
     unsigned head_units;     // B1 * per_seq
     unsigned lazy_from;      // stream units from here on are claimed when due, not one ahead
+    int ring;                // stream through the staging-buffer ring (modes with no draw)
     int t_vec_ok, d_vec_ok;  // rows start on 16-byte boundaries
     float inv_log_v;         // 1 / ln V
     unsigned *ctr;           // header words
@@ -295,8 +306,8 @@ __device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit) {
 // sL, rs: exponent scale and rescale margin (log2e and kRescale at s = 1);
 // kSub: difference-first exponents (the temperature variant).
 template <typename T, bool kEnt, bool kSub = false>
-__device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float sL = kLog2e,
-                                               float rs = kRescale) {
+__device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float4 *ring, bool use_ring,
+                                               float sL = kLog2e, float rs = kRescale) {
     RowAcc hs = acc_empty(), ts = acc_empty();
     if (l < g.head) {
         float z[1] = {Elem<T>::load(g.row + g.v0 + l)};
@@ -310,6 +321,48 @@ __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float
     const int nvec = (int)(g.bytes / 16u);
     StreamAcc s = stream_init(sL, rs);
     int k = l;
+#if SV_STREAM_RING
+    // Where the ring is used (SV_STREAM_RING), chunks of kUnroll vectors per
+    // lane go through two chunk slots in the warp's staging buffer (slot
+    // c & 1, entry q*32 + l): while chunk c is folded from registers, chunks
+    // c+1 and c+2 are in flight, with no registers held. Each lane reads back
+    // only what it copied, so no barrier is needed; the ring is empty again
+    // when the loop ends. Otherwise (and for the last partial chunk) lanes
+    // load directly, kUnroll vectors in flight.
+    static_assert(2 * kUnroll * 32 <= kStage, "two ring slots fit the staging buffer");
+    const int nfull = (nvec - l + kUnroll * 32 - 1 - (kUnroll - 1) * 32) / (kUnroll * 32);   // full chunks of this lane
+    if ((SV_STREAM_RING == 1 || (SV_STREAM_RING == 2 && kEnt) || (SV_STREAM_RING == 3 && use_ring)) && nfull > 0) {
+#pragma unroll
+        for (int q = 0; q < kUnroll; ++q) cp_async16(ring + q * 32 + l, vp + k + q * 32);
+        cp_async_commit();
+        if (nfull > 1) {
+#pragma unroll
+            for (int q = 0; q < kUnroll; ++q) cp_async16(ring + kUnroll * 32 + q * 32 + l, vp + k + kUnroll * 32 + q * 32);
+        }
+        cp_async_commit();
+        for (int c = 0; c < nfull; ++c, k += kUnroll * 32) {
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            float4 *slot = ring + (c & 1) * (kUnroll * 32);
+            uint4 w[kUnroll];
+#pragma unroll
+            for (int q = 0; q < kUnroll; ++q) {
+                const float4 f = slot[q * 32 + l];
+                w[q] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+            }
+            if (c + 2 < nfull) {
+#pragma unroll
+                for (int q = 0; q < kUnroll; ++q) cp_async16(slot + q * 32 + l, vp + k + 2 * kUnroll * 32 + q * 32);
+            }
+            cp_async_commit();
+#pragma unroll
+            for (int q = 0; q < kUnroll; ++q) {
+                stream_chunk<T, kEnt, kSub>(s, w[q], k + q * 32, sL, rs);
+                if (s.bk == k + q * 32) s.bw = w[q];
+            }
+        }
+        cp_async_wait();
+    }
+#endif
     for (; k + (kUnroll - 1) * 32 < nvec; k += kUnroll * 32) {
         uint4 w[kUnroll];
 #pragma unroll
@@ -1114,10 +1167,11 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             const float sc = seq_inv_temp(a, g.b);
             const float sL = sc * kLog2e, rs = __fdiv_rn(kRescale, sc);   // exact for powers of two
             s = skip ? acc_empty()
-                     : (g.target ? unit_consume<T, true, true>(g, l, sL, rs) : unit_consume<T, false, true>(g, l, sL, rs));
+                     : (g.target ? unit_consume<T, true, true>(g, l, wbuf, a.ring, sL, rs)
+                                 : unit_consume<T, false, true>(g, l, wbuf, a.ring, sL, rs));
           }
         } else {
-            s = skip ? acc_empty() : (g.target ? unit_consume<T, true>(g, l) : unit_consume<T, false>(g, l));
+            s = skip ? acc_empty() : (g.target ? unit_consume<T, true>(g, l, wbuf, a.ring) : unit_consume<T, false>(g, l, wbuf, a.ring));
         }
         const int b = g.b;
         unsigned old = 0u;
@@ -1352,6 +1406,7 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
         p.head_units = q.head_units;
         p.units = q.units;
     }
+    a.ring = a.mode != MODE_STOCHASTIC ? 1 : 0;
     a.nT = p.nT;
     a.TS = p.TS;
     a.per_seq = (unsigned)a.rows * (unsigned)p.nT;
