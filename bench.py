@@ -417,8 +417,8 @@ def run_ours(args, w, world, rank, local, pg):
         "hbm_gbs": logit_bytes * world * args.steps / (total_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
-                     "kernel": ("verify_kernel<__nv_bfloat16, 0>" if w.dtype == "bf16"
-                                else "verify_kernel<float, 0>"),
+                     "kernel": ("verify_kernel<__nv_bfloat16, 0, 0>" if w.dtype == "bf16"
+                                else "verify_kernel<float, 0, 0>"),
                      "algorithmic_bytes_per_launch": logit_bytes,
                      "kernel_ms_mean": kern_s * 1e3, "kernel_ms_median": statistics.median(verify_ms),
                      "peak_source": peak_src, "frac_note": "of measured" if "measured" in peak_src
@@ -622,7 +622,7 @@ def time_confidence(w, zd, est, dev, stream, peak, reps=100):
     nbytes = zd.numel() * zd.element_size()
     mean_ms = st.mean(ms)
     return {"ms_mean": mean_ms, "ms_median": st.median(ms), "algorithmic_bytes": nbytes,
-            "frac": nbytes / (mean_ms / 1e3) / 1e9 / peak, "kernel": "verify_kernel<T, 0> (draft rows only)"}
+            "frac": nbytes / (mean_ms / 1e3) / 1e9 / peak, "kernel": "verify_kernel<T, 0, 1> (draft rows only, staging-buffer ring)"}
 
 
 def run_sweep(args):

@@ -61,15 +61,14 @@ namespace sv {
 #ifndef SV_UNROLL
 #define SV_UNROLL 4
 #endif
-// stream through a two-chunk cp.async ring in the warp's staging buffer
-// (the next chunks' loads stay in flight while a chunk is folded):
-// 0 never, 1 always, 2 target rows, 3 in the modes with no draw (greedy,
-// FLy, confidences). Measured: 3 is best. With no draw the stream ends the
-// launch, and keeping loads in flight during the fold paid off (FLy B=128,
-// K=15: 0.1154 against 0.1224 ms). In stochastic mode the ring cost 2-7%
-// (1 or 2), so its rows keep the direct loads.
+// launches with no draw (greedy, FLy, confidences; temperature 1) stream
+// through a two-chunk cp.async ring in the warp's staging buffer, so that
+// the next chunks' loads stay in flight while a chunk is folded (FLy B=128,
+// K=15: 0.1154 against 0.1224 ms). The ring cost stochastic launches 2-7%,
+// whether on all rows or on target rows only, so they keep direct loads and
+// a kernel without the ring's code. 0 turns the ring off.
 #ifndef SV_STREAM_RING
-#define SV_STREAM_RING 3
+#define SV_STREAM_RING 1
 #endif
 // the last SV_LAZY_ROUNDS x (resident warps) stream units are claimed when
 // due instead of one unit ahead
@@ -152,7 +151,6 @@ struct Args {
     unsigned per_seq2;       // rows * nT2
     unsigned head_units;     // B1 * per_seq
     unsigned lazy_from;      // stream units from here on are claimed when due, not one ahead
-    int ring;                // stream through the staging-buffer ring (modes with no draw)
     int t_vec_ok, d_vec_ok;  // rows start on 16-byte boundaries
     float inv_log_v;         // 1 / ln V
     unsigned *ctr;           // header words
@@ -305,9 +303,9 @@ __device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit) {
 // Fold one unit. Returns the warp-merged accumulator (identical in every lane).
 // sL, rs: exponent scale and rescale margin (log2e and kRescale at s = 1);
 // kSub: difference-first exponents (the temperature variant).
-template <typename T, bool kEnt, bool kSub = false>
-__device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float4 *ring, bool use_ring,
-                                               float sL = kLog2e, float rs = kRescale) {
+template <typename T, bool kEnt, bool kSub = false, bool kRing = false>
+__device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float4 *ring, float sL = kLog2e,
+                                               float rs = kRescale) {
     RowAcc hs = acc_empty(), ts = acc_empty();
     if (l < g.head) {
         float z[1] = {Elem<T>::load(g.row + g.v0 + l)};
@@ -321,48 +319,48 @@ __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float
     const int nvec = (int)(g.bytes / 16u);
     StreamAcc s = stream_init(sL, rs);
     int k = l;
-#if SV_STREAM_RING
-    // Where the ring is used (SV_STREAM_RING), chunks of kUnroll vectors per
-    // lane go through two chunk slots in the warp's staging buffer (slot
-    // c & 1, entry q*32 + l): while chunk c is folded from registers, chunks
-    // c+1 and c+2 are in flight, with no registers held. Each lane reads back
-    // only what it copied, so no barrier is needed; the ring is empty again
-    // when the loop ends. Otherwise (and for the last partial chunk) lanes
-    // load directly, kUnroll vectors in flight.
-    static_assert(2 * kUnroll * 32 <= kStage, "two ring slots fit the staging buffer");
-    const int nfull = (nvec - l + kUnroll * 32 - 1 - (kUnroll - 1) * 32) / (kUnroll * 32);   // full chunks of this lane
-    if ((SV_STREAM_RING == 1 || (SV_STREAM_RING == 2 && kEnt) || (SV_STREAM_RING == 3 && use_ring)) && nfull > 0) {
-#pragma unroll
-        for (int q = 0; q < kUnroll; ++q) cp_async16(ring + q * 32 + l, vp + k + q * 32);
-        cp_async_commit();
-        if (nfull > 1) {
-#pragma unroll
-            for (int q = 0; q < kUnroll; ++q) cp_async16(ring + kUnroll * 32 + q * 32 + l, vp + k + kUnroll * 32 + q * 32);
-        }
-        cp_async_commit();
-        for (int c = 0; c < nfull; ++c, k += kUnroll * 32) {
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-            float4 *slot = ring + (c & 1) * (kUnroll * 32);
-            uint4 w[kUnroll];
-#pragma unroll
-            for (int q = 0; q < kUnroll; ++q) {
-                const float4 f = slot[q * 32 + l];
-                w[q] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
-            }
-            if (c + 2 < nfull) {
-#pragma unroll
-                for (int q = 0; q < kUnroll; ++q) cp_async16(slot + q * 32 + l, vp + k + 2 * kUnroll * 32 + q * 32);
+    if constexpr (kRing) {
+        // Where the ring is used (kRing), chunks of kUnroll vectors per
+        // lane go through two chunk slots in the warp's staging buffer (slot
+        // c & 1, entry q*32 + l): while chunk c is folded from registers, chunks
+        // c+1 and c+2 are in flight, with no registers held. Each lane reads back
+        // only what it copied, so no barrier is needed; the ring is empty again
+        // when the loop ends. Otherwise (and for the last partial chunk) lanes
+        // load directly, kUnroll vectors in flight.
+        static_assert(2 * kUnroll * 32 <= kStage, "two ring slots fit the staging buffer");
+        const int nfull = (nvec - l + kUnroll * 32 - 1 - (kUnroll - 1) * 32) / (kUnroll * 32);   // full chunks of this lane
+        if (nfull > 0) {
+    #pragma unroll
+            for (int q = 0; q < kUnroll; ++q) cp_async16(ring + q * 32 + l, vp + k + q * 32);
+            cp_async_commit();
+            if (nfull > 1) {
+    #pragma unroll
+                for (int q = 0; q < kUnroll; ++q) cp_async16(ring + kUnroll * 32 + q * 32 + l, vp + k + kUnroll * 32 + q * 32);
             }
             cp_async_commit();
-#pragma unroll
-            for (int q = 0; q < kUnroll; ++q) {
-                stream_chunk<T, kEnt, kSub>(s, w[q], k + q * 32, sL, rs);
-                if (s.bk == k + q * 32) s.bw = w[q];
+            for (int c = 0; c < nfull; ++c, k += kUnroll * 32) {
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+                float4 *slot = ring + (c & 1) * (kUnroll * 32);
+                uint4 w[kUnroll];
+    #pragma unroll
+                for (int q = 0; q < kUnroll; ++q) {
+                    const float4 f = slot[q * 32 + l];
+                    w[q] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+                }
+                if (c + 2 < nfull) {
+    #pragma unroll
+                    for (int q = 0; q < kUnroll; ++q) cp_async16(slot + q * 32 + l, vp + k + 2 * kUnroll * 32 + q * 32);
+                }
+                cp_async_commit();
+    #pragma unroll
+                for (int q = 0; q < kUnroll; ++q) {
+                    stream_chunk<T, kEnt, kSub>(s, w[q], k + q * 32, sL, rs);
+                    if (s.bk == k + q * 32) s.bw = w[q];
+                }
             }
+            cp_async_wait();
         }
-        cp_async_wait();
     }
-#endif
     for (; k + (kUnroll - 1) * 32 < nvec; k += kUnroll * 32) {
         uint4 w[kUnroll];
 #pragma unroll
@@ -1102,7 +1100,7 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
 // ---------------------------------------------------------------------------
 enum { DUE_NONE = 0, DUE_STREAM = 1, DUE_RESIDUAL = 2 };
 
-template <typename T, bool kTemp>
+template <typename T, bool kTemp, bool kRing = false>
 __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a) {
     const int l = threadIdx.x & 31;
     __shared__ float4 s_stage[NWARP][kStage];   // per-warp staging for finalize and locate
@@ -1167,11 +1165,11 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             const float sc = seq_inv_temp(a, g.b);
             const float sL = sc * kLog2e, rs = __fdiv_rn(kRescale, sc);   // exact for powers of two
             s = skip ? acc_empty()
-                     : (g.target ? unit_consume<T, true, true>(g, l, wbuf, a.ring, sL, rs)
-                                 : unit_consume<T, false, true>(g, l, wbuf, a.ring, sL, rs));
+                     : (g.target ? unit_consume<T, true, true>(g, l, wbuf, sL, rs) : unit_consume<T, false, true>(g, l, wbuf, sL, rs));
           }
         } else {
-            s = skip ? acc_empty() : (g.target ? unit_consume<T, true>(g, l, wbuf, a.ring) : unit_consume<T, false>(g, l, wbuf, a.ring));
+            s = skip ? acc_empty()
+                     : (g.target ? unit_consume<T, true, false, kRing>(g, l, wbuf) : unit_consume<T, false, false, kRing>(g, l, wbuf));
         }
         const int b = g.b;
         unsigned old = 0u;
@@ -1324,9 +1322,10 @@ static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, bool
     p.bytes = align_up(p.gx_off + (size_t)B * 2 * rmax * sizeof(float), 16);
 }
 
+// kernel variants: 0 the default, 1 temperature, 2 the staging-buffer ring
 struct DevInfo {
     int sms = 0;
-    int occ[2][2] = {{0, 0}, {0, 0}};   // [dtype][temperature variant]
+    int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};   // [dtype][variant]
 };
 
 static std::mutex g_dev_mu;
@@ -1334,16 +1333,16 @@ static DevInfo g_dev[64];
 
 constexpr size_t kDynSmem = 0;
 
-template <typename T, bool kTemp>
+template <typename T, bool kTemp, bool kRing>
 static int occupancy() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<T, kTemp>, NT, kDynSmem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<T, kTemp, kRing>, NT, kDynSmem) != cudaSuccess)
         n = 0;
     return n;
 }
 
 // Grid = resident CTAs (SMs x occupancy), at most one warp per unit.
-static int grid_for(int dtype, bool temp, unsigned long long units, int *grid) {
+static int grid_for(int dtype, int variant, unsigned long long units, int *grid) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice failed");
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -1352,17 +1351,20 @@ static int grid_for(int dtype, bool temp, unsigned long long units, int *grid) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return fail(SPEC_ERR_CUDA, "cannot query the SM count");
-        d.occ[0][0] = occupancy<float, false>();
-        d.occ[1][0] = occupancy<__nv_bfloat16, false>();
-        d.occ[0][1] = occupancy<float, true>();
-        d.occ[1][1] = occupancy<__nv_bfloat16, true>();
-        for (int i = 0; i < 4; ++i)
-            if (d.occ[i >> 1][i & 1] < 1)
-                return fail(SPEC_ERR_CUDA, "the verify kernel cannot be resident (shared memory %zu bytes)",
-                            kDynSmem);
+        d.occ[0][0] = occupancy<float, false, false>();
+        d.occ[1][0] = occupancy<__nv_bfloat16, false, false>();
+        d.occ[0][1] = occupancy<float, true, false>();
+        d.occ[1][1] = occupancy<__nv_bfloat16, true, false>();
+        d.occ[0][2] = occupancy<float, false, true>();
+        d.occ[1][2] = occupancy<__nv_bfloat16, false, true>();
+        for (int i = 0; i < 2; ++i)
+            for (int v = 0; v < 3; ++v)
+                if (d.occ[i][v] < 1)
+                    return fail(SPEC_ERR_CUDA, "the verify kernel cannot be resident (shared memory %zu bytes)",
+                                kDynSmem);
         d.sms = sms;
     }
-    unsigned long long g = (unsigned long long)d.sms * (unsigned long long)d.occ[dtype][temp ? 1 : 0];
+    unsigned long long g = (unsigned long long)d.sms * (unsigned long long)d.occ[dtype][variant];
     const unsigned long long need = (units + NWARP - 1) / NWARP;
     if (g > need) g = need;
     *grid = (int)(g < 1 ? 1 : g);
@@ -1406,7 +1408,6 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
         p.head_units = q.head_units;
         p.units = q.units;
     }
-    a.ring = a.mode != MODE_STOCHASTIC ? 1 : 0;
     a.nT = p.nT;
     a.TS = p.TS;
     a.per_seq = (unsigned)a.rows * (unsigned)p.nT;
@@ -1423,7 +1424,10 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     a.inv_log_v = (float)(1.0 / std::log((double)a.V));
     int grid = 1;
     const bool temp = a.inv_temp != nullptr || a.pre;
-    int rc = grid_for(dtype, temp, p.units, &grid);
+    // the staging-buffer ring streams the launches with no draw
+    const bool ring = SV_STREAM_RING && !temp && a.mode != MODE_STOCHASTIC;
+    const int variant = temp ? 1 : (ring ? 2 : 0);
+    int rc = grid_for(dtype, variant, p.units, &grid);
     if (rc != SPEC_OK) return rc;
     const unsigned long long lazy = (unsigned long long)SV_LAZY_ROUNDS * (unsigned long long)grid * NWARP;
     a.lazy_from = p.units > lazy ? (unsigned)(p.units - lazy) : 0u;
@@ -1452,14 +1456,21 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
         e = launch_nucleus(n, st);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "nucleus launch failed: %s", cudaGetErrorString(e));
     }
-    if (dtype == SPEC_BF16 && temp)
-        verify_kernel<__nv_bfloat16, true><<<grid, NT, kDynSmem, st>>>(a);
-    else if (dtype == SPEC_BF16)
-        verify_kernel<__nv_bfloat16, false><<<grid, NT, kDynSmem, st>>>(a);
-    else if (temp)
-        verify_kernel<float, true><<<grid, NT, kDynSmem, st>>>(a);
-    else
-        verify_kernel<float, false><<<grid, NT, kDynSmem, st>>>(a);
+    if (dtype == SPEC_BF16) {
+        if (temp)
+            verify_kernel<__nv_bfloat16, true><<<grid, NT, kDynSmem, st>>>(a);
+        else if (ring)
+            verify_kernel<__nv_bfloat16, false, true><<<grid, NT, kDynSmem, st>>>(a);
+        else
+            verify_kernel<__nv_bfloat16, false><<<grid, NT, kDynSmem, st>>>(a);
+    } else {
+        if (temp)
+            verify_kernel<float, true><<<grid, NT, kDynSmem, st>>>(a);
+        else if (ring)
+            verify_kernel<float, false, true><<<grid, NT, kDynSmem, st>>>(a);
+        else
+            verify_kernel<float, false><<<grid, NT, kDynSmem, st>>>(a);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return SPEC_OK;
