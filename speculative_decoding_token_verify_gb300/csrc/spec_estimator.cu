@@ -105,6 +105,94 @@ __global__ void __launch_bounds__(NT) estimator_kernel(int B, int K, const float
     }
 }
 
+// K <= kSmallK: every thread loads the K features of its sequences once and
+// keeps the per-position partial sums in registers; one pass of reductions
+// follows (a fixed shuffle tree per position, then the warps in order). The
+// sums run in a fixed order, so the result is bit-reproducible; the general
+// kernel above walks the positions one round at a time instead.
+constexpr int kSmallK = 16;
+
+__global__ void __launch_bounds__(NT) estimator_kernel_small(int B, int K, const float *__restrict__ feature,
+                                                             const int32_t *__restrict__ acc_len,
+                                                             const int32_t *__restrict__ draft_len,
+                                                             float *__restrict__ params, float lr,
+                                                             float *__restrict__ grad_out,
+                                                             int32_t *__restrict__ count_out) {
+    __shared__ float g_w[NWARP][kSmallK + 1];
+    __shared__ int c_w[NWARP][kSmallK + 1];
+    __shared__ int n_sh;
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const float omega = params[0];
+    float gi[kSmallK], beta[kSmallK];
+    int ni[kSmallK];
+    float gw = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSmallK; ++i) {
+        gi[i] = 0.f;
+        ni[i] = 0;
+        beta[i] = i < K ? params[1 + i] : 0.f;
+    }
+    for (int b = tid; b < B; b += NT) {
+        // every load of the sequence goes out before any of them is used
+        float fv[kSmallK];
+#pragma unroll
+        for (int i = 0; i < kSmallK; ++i) fv[i] = i < K ? feature[(size_t)b * K + i] : 0.f;
+        const int n = acc_len[b];
+        const int kb = draft_len ? min(max(draft_len[b], 0), K) : K;
+#pragma unroll
+        for (int i = 0; i < kSmallK; ++i) {
+            if (i >= K || i > n || i >= kb) continue;   // not labelled (or never verified)
+            const float y = i < n ? 1.f : 0.f;
+            const float f = fv[i];
+            const float e = 1.f / (1.f + expf(-(omega * f + beta[i]))) - y;
+            gi[i] += e;
+            ++ni[i];
+            gw = fmaf(e, f, gw);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kSmallK; ++i) {
+        if (i < K) {
+            const float g = warp_sum(gi[i]);
+            const int c = warp_sum_i(ni[i]);
+            if (l == 0) {
+                g_w[w][1 + i] = g;
+                c_w[w][1 + i] = c;
+            }
+        }
+    }
+    gw = warp_sum(gw);
+    if (l == 0) g_w[w][0] = gw;
+    __syncthreads();
+    // position k's totals over the warps in order (k = 0: the slope)
+    float g = 0.f;
+    int c = 0;
+    if (tid <= K) {
+        for (int q = 0; q < NWARP; ++q) {
+            g += g_w[q][tid];
+            if (tid > 0) c += c_w[q][tid];
+        }
+    }
+    if (tid == 0) {
+        int N = 0;
+        for (int i = 1; i <= K; ++i) {
+            int ci = 0;
+            for (int q = 0; q < NWARP; ++q) ci += c_w[q][i];
+            N += ci;
+        }
+        n_sh = N;
+        c = N;
+    }
+    __syncthreads();
+    const int N = n_sh;
+    if (tid <= K) {
+        const float gm = N > 0 ? g / (float)N : 0.f;
+        if (grad_out) grad_out[tid] = gm;
+        if (count_out) count_out[tid] = c;
+        if (N > 0) params[tid] = params[tid] - lr * gm;
+    }
+}
+
 }  // namespace sv_est
 
 // defined in spec_verify.cu: sets the thread-local message read by spec_last_error
@@ -119,8 +207,12 @@ static int estimator_impl(int32_t B, int32_t K, const float *feature, const int3
     if (B > 0 && (!feature || !accepted_len))
         return spec_internal_set_error(SPEC_ERR_INVALID_ARG, "feature / accepted_len is NULL");
     spec_internal_set_error(SPEC_OK, "");
-    sv_est::estimator_kernel<<<1, sv_est::NT, 0, static_cast<cudaStream_t>(stream)>>>(
-        B, K, feature, accepted_len, draft_len, est_params, lr, grad_out, count_out);
+    if (K <= sv_est::kSmallK)
+        sv_est::estimator_kernel_small<<<1, sv_est::NT, 0, static_cast<cudaStream_t>(stream)>>>(
+            B, K, feature, accepted_len, draft_len, est_params, lr, grad_out, count_out);
+    else
+        sv_est::estimator_kernel<<<1, sv_est::NT, 0, static_cast<cudaStream_t>(stream)>>>(
+            B, K, feature, accepted_len, draft_len, est_params, lr, grad_out, count_out);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return spec_internal_set_error(SPEC_ERR_CUDA, cudaGetErrorString(e));
     return SPEC_OK;

@@ -341,7 +341,7 @@ def test_gpu_lossless_chi_square():
 # Estimator and confidence entry points
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("B,K", [(256, 8), (1, 1), (1000, 15), (0, 4)])
+@pytest.mark.parametrize("B,K", [(256, 8), (1, 1), (1000, 15), (0, 4), (64, 16), (300, 24)])
 def test_estimator_update_parity(B, K):
     rng = np.random.default_rng(B * 31 + K)
     f = rng.normal(-3.0, 1.5, (B, K)).astype(np.float32)
