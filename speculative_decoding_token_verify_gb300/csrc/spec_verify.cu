@@ -6,18 +6,25 @@
 // block-wide barrier) that pulls work from two queues:
 //
 //  * stream units (sequence b, row r, vocabulary tile t), ordered
-//    sequence-major and claimed with one atomic each. A unit streams its tile
-//    from HBM exactly once with 128-bit non-allocating loads and folds it into
-//    an online softmax accumulator (max, complement mass, entropy moment,
-//    argmax); the partial goes to the workspace. The warp that completes the
-//    last unit of b (per-sequence counter) finalises b: it merges the row
-//    partials, applies the mode's rule, writes the per-position outputs and,
-//    in stochastic mode, publishes b's draw.
+//    sequence-major and claimed with one atomic each (one unit ahead, except
+//    at the end of the queue, where a unit is claimed only when a warp is
+//    free to start it). A unit streams its tile from HBM exactly once with
+//    128-bit loads (direct, or through a cp.async ring in the warp's staging
+//    buffer in the modes with no draw) and folds it into an online softmax
+//    accumulator (max, complement mass, entropy moment, argmax); the partial
+//    goes to the workspace. A sequence's first unit also gathers the logits
+//    at its draft tokens. The warp that completes the last unit of b
+//    (per-sequence counter) finalises b: it merges the row partials, applies
+//    the mode's rule, publishes b's draw (stochastic mode) and writes the
+//    per-position outputs. In stochastic mode the queue's last sequences
+//    stream in smaller tiles, so that the draw chain ending the launch
+//    starts sooner.
 //  * residual units (published sequence, a run of 256-element slices),
-//    taken once the stream queue is empty: they sum max(0, p - q) (or p for
-//    the bonus draw) per slice of the stop rows. The warp that completes the
-//    last residual unit of b locates the token by an inverse-CDF scan of
-//    the slice sums and one slice.
+//    taken once the stream queue is empty and claimed one ahead: each sums
+//    max(0, p - q) (or p for the bonus draw) per slice of the stop rows in
+//    one memory round trip. The warp that completes the last residual unit
+//    of b locates the token by an inverse-CDF scan of the slice sums and one
+//    slice.
 //
 // A warp waits only when the stream queue is empty and residual work is still
 // to be published; every unit in flight completes without waiting, so the
@@ -1027,16 +1034,16 @@ __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l,
 }
 
 // ---------------------------------------------------------------------------
-// Scheduling, per warp (lane 0 keeps the state). Nothing on the stream path
-// waits for a reply:
+// Scheduling, per warp (lane 0 keeps the state):
 //
 //  * Stream units come in sequence-major order, one atomicAdd each, claimed
-//    one unit ahead.
+//    one unit ahead, so that the claim's reply is never waited for; the last
+//    units of the queue are claimed when due instead (see next_job).
 //  * Residual units are taken once the stream queue is empty: claimed with
-//    atomicAdd in publication order and run when their sequence's draw is
-//    published, polled with a short backoff (bounded; SPEC_ERR_TIMEOUT). Run
-//    together at the end, they stream the stop rows at full bandwidth; mixed
-//    into the stream phase they cost more than they save.
+//    atomicAdd in slot order, one ahead, and run when their sequence's draw
+//    is published, polled with a short backoff (bounded; SPEC_ERR_TIMEOUT).
+//    Run together at the end, next to the stream's last units; mixed into
+//    the stream phase they cost more than they save.
 //
 // A warp waits only when it holds no stream unit and has resolved every
 // completion it owes; each publication depends only on stream units held by
