@@ -7,9 +7,17 @@
 // The nucleus of a row is every token whose logit is at least z*, the largest
 // logit value whose upper mass (the tokens with logit >= z*) reaches top_p of
 // the row's mass under p = softmax(s z); tokens tied at z* are all kept.
-// One CTA takes one row at a time (persistent over rows) and finds z* by a
-// mass-weighted radix select, re-reading the row (L2-resident between its
-// passes: two CTAs per SM keep under 100 MB of rows in flight):
+//
+// Two kernels find z* by the same mass-weighted radix select:
+//  * nucleus_cluster_kernel (used when rows are 16-byte aligned and a
+//    cluster of at most 8 CTAs holds one in 32 or 64 KB slices): the row is
+//    read from HBM once into the cluster's distributed shared memory, and
+//    every pass below reads shared memory; see the comment above it.
+//  * nucleus_kernel (every other row): one CTA takes one row at a time
+//    (persistent over rows), re-reading the row between passes (L2-resident:
+//    two CTAs per SM keep under 100 MB of rows in flight).
+//
+// The passes of one row:
 //
 //  A. max M, its lowest index I, and the smallest finite logit;
 //  B. weights e_v = 2^((z_v - M) s log2e), in 2^-40 fixed point, summed for
