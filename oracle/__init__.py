@@ -51,7 +51,13 @@ def _load():
     if _lib is not None:
         return _lib
     build()
-    lib = ctypes.CDLL(_LIB)
+    _lib = bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def bind(lib):
+    """Declare the argument and result types of every oracle entry point on a
+    loaded copy of the library (the one built here, or a test's variant)."""
     P = ctypes.c_void_p
     i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
     lib.oracle_verify.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.c_int, P, i64, P, i64,
@@ -73,7 +79,6 @@ def _load():
     lib.oracle_estimator_loss.restype = dbl
     lib.oracle_row_stats.argtypes = [i64, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
     lib.oracle_row_stats.restype = ctypes.c_int
-    _lib = lib
     return lib
 
 

@@ -76,6 +76,18 @@ def test_av_budget_ties_zeros_and_bad_costs():
     assert r["budget"] == 0 and int(g["budget"].item()) == 0
 
 
+def test_av_budget_cuts_through_a_cross_sequence_tie():
+    """Budgets that end inside a group of equal survival values spread over
+    sequences: ties rank by ascending flat index on both sides."""
+    sv = _sv()
+    g, _ = _budget_case(sv, np.array([[0.5], [0.5]], np.float32), np.zeros(3, np.float32),
+                        np.array([1, 1, 2], np.float32))
+    assert g["draft_len"].cpu().tolist() == [1, 0]
+    g, _ = _budget_case(sv, np.full((3, 2), 0.5, np.float32), np.zeros(7, np.float32),
+                        np.array([1, 1, 1, 1, 1, 4, 4], np.float32))
+    assert g["draft_len"].cpu().tolist() == [2, 1, 1]
+
+
 @pytest.mark.parametrize("mode", ["stochastic", "greedy", "fly"])
 def test_ragged_verify_matches_oracle(mode):
     sv = _sv()

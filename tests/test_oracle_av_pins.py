@@ -74,6 +74,23 @@ def test_ties_keep_prefixes_and_bad_costs_are_ineligible():
     assert r3["budget"] == 0 and list(r3["draft_len"]) == [0, 0]
 
 
+def test_cross_sequence_ties_rank_by_index():
+    # Equal survival in different sequences, with a budget that cuts through
+    # the tie: the reading ranks ties by ascending flat index b*K + i, so the
+    # lower sequence gets the draft. Objectives (B + S_k) / cost_k with
+    # survival .5 everywhere: K = 1, costs 1, 1, 2 give 2, 2.5, 1.5.
+    conf = np.array([[0.5], [0.5]], np.float32)
+    r = oracle.av_budget(conf, np.zeros(3, np.float32), np.array([1, 1, 2], np.float32))
+    assert r["budget"] == 1 and list(r["draft_len"]) == [1, 0]
+    # three sequences, two drafts each, all survival .25 after the first:
+    # costs make a budget of 4 best; ranked (0,0) (1,0) (2,0) at .5, then
+    # (0,1) at .25 -- the lowest sequence takes the tied second draft
+    conf = np.array([[0.5, 0.5], [0.5, 0.5], [0.5, 0.5]], np.float32)
+    vc = np.array([1, 1, 1, 1, 1, 4, 4], np.float32)
+    r = oracle.av_budget(conf, np.zeros(7, np.float32), vc)
+    assert r["budget"] == 4 and list(r["draft_len"]) == [2, 1, 1]
+
+
 def _problem(seed, B=6, K=5, V=64):
     rng = np.random.default_rng(seed)
     zt = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
