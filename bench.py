@@ -287,19 +287,26 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
+def verify_kernel_name(w):
+    """The verify kernel instance a default launch of this workload runs:
+    verify_kernel<T, kTemp = 0, kRing>, the staging-buffer ring (kRing = 1)
+    in the modes with no draw."""
+    t = "__nv_bfloat16" if w.dtype == "bf16" else "float"
+    return f"verify_kernel<{t}, 0, {0 if w.mode == 'stochastic' else 1}>"
+
+
 def recorded_traffic(workload_name):
-    """Per-launch DRAM bytes of the verify kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    """Per-launch DRAM bytes of the verify kernel on this workload from the
+    committed ncu summary, if it was taken on the current kernel source."""
     try:
-        kv = dict(line.strip().split("=", 1) for line in open(TRAFFIC_FILE) if "=" in line)
+        with open(TRAFFIC_FILE) as f:
+            kv = dict(line.strip().split("=", 1) for line in f if "=" in line and not line.startswith("#"))
     except OSError:
         return None
     if kv.get("source_sha256") != source_hash():
         return None
-    if kv.get("workload") != workload_name:
-        return None
     try:
-        return float(kv["dram_bytes_per_launch"])
+        return float(kv["dram_bytes_per_launch." + workload_name])
     except (KeyError, ValueError):
         return None
 
@@ -417,8 +424,7 @@ def run_ours(args, w, world, rank, local, pg):
         "hbm_gbs": logit_bytes * world * args.steps / (total_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
-                     "kernel": ("verify_kernel<__nv_bfloat16, 0, 0>" if w.dtype == "bf16"
-                                else "verify_kernel<float, 0, 0>"),
+                     "kernel": verify_kernel_name(w),
                      "algorithmic_bytes_per_launch": logit_bytes,
                      "kernel_ms_mean": kern_s * 1e3, "kernel_ms_median": statistics.median(verify_ms),
                      "peak_source": peak_src, "frac_note": "of measured" if "measured" in peak_src
@@ -590,10 +596,10 @@ def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, defa
     res = {"verify_ms_mean": mean_ms, "verify_ms_median": st.median(ms),
            "frac": logit_bytes / (mean_ms / 1e3) / 1e9 / peak, "default_verify_ms_mean": default_ms,
            "inv_temperature": "log-uniform [0.5, 2] per sequence",
-           "kernel": "verify_kernel<T, 1> (temperature variant)"}
+           "kernel": "verify_kernel<T, 1, 0> (temperature variant)"}
     if top_p is not None:
         res["top_p"] = top_p
-        res["kernel"] = "nucleus_kernel<T> + verify_kernel<T, 1> (precomputed rows)"
+        res["kernel"] = "nucleus_cluster_kernel<T> + verify_kernel<T, 1, 0> (precomputed rows)"
     return res
 
 
