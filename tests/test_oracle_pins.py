@@ -396,6 +396,23 @@ def test_fly_truth_table_exhaustive(K):
     assert h[0] > 0.99 and h[1] < 1e-6
 
 
+def test_fly_with_a_closed_gate_is_greedy():
+    """Normalised entropy never exceeds 1, so at theta > 1 no deviation is
+    deferred and FLy reduces to greedy exact match, whatever the window."""
+    rng = np.random.default_rng(23)
+    B, K, V = 64, 5, 32
+    zt = rng.normal(0, 1.5, (B, K + 1, V)).astype(np.float32)
+    am = zt.argmax(-1)
+    # drafts that match the target's argmax often, so prefixes of every length occur
+    x = np.where(rng.random((B, K)) < 0.7, am[:, :K], rng.integers(0, V, (B, K))).astype(np.int32)
+    g = oracle.verify(zt, None, x, None, mode=oracle.GREEDY)
+    for W in (1, 2, 4):
+        f = oracle.verify(zt, None, x, None, mode=oracle.FLY, fly_theta=1.5, fly_window=W)
+        np.testing.assert_array_equal(f["accepted_len"], g["accepted_len"])
+        np.testing.assert_array_equal(f["out_tokens"], g["out_tokens"])
+    assert len(np.unique(g["accepted_len"])) >= 4
+
+
 def test_fly_gate_tie_defers():
     # h == theta defers (the gate reads h_j >= theta). A two-token uniform row
     # has normalised entropy exactly 1 in fp64; theta = 1 puts it on the tie.
