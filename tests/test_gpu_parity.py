@@ -262,6 +262,20 @@ def test_greedy_ties_bf16():
     del am, inp
 
 
+def test_fly_with_a_closed_gate_is_greedy_full_size():
+    """A property that holds at any size: normalised entropy never exceeds 1,
+    so at theta > 1 FLy defers nothing and equals greedy exact match, bit
+    for bit, on the full FLy workload (B=128, K=15, V=152064, bf16)."""
+    w = workloads.FLY
+    inp = workloads.make_inputs(w, 1009, DEV)
+    g = sv.verify(inp["zt"], None, inp["x"], None, mode="greedy")
+    for W in (1, 4):
+        f = sv.verify(inp["zt"], None, inp["x"], None, mode="fly", fly_theta=1.5, fly_window=W)
+        torch.cuda.synchronize()
+        assert torch.equal(f["accepted_len"], g["accepted_len"])
+        assert torch.equal(f["out_tokens"], g["out_tokens"])
+
+
 @pytest.mark.parametrize("wl", [workloads.ESTIMATOR, workloads.FLY.scaled(B=64),
                                 workloads.Workload("sweep_B512_K8_V152064_f32", B=512, K=8, V=152064,
                                                    dtype="f32", mode="stochastic")],
