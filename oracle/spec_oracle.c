@@ -744,7 +744,7 @@ int oracle_irls_refit(int32_t K, const double *g, const double *H, const int64_t
  * Readings: survival is an fp32 running product in ascending position (the
  * precision that decides the ranking on the GPU too); ties in survival rank
  * by ascending flat index b*K + i, so each sequence's winners are a prefix
- * * of its drafts; NaN survival ranks last. The top-k sum is kept in fixed
+ * of its drafts; NaN survival ranks last. The top-k sum is kept in fixed
  * point: each positive survival is rounded to the nearest multiple of 2^-32
  * and the multiples are added as integers, so S_k is exact and the same in
  * any order. The decision is taken in fp32 (the pages fix no precision; the
@@ -758,39 +758,40 @@ int oracle_irls_refit(int32_t K, const double *g, const double *H, const int64_t
  * Outputs: draft_len [B], *budget, survival [B][K] f32 (may be NULL),
  * objective [B*K+1] f32 (may be NULL; -inf where ineligible), *gap (may be
  * NULL): the relative gap between the best and the second-best objective. */
-static const float *g_av_key;
+typedef struct {
+    float key;     /* survival (NaN replaced by -1) */
+    int32_t idx;   /* flat index b*K + i */
+} AvRank;
+
 static int av_cmp(const void *pa, const void *pb) {
-    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
-    float ka = g_av_key[a], kb = g_av_key[b];
-    if (ka > kb) return -1;
-    if (ka < kb) return 1;
-    return a < b ? -1 : (a > b ? 1 : 0);
+    const AvRank *a = (const AvRank *)pa, *b = (const AvRank *)pb;
+    if (a->key > b->key) return -1;
+    if (a->key < b->key) return 1;
+    return a->idx < b->idx ? -1 : (a->idx > b->idx ? 1 : 0);
 }
 
 int oracle_av_budget(int32_t B, int32_t K, const float *conf, const float *draft_cost, const float *verify_cost,
                      int32_t *draft_len, int32_t *budget, float *survival, float *objective, double *gap) {
     if (B < 0 || K < 1 || (B > 0 && !conf) || !draft_cost || !verify_cost || !draft_len || !budget) return -1;
     const int64_t N = (int64_t)B * K;
-    float *key = (float *)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
-    int32_t *ord = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    AvRank *rk = (AvRank *)malloc(sizeof(AvRank) * (size_t)(N > 0 ? N : 1));
     float *obj = (float *)malloc(sizeof(float) * (size_t)(N + 1));
-    if (!key || !ord || !obj) { free(key); free(ord); free(obj); return -1; }
+    if (!rk || !obj) { free(rk); free(obj); return -1; }
     for (int32_t b = 0; b < B; ++b) {
         float sv = 1.0f;
         for (int32_t i = 0; i < K; ++i) {
             sv = sv * conf[(size_t)b * K + i];
             if (survival) survival[(size_t)b * K + i] = sv;
-            key[(size_t)b * K + i] = sv == sv ? sv : -1.0f;   /* NaN ranks last */
+            rk[(size_t)b * K + i].key = sv == sv ? sv : -1.0f;   /* NaN ranks last */
+            rk[(size_t)b * K + i].idx = b * K + i;
         }
     }
-    for (int64_t j = 0; j < N; ++j) ord[j] = (int32_t)j;
-    g_av_key = key;
-    qsort(ord, (size_t)N, sizeof(int32_t), av_cmp);
+    qsort(rk, (size_t)N, sizeof(AvRank), av_cmp);
     uint64_t S = 0;                            /* sum of the top k, in units of 2^-32 */
     float best = -INFINITY, second = -INFINITY;
     int64_t kbest = 0;
     for (int64_t k = 0; k <= N; ++k) {
-        if (k > 0 && key[ord[k - 1]] > 0.0f) S += (uint64_t)llrint((double)key[ord[k - 1]] * 4294967296.0);
+        if (k > 0 && rk[k - 1].key > 0.0f) S += (uint64_t)llrint((double)rk[k - 1].key * 4294967296.0);
         volatile float c = draft_cost[k] + verify_cost[k];          /* fp32 add, no contraction */
         volatile float num = (float)((uint64_t)B * 4294967296ull + S);
         volatile float q = num / c;
@@ -801,11 +802,11 @@ int oracle_av_budget(int32_t B, int32_t K, const float *conf, const float *draft
     }
     for (int32_t b = 0; b < B; ++b) draft_len[b] = 0;
     if (best == -INFINITY) kbest = 0;
-    for (int64_t j = 0; j < kbest; ++j) draft_len[ord[j] / K] += 1;
+    for (int64_t j = 0; j < kbest; ++j) draft_len[rk[j].idx / K] += 1;
     *budget = (int32_t)kbest;
     if (objective) for (int64_t k = 0; k <= N; ++k) objective[k] = obj[k];
     if (gap) *gap = (best > -INFINITY && second > -INFINITY) ? ((double)best - second) / fabs((double)best) : INFINITY;
-    free(key); free(ord); free(obj);
+    free(rk); free(obj);
     return 0;
 }
 

@@ -132,8 +132,8 @@ PLANTED = {
         [(NGRAM, "test_hand_cases", {})]),
     # adaptive-verification budget
     "av_ties_to_highest_index": (
-        "    return a < b ? -1 : (a > b ? 1 : 0);\n}\n\nint oracle_av_budget",
-        "    return a > b ? -1 : (a < b ? 1 : 0);\n}\n\nint oracle_av_budget",
+        "    return a->idx < b->idx ? -1 : (a->idx > b->idx ? 1 : 0);",
+        "    return a->idx > b->idx ? -1 : (a->idx < b->idx ? 1 : 0);",
         [(AV, "test_cross_sequence_ties_rank_by_index", {})]),
     "av_survival_not_a_product": (
         "            sv = sv * conf[(size_t)b * K + i];", "            sv = conf[(size_t)b * K + i];",
