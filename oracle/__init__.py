@@ -61,7 +61,8 @@ def bind(lib):
     P = ctypes.c_void_p
     i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
     lib.oracle_verify.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.c_int, P, i64, P, i64,
-                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, P, P, P, P, dbl, ctypes.c_int]
+                                  P, P, dbl, i32, P, P, P, P, P, P, P, P, P, P, P, P, dbl,
+                                  P, P, P, P, P, ctypes.c_int]
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_confidence.argtypes = [i32, i32, i32, ctypes.c_int, P, i64, P, P, P, P, ctypes.c_int]
     lib.oracle_confidence.restype = ctypes.c_int
@@ -96,7 +97,8 @@ def _logits(z):
 
 
 def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_params=None,
-           nthreads=1, want_cdf=False, draft_len=None, inv_temp=None, top_p=1.0):
+           nthreads=1, want_cdf=False, draft_len=None, inv_temp=None, top_p=1.0, force=None,
+           nuc_shift=None):
     """Verify B sequences. zt [B,K+1,V], zd [B,K,V] or None, x [B,K] int32,
     u [B,K+1] float32 or None, draft_len [B] int32 in [0, K] or None (drafts
     submitted for verification per sequence; None: all K), inv_temp [B]
@@ -109,6 +111,17 @@ def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_param
     margin_cdf [B] (margin of the final draw), margin [B] (the smaller of the
     two), flags [B], and with want_cdf the normalised running sum of each
     final draw's weights, cdf [B,V].
+
+    Per-position report (for parity checks of a computation that decided a
+    position in doubt the other way): margin_pos [B,K] (the margin of each
+    decision the scan takes, +inf where none is taken), natural_pos [B,K]
+    (the rule's decision there: 1 accept / gate open, 0 reject / gate
+    closed, -1 none), nuc_doubt [B,2K+1] (top-p: bit 1 the group at a row's
+    z* may be dropped, bit 2 the next group down may be added; rows are
+    target 0..K, then draft 0..K-1). Overrides: force [B,K] int (-1: the
+    rule; 0/1: that decision where the scan reaches the position), nuc_shift
+    [B,2K+1] int (0: the natural nucleus boundary; -1 / +1: one tie group
+    up / down).
     """
     lib = _load()
     zt, dt = _logits(zt)
@@ -132,7 +145,16 @@ def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_param
         margin_acc=np.empty(B, np.float64),
         margin_cdf=np.empty(B, np.float64),
         flags=np.empty(B, np.int32),
+        margin_pos=np.empty((B, K), np.float64),
+        natural_pos=np.empty((B, K), np.int32),
+        nuc_doubt=np.empty((B, 2 * K + 1), np.int32),
     )
+    if force is not None:
+        force = np.ascontiguousarray(force, dtype=np.int32)
+        assert force.shape == (B, K)
+    if nuc_shift is not None:
+        nuc_shift = np.ascontiguousarray(nuc_shift, dtype=np.int32)
+        assert nuc_shift.shape == (B, 2 * K + 1)
     cdf = np.full((B, V), np.nan) if want_cdf else None
     if draft_len is not None:
         draft_len = np.ascontiguousarray(draft_len, dtype=np.int32)
@@ -146,7 +168,9 @@ def verify(zt, zd, x, u, mode=STOCHASTIC, fly_theta=0.3, fly_window=6, est_param
                            _ptr(out["pos_stats"]), _ptr(out["conf"]) if est is not None else None,
                            _ptr(out["feature"]) if zd is not None else None,
                            _ptr(out["margin_acc"]), _ptr(out["margin_cdf"]), _ptr(cdf),
-                           _ptr(out["flags"]), _ptr(draft_len), _ptr(inv_temp), float(top_p), int(nthreads))
+                           _ptr(out["flags"]), _ptr(draft_len), _ptr(inv_temp), float(top_p),
+                           _ptr(force), _ptr(nuc_shift), _ptr(out["margin_pos"]), _ptr(out["natural_pos"]),
+                           _ptr(out["nuc_doubt"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     out["margin"] = np.minimum(out["margin_acc"], out["margin_cdf"])

@@ -125,8 +125,8 @@ static int key_desc(const void *a, const void *b) {
     return x->v < y->v ? -1 : (x->v > y->v ? 1 : 0);
 }
 
-static double nucleus(const void *row, int dtype, int32_t V, double top_p, double *p, OrKey *keys,
-                      double *zstar, double *margin, double *zamb_hi, double *zamb_lo) {
+static double nucleus(const void *row, int dtype, int32_t V, double top_p, int shift, double *p, OrKey *keys,
+                      double *zstar, double *margin_hi, double *margin_lo, double *zamb_hi, double *zamb_lo) {
     for (int32_t v = 0; v < V; ++v) {
         keys[v].z = logit_at(row, dtype, v);
         keys[v].v = v;
@@ -135,7 +135,7 @@ static double nucleus(const void *row, int dtype, int32_t V, double top_p, doubl
     double above = 0.0;   /* mass of logits strictly above the current value */
     int32_t i = 0;
     *zstar = keys[0].z;
-    *margin = INFINITY;
+    *margin_hi = *margin_lo = INFINITY;
     *zamb_hi = *zamb_lo = NAN;
     while (i < V) {
         int32_t j = i;
@@ -146,16 +146,21 @@ static double nucleus(const void *row, int dtype, int32_t V, double top_p, doubl
             *zstar = keys[i].z;
             /* the group at z* may be dropped */
             if (above > 0.0 && top_p - above < OR_NUC_REL * above) {
-                if (g > OR_NUC_BENIGN * P) *margin = dmin(*margin, (top_p - above) / above);
+                if (g > OR_NUC_BENIGN * P) *margin_hi = (top_p - above) / above;
                 *zamb_hi = keys[i].z;
             }
             /* the next group down may be added */
             if (j < V && P - top_p < OR_NUC_REL * P) {
                 double gn = 0.0;
                 for (int32_t k = j; k < V && keys[k].z == keys[j].z; ++k) gn += p[keys[k].v];
-                if (gn > OR_NUC_BENIGN * P) *margin = dmin(*margin, (P - top_p) / P);
+                if (gn > OR_NUC_BENIGN * P) *margin_lo = (P - top_p) / P;
                 *zamb_lo = keys[j].z;
             }
+            /* a caller-chosen boundary one tie group off (parity checks of a
+             * computation that placed a boundary in doubt the other way):
+             * -1 drops the group at z*, +1 adds the next group down */
+            if (shift < 0 && i > 0) *zstar = keys[i - 1].z;
+            if (shift > 0 && j < V) *zstar = keys[j].z;
             break;
         }
         above += g;
@@ -176,18 +181,26 @@ static double nucleus(const void *row, int dtype, int32_t V, double top_p, doubl
  * *zstar (-inf without truncation); *margin takes the smaller of itself and
  * the nucleus boundary's margin, which is 0 when the logit of token `xtok`
  * (-1: none) lies in a tie group whose membership is in doubt. */
-static double processed_row(const void *row, int dtype, int32_t V, double sc, double top_p, double *p,
-                            OrKey *keys, int *ok, double *zstar, double *margin, int32_t xtok) {
+static double processed_row(const void *row, int dtype, int32_t V, double sc, double top_p, int shift,
+                            double *p, OrKey *keys, int *ok, double *zstar, double *margin, int32_t xtok,
+                            int *doubt) {
     double lse = softmax_row(row, dtype, V, sc, p, ok);
     *zstar = -INFINITY;
+    if (doubt) *doubt = 0;
     if (*ok && top_p < 1.0) {
-        double m, zh, zl;
-        lse += log(nucleus(row, dtype, V, top_p, p, keys, zstar, &m, &zh, &zl));
-        *margin = dmin(*margin, m);
+        double mh, ml, zh, zl;
+        lse += log(nucleus(row, dtype, V, top_p, shift, p, keys, zstar, &mh, &ml, &zh, &zl));
+        int tok_hi = 0, tok_lo = 0;
         if (xtok >= 0 && xtok < V) {
             const double zx = logit_at(row, dtype, xtok);
-            if (zx == zh || zx == zl) *margin = 0.0;
+            tok_hi = zx == zh;
+            tok_lo = zx == zl;
         }
+        *margin = dmin(*margin, dmin(mh, ml));
+        if (tok_hi || tok_lo) *margin = 0.0;
+        /* which way the boundary is in doubt: bit 1 the group at z* may be
+         * dropped, bit 2 the next group down may be added */
+        if (doubt) *doubt = ((mh < INFINITY || tok_hi) ? 1 : 0) | ((ml < INFINITY || tok_lo) ? 2 : 0);
     }
     return lse;
 }
@@ -282,7 +295,8 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
                        const double *est, int32_t *out_tokens, int32_t *acc_len,
                        double *pos_stats, double *conf, double *feature,
                        double *margin_acc, double *margin_cdf, double *cdf_out, int *flags,
-                       double *p, double *q, double *r, OrKey *keys) {
+                       const int32_t *force, const int32_t *nshift, double *margin_pos, int32_t *natural_pos,
+                       int32_t *nuc_doubt, double *p, double *q, double *r, OrKey *keys) {
     const size_t es = dtype == OR_F32 ? 4 : 2;
     const char *tbase = (const char *)zt;
     const char *dbase = (const char *)zd;
@@ -290,6 +304,15 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
     double mn = INFINITY;      /* nucleus boundary margin (top-p), folded into mg at the end */
     double mc = INFINITY;      /* margin of the final inverse-CDF draw */
     int fl = 0;
+    /* boundary override of row (target j: j; draft j: K+1+j), 0 = natural */
+#define OR_SHIFT_T(j) (nshift ? nshift[(j)] : 0)
+#define OR_SHIFT_D(j) (nshift ? nshift[K + 1 + (j)] : 0)
+    for (int32_t j = 0; j < K; ++j) {
+        if (margin_pos) margin_pos[j] = INFINITY;
+        if (natural_pos) natural_pos[j] = -1;
+    }
+    if (nuc_doubt)
+        for (int32_t j = 0; j < 2 * K + 1; ++j) nuc_doubt[j] = 0;
 
     /* Per-position statistics (written whether or not the position is reached).
      * Only the first Kb drafts were submitted for verification (Kb = K unless
@@ -306,14 +329,19 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
         const void *trow = tbase + (size_t)j * (size_t)t_stride * es;
         int ok;
         double zs_t, zs_d;
-        double lse_t = processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs_t, &mn, j < Kb ? x[j] : -1);
+        int dbt = 0;
+        double lse_t = processed_row(trow, dtype, V, sc, top_p, OR_SHIFT_T(j), p, keys, &ok, &zs_t, &mn,
+                                     j < Kb ? x[j] : -1, &dbt);
+        if (nuc_doubt) nuc_doubt[j] = dbt;
         if (!ok) fl |= OR_FLAG_BAD_ROW;
         double h = norm_entropy(p, V);
         double lr = NAN, f = NAN;
         if (j < Kb && zd) {
             const void *drow = dbase + (size_t)j * (size_t)d_stride * es;
             int okd;
-            double lse_d = processed_row(drow, dtype, V, sc, top_p, q, keys, &okd, &zs_d, &mn, x[j]);
+            double lse_d = processed_row(drow, dtype, V, sc, top_p, OR_SHIFT_D(j), q, keys, &okd, &zs_d, &mn,
+                                         x[j], &dbt);
+            if (nuc_doubt) nuc_doubt[K + 1 + j] = dbt;
             if (!okd) fl |= OR_FLAG_BAD_ROW;
             int32_t amax_d = argmax_row(drow, dtype, V);
             f = logit_qmax(q, V, amax_d, &fl);
@@ -347,8 +375,10 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
             const void *drow = dbase + (size_t)i * (size_t)d_stride * es;
             int ok;
             double zs;
-            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mn, x[i]);
-            processed_row(drow, dtype, V, sc, top_p, q, keys, &ok, &zs, &mn, x[i]);
+            double mni = INFINITY;   /* nucleus margins of this position's two rows */
+            processed_row(trow, dtype, V, sc, top_p, OR_SHIFT_T(i), p, keys, &ok, &zs, &mni, x[i], NULL);
+            processed_row(drow, dtype, V, sc, top_p, OR_SHIFT_D(i), q, keys, &ok, &zs, &mni, x[i], NULL);
+            mn = dmin(mn, mni);
             double px = p[x[i]], qx = q[x[i]];
             double acc;
             if (qx > 0.0) {
@@ -360,7 +390,15 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
                 acc = px > 0.0 ? 1.0 : 0.0;
             }
             mg = dmin(mg, fabs((double)u[i] - acc));
-            if ((double)u[i] < acc) { ++n; continue; }
+            int take = (double)u[i] < acc;
+            /* per-position report: the margin of this decision (with its
+             * rows' nucleus margins) and the decision the rule takes */
+            if (margin_pos) margin_pos[i] = dmin(fabs((double)u[i] - acc), mni);
+            if (natural_pos) natural_pos[i] = take;
+            /* a caller-imposed decision (parity checks of a computation that
+             * decided a position in doubt the other way) */
+            if (force && force[i] >= 0) take = force[i] != 0;
+            if (take) { ++n; continue; }
             double Z = 0.0;
             for (int32_t v = 0; v < V; ++v) {
                 r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
@@ -384,7 +422,7 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
             const void *trow = tbase + (size_t)Kb * (size_t)t_stride * es;
             int ok;
             double zs;
-            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mn, -1);
+            processed_row(trow, dtype, V, sc, top_p, OR_SHIFT_T(Kb), p, keys, &ok, &zs, &mn, -1, NULL);
             double Z = 0.0;
             for (int32_t v = 0; v < V; ++v) Z += p[v];
             token = inverse_cdf(p, V, Z, (double)u[K], &mc, &fl);
@@ -414,11 +452,17 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
             if (x[j] == a) continue;               /* no deviation: accept j */
             int ok;
             double zs;
-            processed_row(trow, dtype, V, sc, top_p, p, keys, &ok, &zs, &mn, -1);
+            double mnj = INFINITY;
+            processed_row(trow, dtype, V, sc, top_p, OR_SHIFT_T(j), p, keys, &ok, &zs, &mnj, -1, NULL);
+            mn = dmin(mn, mnj);
             double h = norm_entropy(p, V);
             mg = dmin(mg, fabs(h - fly_theta));
+            int open = h >= fly_theta;
+            if (margin_pos) margin_pos[j] = dmin(fabs(h - fly_theta), mnj);
+            if (natural_pos) natural_pos[j] = open;
+            if (force && force[j] >= 0) open = force[j] != 0;   /* caller-imposed gate */
             int reject;
-            if (h < fly_theta) {
+            if (!open) {
                 reject = 1;                        /* confident target */
             } else if (j + fly_window > Kb - 1) {
                 reject = 1;                        /* window past the draft end */
@@ -445,6 +489,8 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
     if (margin_acc) *margin_acc = mg;
     if (margin_cdf) *margin_cdf = mc;
     if (flags) *flags = fl;
+#undef OR_SHIFT_T
+#undef OR_SHIFT_D
 }
 
 /* Full verification over B sequences. Layouts (row-major, elements):
@@ -473,6 +519,23 @@ static void verify_one(int32_t K, int32_t Kb, double sc, double top_p, int32_t V
  *    further truncated to its nucleus (see nucleus()) and renormalised,
  *    before every use; the nucleus boundary's margin (see nucleus()) joins
  *    margin_acc.
+ * Per-position report and overrides, for parity checks of a computation
+ * that decided a position in doubt the other way (all may be NULL):
+ *  margin_pos [B][K]: the margin of each decision the scan takes
+ *    (stochastic: |u_i - min(1, p/q)|; FLy: |h_j - theta| at each gate
+ *    evaluated), with the nucleus margins of the position's rows under
+ *    top-p; +inf at positions not decided,
+ *  natural_pos [B][K]: the decision the rule takes there (1 accept / gate
+ *    open, 0 reject / gate closed), -1 at positions not decided,
+ *  force [B][K]: -1 follows the rule; 0 or 1 imposes that decision at the
+ *    position if the scan reaches it (margin_pos and natural_pos still
+ *    report the rule's own),
+ *  nshift [B][2K+1] (rows: target 0..K, then draft 0..K-1): 0 the natural
+ *    nucleus boundary, -1 the group at z* dropped, +1 the next group down
+ *    added (top-p only),
+ *  nuc_doubt [B][2K+1]: which way each verified row's nucleus boundary is in
+ *    doubt (bit 1: the group at z* may be dropped; bit 2: the next group
+ *    down may be added).
  * nthreads > 0 sets the OpenMP thread count. Returns 0, or -1 on bad args. */
 int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const void *zt, int64_t t_stride, const void *zd, int64_t d_stride,
@@ -480,7 +543,9 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                   const double *est, int32_t *out_tokens, int32_t *accepted_len,
                   double *pos_stats, double *conf, double *feature,
                   double *margin_acc, double *margin_cdf, double *cdf, int32_t *flags,
-                  const int32_t *draft_len, const float *inv_temp, double top_p, int nthreads) {
+                  const int32_t *draft_len, const float *inv_temp, double top_p,
+                  const int32_t *force, const int32_t *nshift, double *margin_pos, int32_t *natural_pos,
+                  int32_t *nuc_doubt, int nthreads) {
     if (B < 0 || K < 1 || V < 2 || !zt || !x || !out_tokens || !accepted_len) return -1;
     if (!(top_p > 0.0 && top_p <= 1.0)) return -1;
     if (inv_temp)
@@ -517,7 +582,12 @@ int oracle_verify(int32_t B, int32_t K, int32_t V, int dtype, int mode,
                            conf ? conf + (size_t)b * K : NULL,
                            feature ? feature + (size_t)b * K : NULL,
                            margin_acc ? margin_acc + b : NULL, margin_cdf ? margin_cdf + b : NULL,
-                           cdf ? cdf + (size_t)b * (size_t)V : NULL, &fl, p, q, r, keys);
+                           cdf ? cdf + (size_t)b * (size_t)V : NULL, &fl,
+                           force ? force + (size_t)b * K : NULL,
+                           nshift ? nshift + (size_t)b * (2 * K + 1) : NULL,
+                           margin_pos ? margin_pos + (size_t)b * K : NULL,
+                           natural_pos ? natural_pos + (size_t)b * K : NULL,
+                           nuc_doubt ? nuc_doubt + (size_t)b * (2 * K + 1) : NULL, p, q, r, keys);
                 if (flags) flags[b] = fl;
             }
         }

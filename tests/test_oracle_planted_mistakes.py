@@ -28,6 +28,7 @@ TOP_P = "test_oracle_top_p_pins"
 IRLS = "test_oracle_irls_pins"
 AV = "test_oracle_av_pins"
 NGRAM = "test_oracle_ngram_pins"
+DEC = "test_oracle_decision_report_pins"
 
 # name: (expression in spec_oracle.c, the planted mistake, pins that catch it
 # as (module, test, keyword arguments))
@@ -62,7 +63,7 @@ PLANTED = {
         [(PINS, "test_confidence_is_sigmoid_of_affine_feature", {})]),
     # the accept rule and the draws
     "accept_test_flipped": (
-        "if ((double)u[i] < acc) { ++n; continue; }", "if ((double)u[i] > acc) { ++n; continue; }",
+        "int take = (double)u[i] < acc;", "int take = (double)u[i] > acc;",
         [(PINS, "test_footnote_two_token_example", {}), (PINS, "test_p_equals_q_accepts_everything", {})]),
     "residual_operands_transposed": (
         "r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;", "r[v] = q[v] > p[v] ? q[v] - p[v] : 0.0;",
@@ -81,7 +82,7 @@ PLANTED = {
         [(PINS, "test_greedy_is_argmax_match_with_ties", {}), (TEMP, "test_low_temperature_is_greedy", {})]),
     # FLy's gate and window
     "fly_gate_tie_rejects": (
-        "            if (h < fly_theta) {", "            if (h <= fly_theta) {",
+        "int open = h >= fly_theta;", "int open = h > fly_theta;",
         [(PINS, "test_fly_gate_tie_defers", {})]),
     "fly_window_one_short": (
         "for (int32_t k = j + 1; k <= j + fly_window; ++k) {", "for (int32_t k = j + 1; k < j + fly_window; ++k) {",
@@ -122,6 +123,27 @@ PLANTED = {
     "nucleus_drops_boundary_ties": (
         "        if (logit_at(row, dtype, v) >= *zstar) P += p[v];", "        if (logit_at(row, dtype, v) > *zstar) P += p[v];",
         [(TOP_P, "test_ties_at_the_boundary_are_all_kept", {}), (TOP_P, "test_closed_form_four_tokens", {})]),
+    # the per-position decision report and its overrides
+    "imposed_decision_ignored": (
+        "            if (force && force[i] >= 0) take = force[i] != 0;", "",
+        [(DEC, "test_imposed_acceptance_draws_the_bonus_from_the_last_row", {}),
+         (DEC, "test_imposed_rejection_draws_the_residual_of_that_row", {"i": 1})]),
+    "imposed_gate_inverted": (
+        "if (force && force[j] >= 0) open = force[j] != 0;", "if (force && force[j] >= 0) open = force[j] == 0;",
+        [(DEC, "test_fly_imposed_gates_follow_the_window_rule", {"W": 2})]),
+    "position_margin_of_the_ratio_alone": (
+        "if (margin_pos) margin_pos[i] = dmin(fabs((double)u[i] - acc), mni);",
+        "if (margin_pos) margin_pos[i] = dmin(acc, mni);",
+        [(DEC, "test_stochastic_report_against_scipy", {})]),
+    "nucleus_shift_direction_swapped": (
+        "            if (shift < 0 && i > 0) *zstar = keys[i - 1].z;\n            if (shift > 0 && j < V) *zstar = keys[j].z;",
+        "            if (shift > 0 && i > 0) *zstar = keys[i - 1].z;\n            if (shift < 0 && j < V) *zstar = keys[j].z;",
+        [(DEC, "test_nucleus_shift_moves_the_boundary_one_group", {"shift": -1}),
+         (DEC, "test_nucleus_shift_moves_the_boundary_one_group", {"shift": 1})]),
+    "nucleus_doubt_bits_swapped": (
+        "if (doubt) *doubt = ((mh < INFINITY || tok_hi) ? 1 : 0) | ((ml < INFINITY || tok_lo) ? 2 : 0);",
+        "if (doubt) *doubt = ((mh < INFINITY || tok_hi) ? 2 : 0) | ((ml < INFINITY || tok_lo) ? 1 : 0);",
+        [(DEC, "test_nucleus_doubt_bits", {})]),
     # n-gram drafting
     "ngram_shortest_first": (
         "for (int32_t n = n_max; n >= n_min && start < 0; --n) {",
