@@ -204,8 +204,10 @@ def verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
 
 
 def confidence(draft_logits: torch.Tensor, est_params: Optional[torch.Tensor] = None,
-               workspace: Optional[Workspace] = None, stream: Optional[torch.cuda.Stream] = None):
-    """Run spec_confidence: returns (feature [B,K], conf [B,K] or None)."""
+               workspace: Optional[Workspace] = None, stream: Optional[torch.cuda.Stream] = None,
+               out: Optional[dict] = None):
+    """Run spec_confidence: returns (feature [B,K], conf [B,K] or None).
+    ``out`` may supply preallocated ``feature`` / ``conf`` tensors."""
     zd = draft_logits
     if not zd.is_cuda:
         raise ValueError("draft_logits must be a CUDA tensor")
@@ -213,8 +215,19 @@ def confidence(draft_logits: torch.Tensor, est_params: Optional[torch.Tensor] = 
     B, K, V = zd.shape
     dt = _dtype_code(zd)
     ds = _row_stride(zd, "draft_logits")
-    feat = torch.empty((B, K), dtype=torch.float32, device=dev)
-    conf = torch.empty((B, K), dtype=torch.float32, device=dev) if est_params is not None else None
+    o = dict(out or {})
+    feat = o.get("feature")
+    if feat is None:
+        feat = torch.empty((B, K), dtype=torch.float32, device=dev)
+    conf = None
+    if est_params is not None:
+        conf = o.get("conf")
+        if conf is None:
+            conf = torch.empty((B, K), dtype=torch.float32, device=dev)
+    for t in (feat, conf):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (B, K) or not t.is_contiguous()
+                              or t.device != dev):
+            raise ValueError("confidence: out tensors must be contiguous float32 [B, K] on the logits' device")
     L = _native.lib()
     nbytes = int(L.spec_confidence_workspace_size(B, K, V, dt))
     if nbytes == 0:

@@ -18,6 +18,7 @@ import pytest
 import oracle
 import workloads
 from helpers import compare, oracle_run
+import helpers as hv
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -99,7 +100,7 @@ def test_ragged_verify_matches_oracle(mode):
     dl[:3] = [0, w.K, 1]
     est = torch.tensor(np.r_[1.0, np.zeros(w.K)], dtype=torch.float32, device=DEV)
     kw = dict(fly_theta=0.3, fly_window=2) if mode == "fly" else {}
-    g = sv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"] if mode == "stochastic" else None, mode=mode,
+    g = hv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"] if mode == "stochastic" else None, mode=mode,
                   est_params=est, want_pos_stats=True, want_feature=True, want_conf=True,
                   draft_len=torch.tensor(dl, device=DEV), **kw)
     torch.cuda.synchronize()
@@ -114,8 +115,8 @@ def test_full_draft_length_equals_the_unpruned_launch():
     w = workloads.ESTIMATOR
     w = type(w)(**{**w.__dict__, "B": 32})
     inp = workloads.make_inputs(w, 77, DEV)
-    a = sv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], want_pos_stats=True, want_feature=True)
-    b = sv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], want_pos_stats=True, want_feature=True,
+    a = hv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], want_pos_stats=True, want_feature=True)
+    b = hv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], want_pos_stats=True, want_feature=True,
                   draft_len=torch.full((w.B,), w.K, dtype=torch.int32, device=DEV))
     torch.cuda.synchronize()
     for k in ("out_tokens", "accepted_len", "pos_stats", "feature"):
@@ -161,9 +162,9 @@ def test_av_step_end_to_end():
     N = w.B * w.K
     dc, vc = _costs(np.random.default_rng(1), N, w.B)
     # GPU pipeline
-    _, conf = sv.confidence(inp["zd"], est)
+    _, conf = hv.confidence(inp["zd"], est)
     bud = sv.av_budget(conf, torch.tensor(dc, device=DEV), torch.tensor(vc, device=DEV))
-    g = sv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], est_params=est, want_pos_stats=True,
+    g = hv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], est_params=est, want_pos_stats=True,
                   want_feature=True, want_conf=True, draft_len=bud["draft_len"])
     torch.cuda.synchronize()
     # oracle pipeline

@@ -13,6 +13,7 @@ import pytest
 import oracle
 import workloads
 from helpers import compare
+import helpers as hv
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -67,7 +68,7 @@ def test_prompt_lookup_drafts_verified(mode):
     lens[:] = np.maximum(lens, 16)
     d = sv.ngram_draft(torch.tensor(ctx, device=DEV), torch.tensor(lens, device=DEV), 1, 4, w.K)
     kw = dict(fly_theta=w.fly_theta, fly_window=w.fly_window) if mode == "fly" else {}
-    g = sv.verify(inp["zt"], None, d["draft_tokens"], None, mode=mode, want_pos_stats=True,
+    g = hv.verify(inp["zt"], None, d["draft_tokens"], None, mode=mode, want_pos_stats=True,
                   draft_len=d["draft_len"], **kw)
     torch.cuda.synchronize()
     toks, dl = oracle.ngram_draft(ctx, lens, 1, 4, w.K)

@@ -16,6 +16,7 @@ import oracle
 import speculative_decoding_token_verify_gb300 as sv
 import workloads
 from helpers import compare, oracle_run
+import helpers as hv
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +36,7 @@ def _est(K):
 
 
 def _run(inp, mode, s, with_draft=True, est=None, draft_len=None, **kw):
-    out = sv.verify(inp["zt"], inp["zd"] if with_draft else None, inp["x"],
+    out = hv.verify(inp["zt"], inp["zd"] if with_draft else None, inp["x"],
                     inp["u"] if mode == "stochastic" else None, mode=mode, est_params=est,
                     want_pos_stats=True, want_feature=with_draft, want_conf=est is not None and with_draft,
                     inv_temperature=s, draft_len=draft_len, **kw)
@@ -109,7 +110,9 @@ def test_full_size_estimator_shape_sampled():
     r = oracle_run(sub, oracle.STOCHASTIC, nthreads=16, est=np.r_[1.0, np.zeros(w.K)],
                    inv_temp=sub["inv_temp"].cpu().numpy())
     gs = {k: g[k][idx.to(DEV)] for k in ("accepted_len", "out_tokens", "pos_stats", "feature", "conf")}
-    print(compare(gs, r, w.dtype, check_feature=True, check_conf=True))
+    s = compare(gs, r, w.dtype, check_feature=True, check_conf=True)
+    print(s)
+    hv.record("temperature_" + w.name + "_sampled40", s)
 
 
 def test_unit_temperature_agrees_with_the_default_path():
@@ -120,7 +123,7 @@ def test_unit_temperature_agrees_with_the_default_path():
     inp = workloads.make_inputs(w, 4500, DEV)
     one = torch.ones(w.B, dtype=torch.float32, device=DEV)
     a = _run(inp, "stochastic", one, est=_est(w.K))
-    b = sv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], est_params=_est(w.K), want_pos_stats=True,
+    b = hv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], est_params=_est(w.K), want_pos_stats=True,
                   want_feature=True, want_conf=True)
     torch.cuda.synchronize()
     pa, pb = a["pos_stats"].nan_to_num(7.0), b["pos_stats"].nan_to_num(7.0)
@@ -178,7 +181,7 @@ def test_gpu_lossless_chi_square_at_a_temperature():
     u = rng.random((N, K + 1), dtype=np.float32)
     zt = torch.from_numpy(zt1).to(DEV).expand(N, K + 1, V).contiguous()
     zd = torch.from_numpy(zd1).to(DEV).expand(N, K, V).contiguous()
-    g = sv.verify(zt, zd, torch.from_numpy(x).to(DEV), torch.from_numpy(u).to(DEV),
+    g = hv.verify(zt, zd, torch.from_numpy(x).to(DEV), torch.from_numpy(u).to(DEV),
                   inv_temperature=torch.full((N,), s, dtype=torch.float32, device=DEV))
     torch.cuda.synchronize()
     toks = g["out_tokens"].cpu().numpy()

@@ -18,6 +18,7 @@ import oracle
 import speculative_decoding_token_verify_gb300 as sv
 import workloads
 from helpers import compare, oracle_run
+import helpers as hv
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +38,7 @@ def _est(K):
 
 
 def _run(inp, mode, top_p, s=None, with_draft=True, est=None, draft_len=None, **kw):
-    out = sv.verify(inp["zt"], inp["zd"] if with_draft else None, inp["x"],
+    out = hv.verify(inp["zt"], inp["zd"] if with_draft else None, inp["x"],
                     inp["u"] if mode == "stochastic" else None, mode=mode, est_params=est,
                     want_pos_stats=True, want_feature=with_draft, want_conf=est is not None and with_draft,
                     inv_temperature=s, top_p=top_p, draft_len=draft_len, **kw)
@@ -54,14 +55,13 @@ def _wl(B, K, V, dt, lo=None, hi=None, **kw):
 def _cmp(g, r, dt, **kw):
     """compare() for top-p runs. A nucleus boundary in doubt (a tie group
     holding over 1e-6 of the nucleus, within 1e-5 relative of top_p; common
-    with bf16 ties at 128K vocabularies) flags its sequence; flagged
-    sequences may differ only where the GPU actually placed the boundary one
-    group off, which its 1.5e-6 worst-case mass error makes rare: at most a
-    tenth of them, and a tenth of all sequences overall."""
-    s = compare(g, r, dt, max_flagged_frac=1.0, doubt_frac=0.1, **kw)
+    with bf16 ties at 128K vocabularies) may be placed one tie group off by
+    the GPU; compare() then checks the sequence in full against the oracle
+    with that boundary moved. Such sequences may differ from the oracle's
+    natural result, on top of the usual bound."""
     B = len(r["accepted_len"])
-    assert s["mismatched"] <= max(1, 0.1 * B), s
-    return s
+    doubt = int((r["nuc_doubt"] != 0).any(1).sum())
+    return compare(g, r, dt, max_diff=2 + int(0.01 * B) + doubt, **kw)
 
 
 def _oracle(inp, mode, top_p, temp=True, **kw):
@@ -159,7 +159,9 @@ def test_full_size_estimator_shape_sampled():
     sub = {k: v[idx.to(v.device)] for k, v in inp.items()}
     r = _oracle(sub, oracle.STOCHASTIC, 0.95, nthreads=16, est=np.r_[1.0, np.zeros(w.K)])
     gs = {k: g[k][idx.to(DEV)] for k in ("accepted_len", "out_tokens", "pos_stats", "feature", "conf")}
-    print(_cmp(gs, r, w.dtype, check_feature=True, check_conf=True))
+    s = _cmp(gs, r, w.dtype, check_feature=True, check_conf=True)
+    print(s)
+    hv.record("top_p0.95_" + w.name + "_sampled32", s)
 
 
 def test_top_p_one_is_the_temperature_path_and_runs_repeat():
@@ -201,7 +203,7 @@ def test_gpu_lossless_chi_square_under_top_p():
     u = rng.random((N, K + 1), dtype=np.float32)
     zt = torch.from_numpy(zt1).to(DEV).expand(N, K + 1, V).contiguous()
     zd = torch.from_numpy(zd1).to(DEV).expand(N, K, V).contiguous()
-    g = sv.verify(zt, zd, torch.from_numpy(x).to(DEV), torch.from_numpy(u).to(DEV), top_p=tp)
+    g = hv.verify(zt, zd, torch.from_numpy(x).to(DEV), torch.from_numpy(u).to(DEV), top_p=tp)
     torch.cuda.synchronize()
     toks = g["out_tokens"].cpu().numpy()
     n = g["accepted_len"].cpu().numpy()
