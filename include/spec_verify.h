@@ -66,6 +66,7 @@ extern "C" {
 #define SPEC_ERR_BAD_TEMPERATURE 7 /* device status: an inverse temperature was out of range */
 
 /* limits */
+#define SPEC_MAX_B (1 << 24)     /* sequences per call                      */
 #define SPEC_MAX_K 31            /* draft positions per sequence            */
 #define SPEC_MAX_V (1 << 20)     /* vocabulary size                         */
 #define SPEC_STATIC_SCRATCH_BYTES (16u << 20) /* scratch of spec_verify_static */
@@ -81,7 +82,7 @@ typedef enum {
 } spec_mode;
 
 typedef struct {
-    int32_t B;            /* sequences, >= 1                                  */
+    int32_t B;            /* sequences, 1 .. SPEC_MAX_B                       */
     int32_t K;            /* draft positions, 1 .. SPEC_MAX_K                 */
     int32_t V;            /* vocabulary size, 2 .. SPEC_MAX_V                 */
     int32_t dtype;        /* spec_dtype of both logit tensors                 */
@@ -169,14 +170,23 @@ int spec_verify(const spec_verify_params *params, const void *target_logits,
  *    in it; each call clears the parts that must start at zero. Calls that
  *    can overlap on the GPU (other streams, other threads) race on it:
  *    serialise them.
- *  - The device status word lives in that array too; it is not readable
- *    through spec_get_device_status.
+ *  - The device status word lives in that array too: read it with
+ *    spec_static_device_status (not spec_get_device_status).
  * Arguments, rules and errors are those of spec_verify.
  */
 int spec_verify_static(const spec_verify_params *params, const void *target_logits,
                        const void *draft_logits, const int32_t *draft_tokens, const float *uniforms,
                        int32_t *out_tokens, int32_t *accepted_len, float *pos_stats,
                        const float *est_params, float *feature, float *conf, void *stream);
+
+/*
+ * Synchronously read the device status word of the last spec_verify_static
+ * call on the current device (waits for the device; allocates nothing).
+ * *status_out gets SPEC_OK or the largest device-side code that call raised,
+ * as for spec_get_device_status. SPEC_OK before any static call on this
+ * device. Like spec_verify_static, the pages have no counterpart to it.
+ */
+int spec_static_device_status(int32_t *status_out);
 
 /* Workspace bytes spec_confidence needs; 0 if the arguments are invalid. */
 size_t spec_confidence_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype);
@@ -386,6 +396,18 @@ int spec_irls_refit(int32_t K, void *state, float *est_params, double damping, d
  * SPEC_ERR_BAD_ROW, SPEC_ERR_BAD_TOKEN). For tests and debugging.
  */
 int spec_get_device_status(const void *workspace, int32_t *status_out);
+
+/*
+ * Testing hook for the bounded waits (no counterpart on the pages). A warp of
+ * the verification kernel whose stream work is done waits for the draw of
+ * the residual unit it claimed; it polls at most `polls` times (default
+ * 2^20, well under a second) before it raises SPEC_ERR_TIMEOUT in the status
+ * word and leaves that work undone. 0 makes every such wait give up at once,
+ * so that a test can see the timeout path without a hang: the outputs of
+ * the draw are then unspecified. The setting applies to launches enqueued
+ * after the call, from any thread; returns the previous setting.
+ */
+uint32_t spec_debug_set_wait_limit(uint32_t polls);
 
 /* Message of the calling thread's last failure ("" if none). */
 const char *spec_last_error(void);

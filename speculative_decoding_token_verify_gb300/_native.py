@@ -118,6 +118,8 @@ SIGNATURES = {
     "spec_irls_accumulate": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _P]),
     "spec_irls_refit": (ctypes.c_int, [_I32, _P, _P, ctypes.c_double, _P, _P]),
     "spec_get_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_I32)]),
+    "spec_static_device_status": (ctypes.c_int, [ctypes.POINTER(_I32)]),
+    "spec_debug_set_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
     "spec_last_error": (ctypes.c_char_p, []),
     "spec_version": (ctypes.c_char_p, []),
 }

@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -96,7 +97,7 @@ static_assert(SV_RES_SLICES_BF16 % kResBatch == 0 && SV_RES_SLICES_F32 % kResBat
               "residual units hold whole batches");
 constexpr int kStage = 256;            // 16-byte entries of a warp's shared staging buffer (4 KB)
 constexpr int kScanPer = 4 * kStage / 32;  // slice sums per lane in one pass of the locate scan
-constexpr unsigned kSpinLimit = 1u << 20;  // polls before giving up (< 1 s)
+constexpr unsigned kSpinLimit = 1u << 20;  // default polls before giving up (< 1 s)
 constexpr unsigned kFull = 0xffffffffu;
 // lane that publishes results and counts completions (lane 0 keeps the
 // scheduling state, so the two sets of long-latency operations stay apart)
@@ -174,6 +175,7 @@ struct Args {
                              // and (M_t, M_d, sL, 0)
     float *slices;           // [B][sstride] residual mass per slice
     float *gx;               // [B][2K] logits at the draft tokens: target rows, then draft rows
+    unsigned spin_limit;     // polls of a residual wait before SPEC_ERR_TIMEOUT
 };
 
 __device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
@@ -1080,7 +1082,7 @@ __device__ __forceinline__ int next_job(const Args &a, Sched &q, unsigned &id) {
 // unit is left and the warp has resolved every completion it owes.
 __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
     unsigned ns = 32;
-    for (unsigned it = 0; it < kSpinLimit; ++it) {
+    for (unsigned it = 0; it < a.spin_limit; ++it) {
         if (q.pend == kNone) {
             if (ld_relaxed(a.ctr + CTR_RES_CLAIM) >= a.res_units) return JOB_DONE;
             q.pend = atomicAdd(a.ctr + CTR_RES_CLAIM, 1u);
@@ -1338,6 +1340,9 @@ struct DevInfo {
 static std::mutex g_dev_mu;
 static DevInfo g_dev[64];
 
+// polls of a residual wait before it gives up (spec_debug_set_wait_limit)
+static std::atomic<unsigned> g_wait_limit{kSpinLimit};
+
 constexpr size_t kDynSmem = 0;
 
 template <typename T, bool kTemp, bool kRing>
@@ -1429,6 +1434,7 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     a.units = (unsigned)p.units;
     a.res_units = a.mode == MODE_STOCHASTIC ? (unsigned)a.B * (unsigned)p.nR : 0u;
     a.inv_log_v = (float)(1.0 / std::log((double)a.V));
+    a.spin_limit = g_wait_limit.load();
     int grid = 1;
     const bool temp = a.inv_temp != nullptr || a.pre;
     // the staging-buffer ring streams the launches with no draw
@@ -1485,6 +1491,8 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
 
 static int check_common(int B, int K, int V, int dtype) {
     if (B < 1) return fail(SPEC_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
+    // the draw record packs the sequence index as 64 b + 2 n + bonus in an int
+    if (B > SPEC_MAX_B) return fail(SPEC_ERR_UNSUPPORTED, "B must be <= %d (got %d)", SPEC_MAX_B, B);
     if (K < 1 || K > SPEC_MAX_K) return fail(SPEC_ERR_UNSUPPORTED, "K must be in [1, %d] (got %d)", SPEC_MAX_K, K);
     if (V < 2 || V > SPEC_MAX_V) return fail(SPEC_ERR_UNSUPPORTED, "V must be in [2, %d] (got %d)", SPEC_MAX_V, V);
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_UNSUPPORTED, "unknown dtype %d", dtype);
@@ -1720,6 +1728,8 @@ int spec_get_device_status(const void *workspace, int32_t *status_out) {
 }
 
 
+uint32_t spec_debug_set_wait_limit(uint32_t polls) { return g_wait_limit.exchange(polls); }
+
 // Allocation-free variant of spec_verify: the workspace is the library's
 // static scratch array instead of caller memory. The host-side name of that
 // array is not a device address, so its address is looked up once per device
@@ -1757,6 +1767,27 @@ int spec_verify_static(const spec_verify_params *p, const void *target_logits, c
     // spec_verify zeroes the counters it needs (cudaMemsetAsync, no allocation)
     return spec_verify(p, target_logits, draft_logits, draft_tokens, uniforms, out_tokens, accepted_len,
                        pos_stats, est_params, feature, conf, ws, kStaticScratchBytes, stream);
+}
+
+// Status word of the last static call on the current device: read straight
+// from the static array through its looked-up device address (no allocation).
+int spec_static_device_status(int32_t *status_out) {
+    g_err.clear();
+    if (!status_out) return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(SPEC_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_static_mu);
+        ws = g_static_ptr[dev];
+    }
+    if (!ws) {
+        *status_out = SPEC_OK;   // no static call on this device yet
+        return SPEC_OK;
+    }
+    return spec_get_device_status(ws, status_out);
 }
 
 }  // extern "C"

@@ -245,3 +245,29 @@ def test_python_binding_rejects_bad_tensors():
     zt = torch.zeros((2, 3, 8))                      # CPU tensor: refused before the ABI
     with pytest.raises(ValueError):
         sv.verify(zt, None, torch.zeros((2, 2), dtype=torch.int32), None, mode="greedy")
+
+
+@pytest.mark.parametrize("B", [(1 << 24) + 1, 1 << 25, 700_000_000])
+def test_batches_beyond_the_limit_are_refused(L, B):
+    """B > SPEC_MAX_B (2^24) is refused on the host, in every mode, before any
+    pointer is used: the draw record of the stochastic rule packs the
+    sequence index as 64 b + 2 n + bonus in a 32-bit int, which would
+    overflow at B >= 2^25. spec_workspace_size returns 0 for such B."""
+    for mode in ("stochastic", "greedy", "fly"):
+        p = _params(B=B, K=1, V=2, mode=mode)
+        assert L.spec_workspace_size(ctypes.byref(p)) == 0
+        assert _call(L, p) == sv.api.SPEC_ERR_UNSUPPORTED
+        assert b"B must be <=" in L.spec_last_error()
+    assert L.spec_confidence_workspace_size(B, 1, 2, sv.F32) == 0
+    ok = _params(B=1 << 24, K=1, V=2)
+    assert L.spec_workspace_size(ctypes.byref(ok)) > 0
+
+
+def test_wait_limit_hook_round_trips(L):
+    prev = L.spec_debug_set_wait_limit(123)
+    try:
+        assert prev == 1 << 20
+        assert L.spec_debug_set_wait_limit(0) == 123
+    finally:
+        L.spec_debug_set_wait_limit(prev)
+    assert L.spec_debug_set_wait_limit(prev) == prev
