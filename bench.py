@@ -33,6 +33,23 @@ UNIT = "positions/s"
 KERNEL_SOURCES = ("speculative_decoding_token_verify_gb300/csrc/spec_verify.cu",
                   "speculative_decoding_token_verify_gb300/csrc/spec_device.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_kernel_traffic.txt")
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (~8 TB/s)
+L2_BYTES = 129e6
+
+# the other configurations of the verification pass, timed alone in the
+# default run (spec_verify only, inputs resident): (workload name, mode)
+CONFIG_POINTS = (
+    ("tiny_B4_K4_V1024_f32", "stochastic"),
+    ("tiny_B4_K4_V1024_f32", "greedy"),
+    ("llama3vocab_B64_K5_V128256_bf16", "stochastic"),
+    ("fly_B128_K15_V152064_bf16", "fly"),
+    ("sweep_B32_K4_V32000_bf16", "stochastic"),
+    ("sweep_B32_K8_V128256_bf16", "stochastic"),
+    ("sweep_B128_K8_V128256_bf16", "stochastic"),
+    ("sweep_B512_K8_V152064_bf16", "stochastic"),
+    ("sweep_B128_K4_V152064_f32", "stochastic"),
+    ("sweep_B1024_K8_V152064_f32", "stochastic"),
+)
 
 
 def parse_args():
@@ -61,6 +78,8 @@ def parse_args():
                     help="also time the IRLS refit entry points (spec_irls_*) on this workload's B, K")
     ap.add_argument("--confidence", action="store_true",
                     help="also time the draft-only confidence pass (spec_confidence) on this workload's draft rows")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration timings (C1, C2, C4 and six sweep points)")
     ap.add_argument("--sweep", action="store_true",
                     help="time spec_verify alone at every point of the throughput sweep (B x K x V x dtype, "
                          "stochastic) and print one JSON line per point instead of the step line")
@@ -244,6 +263,16 @@ def cpu_baseline(w, seed, target_s=1.0):
                       f"sequences, {cores} threads, {dt:.2f} s wall)"}
 
 
+def step_config(w, world):
+    """The `config` object of the step line, shared by both arms."""
+    logit_bytes = w.logit_bytes(w.mode == "stochastic" or w.with_confidence)
+    l2_note = ("inputs larger than L2 (%.2f GB of logits per step, L2 129 MB)" % (logit_bytes / 1e9)
+               if logit_bytes > 2 * L2_BYTES else "L2 flushed between steps")
+    return {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
+            "mode": w.mode + ("+confidence+estimator_update" if w.with_confidence else ""),
+            "l2": l2_note, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args, w, world, rank, pg):
     import oracle
 
@@ -265,8 +294,9 @@ def run_reference(args, w, world, rank, pg):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
-                   "mode": w.mode, "step_sample_sequences": n_seq},
+        "config": step_config(w, world),
+        "sample": f"each step: the oracle's full step (verification, confidences, estimator update) on "
+                  f"the first {n_seq} of {w.B} sequences of {w.name}",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"each step: first {n_seq} of {w.B} sequences of {w.name}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -341,12 +371,18 @@ def run_ours(args, w, world, rank, local, pg):
         out["feature"] = torch.empty((w.B, w.K), dtype=torch.float32, device=dev)
         out["conf"] = torch.empty((w.B, w.K), dtype=torch.float32, device=dev)
 
+    nvtx = torch.cuda.nvtx
+
     def step(zt_, zd_, x_, u_):
+        nvtx.range_push("spec_verify")
         sv.verify(zt_, zd_, x_, u_, mode=w.mode, fly_theta=w.fly_theta, fly_window=w.fly_window,
                   est_params=est if w.with_confidence else None, out=out, workspace=ws,
                   want_feature=w.with_confidence, want_conf=w.with_confidence)
+        nvtx.range_pop()
         if w.with_confidence:
+            nvtx.range_push("spec_estimator_update")
             sv.estimator_update(out["feature"], out["accepted_len"], est, w.estimator_lr)
+            nvtx.range_pop()
 
     launches_per_step = 2 if w.with_confidence else 1
     for _ in range(args.warmup):
@@ -354,10 +390,8 @@ def run_ours(args, w, world, rank, local, pg):
     torch.cuda.synchronize(dev)
 
     logit_bytes = w.logit_bytes(with_draft)
-    l2_note = ("inputs larger than L2 (%.2f GB of logits per step, L2 129 MB)" % (logit_bytes / 1e9)
-               if logit_bytes > 2 * 129e6 else "L2 flushed between steps")
     flush = None
-    if logit_bytes <= 2 * 129e6:
+    if logit_bytes <= 2 * L2_BYTES:
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     clocks = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
@@ -418,12 +452,11 @@ def run_ours(args, w, world, rank, local, pg):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
-                   "mode": w.mode + ("+confidence+estimator_update" if w.with_confidence else ""),
-                   "l2": l2_note, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": step_config(w, world),
         "hbm_gbs": logit_bytes * world * args.steps / (total_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "frac": achieved / peak, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS, "traffic": recorded_traffic(w.name),
                      "kernel": verify_kernel_name(w),
                      "algorithmic_bytes_per_launch": logit_bytes,
                      "kernel_ms_mean": kern_s * 1e3, "kernel_ms_median": statistics.median(verify_ms),
@@ -447,6 +480,10 @@ def run_ours(args, w, world, rank, local, pg):
                                          kern_s * 1e3, top_p=args.top_p)
     if args.confidence and zd is not None:
         line["confidence"] = time_confidence(w, zd, est, dev, stream, peak)
+    if not args.no_configs and world == 1:
+        del inp
+        torch.cuda.empty_cache()
+        line["configs"] = time_configs(dev, stream, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
     if rank == 0:
@@ -629,6 +666,72 @@ def time_confidence(w, zd, est, dev, stream, peak, reps=100):
     mean_ms = st.mean(ms)
     return {"ms_mean": mean_ms, "ms_median": st.median(ms), "algorithmic_bytes": nbytes,
             "frac": nbytes / (mean_ms / 1e3) / 1e9 / peak, "kernel": "verify_kernel<T, 0, 1> (draft rows only, staging-buffer ring)"}
+
+
+def time_configs(dev, stream, peak, reps=50):
+    """spec_verify alone on each configuration of CONFIG_POINTS, inputs
+    resident in HBM, CUDA events around each call on the launching stream
+    (an L2 flush before each call where the logits are under twice the L2
+    size). The tiny workload is launch-bound: its calls are timed back to back
+    with the stream held while the host enqueues them (device time per
+    call). Each entry: kernel time, GB/s, positions/s and the fractions of the
+    measured and the nominal HBM bandwidth."""
+    import torch
+
+    import speculative_decoding_token_verify_gb300 as sv
+    import workloads
+
+    sweep = {w.name: w for w in workloads.sweep()}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    for k, (name, mode) in enumerate(CONFIG_POINTS):
+        w = workloads.WORKLOADS.get(name) or sweep[name]
+        inp = workloads.make_inputs(w, 1000 + k, dev)
+        with_draft = mode == "stochastic"
+        zd = inp["zd"] if with_draft else None
+        u = inp["u"] if mode == "stochastic" else None
+        ws = sv.Workspace(dev)
+        out = {"out_tokens": torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev),
+               "accepted_len": torch.empty((w.B,), dtype=torch.int32, device=dev)}
+        nbytes = w.logit_bytes(with_draft)
+
+        def call():
+            sv.verify(inp["zt"], zd, inp["x"], u, mode=mode, fly_theta=w.fly_theta, fly_window=w.fly_window,
+                      out=out, workspace=ws)
+
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize(dev)
+        if nbytes < 4 << 20:
+            us = device_us(call, stream, 200)
+            ms = [us / 1e3]
+            timing = "launch-bound: 200 back-to-back calls, device time per call"
+        else:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            small = nbytes <= 2 * L2_BYTES
+            for a, b in ev:
+                if small:
+                    flush.add_(1)
+                a.record(stream)
+                call()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = [a.elapsed_time(b) for a, b in ev]
+            timing = ("L2 flushed before each call" if small else "inputs larger than L2") + f", {reps} calls"
+        mean_s = statistics.mean(ms) / 1e3
+        gbs = nbytes / mean_s / 1e9
+        t = "__nv_bfloat16" if w.dtype == "bf16" else "float"
+        res[f"{name}:{mode}"] = {
+            "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype, "mode": mode,
+            "rows": "target + draft" if with_draft else "target only",
+            "kernel_ms_mean": mean_s * 1e3, "kernel_ms_median": statistics.median(ms),
+            "positions_per_s": w.B * w.K / mean_s, "hbm_gbs": gbs, "algorithmic_bytes": nbytes,
+            "frac": gbs / peak, "frac_nominal": gbs / NOMINAL_HBM_GBS,
+            "kernel": f"verify_kernel<{t}, 0, {0 if mode == 'stochastic' else 1}>", "timing": timing,
+            "status": sv.device_status(ws.buf)}
+        del inp, zd, u, ws, out
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_sweep(args):
