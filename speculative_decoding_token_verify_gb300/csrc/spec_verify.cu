@@ -176,6 +176,7 @@ struct Args {
     float *slices;           // [B][sstride] residual mass per slice
     float *gx;               // [B][2K] logits at the draft tokens: target rows, then draft rows
     unsigned spin_limit;     // polls of a residual wait before SPEC_ERR_TIMEOUT
+    int need_ent;            // target rows carry the entropy moment (pos_stats requested, or FLy)
 };
 
 __device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
@@ -677,9 +678,11 @@ __device__ __forceinline__ float slice_lane_sum(const Args &a, const T *tr, cons
     return sum8(r);
 }
 
-// Stage slice sums c0 .. c0 + 32*kScanPer - 1 of one sequence (row start
-// 16-byte aligned) in the warp's buffer; lane l then owns the contiguous run
-// l*kScanPer .. of the chunk. Entries past n are not staged and read as 0.
+// Stage slice sums c0 .. c0 + 32*kScanPer - 1 of one sequence (the row of
+// slice sums starts 16-byte aligned and is padded to a multiple of 4) in the
+// warp's buffer, with copies that hold no registers; lane l then owns the
+// contiguous run l*kScanPer .. of the chunk. Nothing past the row's padding
+// is read; entries at or past n read back as 0 (run_get).
 __device__ __forceinline__ void stage_issue(const float *ss, int n, int c0, int l, float4 *buf) {
     const int cn = min(4 * kStage, n - c0);
     const float4 *src = reinterpret_cast<const float4 *>(ss + c0);
@@ -691,16 +694,29 @@ __device__ __forceinline__ void stage_slices(const float *ss, int n, int c0, int
     __syncwarp();
 }
 
-__device__ __forceinline__ float staged(const float4 *buf, int i, int cn) {
-    return i < cn ? reinterpret_cast<const float *>(buf)[i] : 0.f;
+// group j (4 values) of lane l's staged run, entries at or past cn as 0
+__device__ __forceinline__ float4 run_get(const float4 *buf, int l, int j, int cn) {
+    const int i = l * kScanPer + 4 * j;
+    float4 v = i < cn ? buf[i / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i + 1 >= cn) v.y = 0.f;
+    if (i + 2 >= cn) v.z = 0.f;
+    if (i + 3 >= cn) v.w = 0.f;
+    return v;
 }
 
 // fp32 sum of lane l's run of the staged chunk, in ascending order (at most
-// kScanPer terms: relative error below 2e-6 of the run, so below 2e-6 of Z)
+// kScanPer terms: relative error below 2e-6 of the run, so below 2e-6 of Z);
+// read 16 bytes at a time
 __device__ __forceinline__ float run_sum(const float4 *buf, int l, int cn) {
     float seg = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < kScanPer; ++j) seg += staged(buf, l * kScanPer + j, cn);
+#pragma unroll 2
+    for (int j = 0; j < kScanPer / 4; ++j) {
+        const float4 v = run_get(buf, l, j, cn);
+        seg += v.x;
+        seg += v.y;
+        seg += v.z;
+        seg += v.w;
+    }
     return seg;
 }
 
@@ -744,7 +760,7 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
             stage_slices(ss, n, c0, l, buf);
         }
         Z += warp_sum_f(run_sum(buf, l, n - c0));
-        __syncwarp();
+        if (n > kChunk) __syncwarp();
     }
     if (!(Z > 0.f)) return -1;
     const float target = d.u * Z;
@@ -764,13 +780,18 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
         float c = 0.f;
         int found = -1;
         float Pf = 0.f;
-        for (int j = 0; j < kScanPer; ++j) {
-            const float prev = c;
-            c += staged(buf, l * kScanPer + j, cn);
-            if (c > rel) {
-                found = c0 + l * kScanPer + j;
-                Pf = excl + prev;
-                break;
+#pragma unroll 1
+        for (int j = 0; j < kScanPer / 4; ++j) {
+            const float4 v = run_get(buf, l, j, cn);
+            const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float prev = c;
+                c += e[i];
+                if (found < 0 && c > rel) {
+                    found = c0 + l * kScanPer + 4 * j + i;
+                    Pf = excl + prev;
+                }
             }
         }
         const unsigned m = __ballot_sync(kFull, found >= 0);
@@ -790,8 +811,14 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
             __syncwarp();
             stage_slices(ss, n, c0, l, buf);
             int lm = -1;
-            for (int j = 0; j < kScanPer; ++j)
-                if (staged(buf, l * kScanPer + j, n - c0) > 0.f) lm = l * kScanPer + j;
+#pragma unroll
+            for (int j = 0; j < kScanPer / 4; ++j) {
+                const float4 v = run_get(buf, l, j, n - c0);
+                if (v.x > 0.f) lm = l * kScanPer + 4 * j;
+                if (v.y > 0.f) lm = l * kScanPer + 4 * j + 1;
+                if (v.z > 0.f) lm = l * kScanPer + 4 * j + 2;
+                if (v.w > 0.f) lm = l * kScanPer + 4 * j + 3;
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(kFull, lm, o));
             if (lm >= 0) entry = c0 + lm;
@@ -1166,7 +1193,9 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             const int kb = verified(a, g.b);
             skip = g.target ? g.r > kb : g.r - a.nt_rows >= kb;
         }
-        // target rows also carry the entropy moment; draft rows do not need it
+        // target rows carry the entropy moment when something reads it
+        // (pos_stats, or FLy's gate); draft rows never need it
+        const bool ent = g.target && a.need_ent;
         RowAcc s = acc_empty();
         if constexpr (kTemp) {
           if (!a.pre) {
@@ -1174,11 +1203,11 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             const float sc = seq_inv_temp(a, g.b);
             const float sL = sc * kLog2e, rs = __fdiv_rn(kRescale, sc);   // exact for powers of two
             s = skip ? acc_empty()
-                     : (g.target ? unit_consume<T, true, true>(g, l, wbuf, sL, rs) : unit_consume<T, false, true>(g, l, wbuf, sL, rs));
+                     : (ent ? unit_consume<T, true, true>(g, l, wbuf, sL, rs) : unit_consume<T, false, true>(g, l, wbuf, sL, rs));
           }
         } else {
             s = skip ? acc_empty()
-                     : (g.target ? unit_consume<T, true, false, kRing>(g, l, wbuf) : unit_consume<T, false, false, kRing>(g, l, wbuf));
+                     : (ent ? unit_consume<T, true, false, kRing>(g, l, wbuf) : unit_consume<T, false, false, kRing>(g, l, wbuf));
         }
         const int b = g.b;
         unsigned old = 0u;
@@ -1435,6 +1464,8 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     a.res_units = a.mode == MODE_STOCHASTIC ? (unsigned)a.B * (unsigned)p.nR : 0u;
     a.inv_log_v = (float)(1.0 / std::log((double)a.V));
     a.spin_limit = g_wait_limit.load();
+    // the entropy moment of target rows feeds pos_stats and FLy's gate only
+    a.need_ent = (a.pos_stats != nullptr || a.mode == MODE_FLY) ? 1 : 0;
     int grid = 1;
     const bool temp = a.inv_temp != nullptr || a.pre;
     // the staging-buffer ring streams the launches with no draw
