@@ -83,6 +83,21 @@ namespace sv {
 #ifndef SV_LAZY_ROUNDS
 #define SV_LAZY_ROUNDS 4
 #endif
+// likewise the last SV_RES_LAZY x (resident warps) residual units, in 1/4
+// rounds (a unit held ahead by a warp still busy with another would wait
+// while idle warps run dry; at the queue's end those units carry the draw
+// chain of the last sequences)
+#ifndef SV_RES_LAZY
+#define SV_RES_LAZY 0
+#endif
+// words between consecutive published-draw flags (polled by waiting warps)
+#ifndef SV_READY_STRIDE
+#define SV_READY_STRIDE 1
+#endif
+// longest sleep between polls of a waiting warp (ns)
+#ifndef SV_POLL_NS_MAX
+#define SV_POLL_NS_MAX 256
+#endif
 
 constexpr int NT = SV_THREADS;         // threads per CTA (independent warps)
 constexpr int NWARP = NT / 32;
@@ -165,6 +180,7 @@ struct Args {
     unsigned *seq_done;      // [B] completed units per sequence
     float4 *part;            // [B][rows][nT] tile partials, one per stream unit
     unsigned res_units;      // B * nR in stochastic mode, else 0
+    unsigned res_lazy_from;  // residual units from here on are claimed when due, not one ahead
     int nR;                  // residual units per sequence
     int nslice;              // scan slices per row
     int sstride;             // slice sums per sequence in `slices` (nslice rounded up to 4)
@@ -638,7 +654,7 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
             } else {
                 a.slotrec[slot] = rec;
             }
-            st_release(a.res_ready + slot, 1u);
+            st_release(a.res_ready + (size_t)slot * SV_READY_STRIDE, 1u);
         }
         // K <= 31: lane j writes position j (lane j holds draft token j)
         if (l <= K && !(draw && l == n)) a.out_tokens[(size_t)b * (K + 1) + l] = l < n ? xi : (l == n ? am_n : -1);
@@ -1115,16 +1131,20 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
             q.pend = atomicAdd(a.ctr + CTR_RES_CLAIM, 1u);
         }
         if (q.pend >= a.res_units) return JOB_DONE;
-        if (ld_relaxed(a.res_ready + q.pend / (unsigned)a.nR)) {
+        if (ld_relaxed(a.res_ready + (size_t)(q.pend / (unsigned)a.nR) * SV_READY_STRIDE)) {
             fence_acquire();
             id = q.pend;
-            // the next unit is claimed now; its reply is read only when this
-            // unit is done
-            q.pend = atomicAdd(a.ctr + CTR_RES_CLAIM, 1u);
+            // the next unit is claimed now (its reply is read only when this
+            // unit is done), except by the warp running a draw's last unit
+            // (usually the one that completes it, and then locates the token:
+            // a unit held meanwhile would wait while idle warps run dry), and
+            // at the queue's end, where units are claimed when a warp is free
+            const bool last_part = id % (unsigned)a.nR == (unsigned)a.nR - 1u;
+            q.pend = !last_part && id + 1u < a.res_lazy_from ? atomicAdd(a.ctr + CTR_RES_CLAIM, 1u) : kNone;
             return JOB_RESIDUAL;
         }
         __nanosleep(ns);
-        ns = min(ns * 2u, 256u);
+        ns = min(ns * 2u, (unsigned)SV_POLL_NS_MAX);
     }
     raise_status(a, SPEC_ERR_TIMEOUT);
     return JOB_DONE;
@@ -1349,7 +1369,7 @@ static void plan_workspace(int B, int rows_a, int rows_b, int V, int esize, bool
     plan_tiles(B, rows_a, V, esize, draw, p);
     p.seq_off = kHeaderWords * sizeof(unsigned);
     p.ready_off = p.seq_off + (size_t)B * sizeof(unsigned);
-    p.done_off = p.ready_off + (size_t)B * sizeof(unsigned);
+    p.done_off = p.ready_off + (size_t)B * SV_READY_STRIDE * sizeof(unsigned);
     p.zero_bytes = p.done_off + (size_t)B * sizeof(unsigned);
     p.rec_off = align_up(p.zero_bytes, 16);
     p.part_off = align_up(p.rec_off + (size_t)2 * B * sizeof(float4), 16);
@@ -1475,6 +1495,8 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     if (rc != SPEC_OK) return rc;
     const unsigned long long lazy = (unsigned long long)SV_LAZY_ROUNDS * (unsigned long long)grid * NWARP;
     a.lazy_from = p.units > lazy ? (unsigned)(p.units - lazy) : 0u;
+    const unsigned long long res_lazy = (unsigned long long)SV_RES_LAZY * (unsigned long long)grid * NWARP / 4ull;
+    a.res_lazy_from = a.res_units > res_lazy ? (unsigned)(a.res_units - res_lazy) : 0u;
     cudaError_t e = cudaMemsetAsync(ws, 0, p.zero_bytes, st);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "workspace reset failed: %s", cudaGetErrorString(e));
     if (a.pre) {

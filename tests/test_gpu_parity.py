@@ -108,6 +108,16 @@ def test_workloads_full_size(wl):
                                                  g["accepted_len"].cpu().numpy(),
                                                  np.r_[1.0, np.zeros(w.K)], w.estimator_lr)
             np.testing.assert_allclose(p.cpu().numpy(), newp, rtol=1e-5, atol=1e-6)
+        # the benchmark's own launch asks for features and confidences only
+        # (no pos_stats): same bits as the launch checked above
+        b = hv.verify(inp["zt"], inp["zd"], inp["x"], inp["u"], est_params=est, want_feature=True,
+                      want_conf=est is not None)
+        torch.cuda.synchronize()
+        for k in ("out_tokens", "accepted_len", "feature") + (("conf",) if est is not None else ()):
+            x_, y_ = g[k], b[k]
+            if x_.dtype == torch.float32:
+                x_, y_ = x_.view(torch.int32), y_.view(torch.int32)
+            assert torch.equal(x_, y_), k
     print(w.name, s)
     hv.record(w.name, s)
 
@@ -321,6 +331,46 @@ def test_bad_token_and_bad_row_status():
     # a clean call resets the status word
     g = _run(_rand_inputs(B, K, V, "f32", seed=3), "stochastic")
     assert sv.device_status(g["_workspace"]) == 0
+
+
+@pytest.mark.parametrize("case", ["estimator", "masked_f32", "greedy_bf16", "fly_bf16", "temperature"])
+def test_outputs_do_not_depend_on_pos_stats(case):
+    """Target rows fold the entropy moment only when something reads it
+    (pos_stats, or FLy's gate). Tokens, accepted lengths, features and
+    confidences must be the same bits with and without pos_stats requested,
+    on ordinary, masked (-inf) and temperature-processed rows."""
+    kw = {}
+    if case == "estimator":
+        inp = workloads.make_inputs(workloads.ESTIMATOR.scaled(B=40), 7101, DEV)
+        mode, K = "stochastic", workloads.ESTIMATOR.K
+    elif case == "masked_f32":
+        inp = _rand_inputs(16, 4, 3000, "f32", seed=7102)
+        gen = torch.Generator(device=DEV).manual_seed(7)
+        inp["zt"] = inp["zt"].masked_fill(torch.rand(inp["zt"].shape, generator=gen, device=DEV) < 0.3,
+                                          float("-inf"))
+        mode, K = "stochastic", 4
+    elif case == "greedy_bf16":
+        inp = _rand_inputs(24, 6, 50000, "bf16", seed=7103)
+        mode, K = "greedy", 6
+    elif case == "fly_bf16":
+        inp = workloads.make_inputs(workloads.FLY.scaled(B=16), 7104, DEV)
+        mode, K = "fly", workloads.FLY.K
+        kw = dict(fly_theta=0.3, fly_window=6)
+    else:
+        w = workloads.ESTIMATOR.scaled(B=24, inv_temp_range=(0.5, 2.0))
+        inp = workloads.make_inputs(w, 7105, DEV)
+        mode, K = "stochastic", w.K
+        kw = dict(inv_temperature=inp["inv_temp"])
+    est = _est(K)
+    u = inp["u"] if mode == "stochastic" else None
+    runs = [hv.verify(inp["zt"], inp["zd"], inp["x"], u, mode=mode, est_params=est, want_pos_stats=ps,
+                      want_feature=True, want_conf=True, **kw) for ps in (True, False)]
+    torch.cuda.synchronize()
+    for k in ("out_tokens", "accepted_len", "feature", "conf"):
+        a, b = runs[0][k], runs[1][k]
+        if a.dtype == torch.float32:
+            a, b = a.view(torch.int32), b.view(torch.int32)
+        assert torch.equal(a, b), k
 
 
 def test_a_residual_wait_that_runs_out_sets_timeout():
