@@ -44,6 +44,12 @@
  *    SPEC_ERR_BAD_TOKEN in the status word.
  *  - Outputs are deterministic: the same inputs give the same bits on every
  *    run (fixed reduction orders, no floating-point atomics).
+ *  - Checked builds (compiled with SPEC_CHECKED, libspecverify_checked.so)
+ *    export the same calls with the same results; their kernels also check
+ *    every index they derive (work item, sequence, row, tile, draw slot,
+ *    slice, token) against the buffer it addresses before the access, and
+ *    on a failed check skip the access and raise SPEC_ERR_INDEX in the
+ *    status word. They are for testing; the default build has no checks.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -64,6 +70,7 @@ extern "C" {
 #define SPEC_ERR_BAD_ROW 5       /* device status: a row had no finite logit */
 #define SPEC_ERR_BAD_TOKEN 6     /* device status: a draft token was outside [0,V) */
 #define SPEC_ERR_BAD_TEMPERATURE 7 /* device status: an inverse temperature was out of range */
+#define SPEC_ERR_INDEX 8         /* device status, checked builds only: an index check failed */
 
 /* limits */
 #define SPEC_MAX_B (1 << 24)     /* sequences per call                      */

@@ -18,6 +18,9 @@ _ROOT = os.path.dirname(_PKG)
 _CSRC = os.path.join(_PKG, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+# the same library with the kernels' index checks compiled in (SPEC_CHECKED);
+# for tests
+CHECKED_LIB_PATH = os.path.join(_PKG, "libspecverify_checked.so")
 SOURCES = ("spec_verify.cu", "spec_nucleus.cu", "spec_estimator.cu", "spec_irls.cu", "spec_av.cu", "spec_ngram.cu")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -32,27 +35,36 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: cannot build libspecverify.so")
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = True) -> str:
     """Compile the CUDA sources (in parallel, one object each) and link the
-    shared library next to this file. Returns its path."""
+    shared library next to this file; with `checked`, the checked variant
+    (SPEC_CHECKED) as well, from the same nvcc run. Returns the library's
+    path."""
     srcs = [os.path.join(_CSRC, s) for s in SOURCES]
     deps = srcs + [os.path.join(_CSRC, "spec_device.cuh"), os.path.join(_CSRC, "spec_nucleus.cuh"),
             os.path.join(_INCLUDE, "spec_verify.h")]
-    if (not force and os.path.exists(LIB_PATH)
-            and os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps)):
+    targets = [(LIB_PATH, [])] + ([(CHECKED_LIB_PATH, ["-DSPEC_CHECKED"])] if checked else [])
+    newest = max(os.path.getmtime(d) for d in deps)
+    targets = [(path, flags) for path, flags in targets
+               if force or not os.path.exists(path) or os.path.getmtime(path) < newest]
+    if not targets:
         return LIB_PATH
     nvcc = _nvcc()
     common = ["-O3", "-std=c++17", *ARCH_FLAGS, "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=default", f"-I{_INCLUDE}", f"-I{_CSRC}", *extra_flags]
     if verbose:
         common += ["-Xptxas", "-v"]
-    objs, procs = [], []
     tag = f"{os.getpid()}"
-    for s in srcs:
-        o = os.path.join(_CSRC, os.path.basename(s) + f".{tag}.o")
-        objs.append(o)
-        procs.append(subprocess.Popen([nvcc, *common, "-c", s, "-o", o],
-                                      stdout=subprocess.PIPE, stderr=subprocess.STDOUT))
+    jobs = []   # (target, objects)
+    procs = []
+    for k, (path, flags) in enumerate(targets):
+        objs = []
+        for s in srcs:
+            o = os.path.join(_CSRC, os.path.basename(s) + f".{tag}.{k}.o")
+            objs.append(o)
+            procs.append(subprocess.Popen([nvcc, *common, *flags, "-c", s, "-o", o],
+                                          stdout=subprocess.PIPE, stderr=subprocess.STDOUT))
+        jobs.append((path, objs))
     logs = []
     ok = True
     for p in procs:
@@ -62,13 +74,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     try:
         if not ok:
             raise RuntimeError("nvcc failed:\n" + "\n".join(logs))
-        tmp = LIB_PATH + f".{tag}.tmp"
-        subprocess.check_call([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB_PATH)
+        for path, objs in jobs:
+            tmp = path + f".{tag}.tmp"
+            subprocess.check_call([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs])
+            os.replace(tmp, path)
     finally:
-        for o in objs:
-            if os.path.exists(o):
-                os.remove(o)
+        for _, objs in jobs:
+            for o in objs:
+                if os.path.exists(o):
+                    os.remove(o)
     if verbose:
         print("\n".join(logs))
     return LIB_PATH
@@ -137,13 +151,32 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(
                 f"{LIB_PATH} is missing: build it first "
                 "(python -c 'import __graft_entry__ as g; g.build()')")
-        L = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+def _load(path):
+    L = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
+_checked = None
+
+
+def lib_checked() -> ctypes.CDLL:
+    """The checked variant (index checks in the kernels), for tests. Raises if
+    it has not been built."""
+    global _checked
+    with _lock:
+        if _checked is None:
+            if not os.path.exists(CHECKED_LIB_PATH):
+                raise RuntimeError(f"{CHECKED_LIB_PATH} is missing: build it first")
+            _checked = _load(CHECKED_LIB_PATH)
+    return _checked
 
 
 def last_error() -> str:

@@ -26,6 +26,7 @@ SPEC_ERR_TIMEOUT = 4
 SPEC_ERR_BAD_ROW = 5
 SPEC_ERR_BAD_TOKEN = 6
 SPEC_ERR_BAD_TEMPERATURE = 7
+SPEC_ERR_INDEX = 8
 MAX_K = 31
 MAX_V = 1 << 20
 

@@ -193,6 +193,7 @@ struct Args {
     float *gx;               // [B][2K] logits at the draft tokens: target rows, then draft rows
     unsigned spin_limit;     // polls of a residual wait before SPEC_ERR_TIMEOUT
     int need_ent;            // target rows carry the entropy moment (pos_stats requested, or FLy)
+    unsigned part_cap;       // tile-partial slots in the workspace
 };
 
 __device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
@@ -234,6 +235,19 @@ __device__ __forceinline__ int verified(const Args &a, int b) {
 __device__ __forceinline__ void raise_status(const Args &a, unsigned code) {
     atomicMax(a.ctr + CTR_STATUS, code);
 }
+
+// Checked builds (SPEC_CHECKED): structural index checks before the accesses
+// they guard; a failed check raises SPEC_ERR_INDEX and the access is
+// skipped. Other builds compile the checks away.
+#ifdef SPEC_CHECKED
+__device__ __forceinline__ bool sv_ok(const Args &a, bool cond) {
+    if (!cond) raise_status(a, SPEC_ERR_INDEX);
+    return cond;
+}
+#define SV_OK(a, cond) sv_ok((a), (cond))
+#else
+#define SV_OK(a, cond) true
+#endif
 
 // inverse temperature of sequence b; outside [SPEC_MIN_INV_TEMPERATURE,
 // SPEC_MAX_INV_TEMPERATURE] (or NaN) the sequence runs at s = 1, and its
@@ -465,9 +479,10 @@ __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *
     const int nT = b < a.B1 ? a.nT : a.nT2;
     const int rc = min(kStage / nT, 32);       // whole rows per staging pass, one lane each at least
     const float4 *base = a.part + seq_base(a, b);
-    const int drow = a.nt_rows + l;            // row index of lane l's draft row
     tr = acc_empty();
     dr = acc_empty();
+    if (!SV_OK(a, nT >= 1 && nT <= kStage && seq_base(a, b) + (unsigned)(a.rows * nT) <= a.part_cap)) return;
+    const int drow = a.nt_rows + l;            // row index of lane l's draft row
     for (int r0 = 0; r0 < a.rows; r0 += rc) {
         const int rn = min(rc, a.rows - r0);
         const int cnt = rn * nT;
@@ -501,7 +516,7 @@ __device__ __forceinline__ void merge_rows(const Args &a, int b, int l, float4 *
 template <typename T>
 __device__ __noinline__ void gather_tokens(const Args &a, int b, int l) {
     const int K = a.K;
-    if (l < verified(a, b)) {
+    if (SV_OK(a, b >= 0 && b < a.B) && l < verified(a, b)) {
         const int xv = __ldg(a.x + (size_t)b * K + l);
         if (xv >= 0 && xv < a.V) {
             const float zt = Elem<T>::load(trow_ptr<T>(a, b, l) + xv);
@@ -524,6 +539,7 @@ __device__ __noinline__ void gather_tokens(const Args &a, int b, int l) {
 template <typename T, bool kTemp>
 __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) {
     const int K = a.K;
+    if (!SV_OK(a, b >= 0 && b < a.B)) return;
     float sc = 1.f;
     if constexpr (kTemp) {
         if (a.inv_temp) {
@@ -643,7 +659,7 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
         }
         const int am_n = __shfl_sync(kFull, amax_t, n);
         const float u_draw = __shfl_sync(kFull, ui, K);
-        if (draw && l == kSig) {
+        if (draw && l == kSig && SV_OK(a, slot < (unsigned)a.B)) {
             // hand the draw to the residual units of b before any other
             // output goes out, so that the release waits on the record
             // alone; the release store orders the record before the flag
@@ -957,7 +973,7 @@ __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T 
 #pragma unroll
             for (int i = 0; i < kResBatch; ++i) {
                 const float sm = warp_sum_f(part[i]);
-                if (l == kSig) a.slices[(size_t)b * a.sstride + s0 + i] = sm;
+                if (l == kSig && SV_OK(a, s0 + i < a.nslice)) a.slices[(size_t)b * a.sstride + s0 + i] = sm;
             }
             cp_async_wait();
             if (dr) batch_staged_bf16<true, kTemp>(buf, l, d, part);
@@ -965,7 +981,7 @@ __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T 
 #pragma unroll
             for (int i = 0; i < kResBatch; ++i) {
                 const float sm = warp_sum_f(part[i]);
-                if (l == kSig) a.slices[(size_t)b * a.sstride + s1 + i] = sm;
+                if (l == kSig && SV_OK(a, s1 + i < a.nslice)) a.slices[(size_t)b * a.sstride + s1 + i] = sm;
             }
             __syncwarp();   // the buffer is reused by the next staged job
             return;
@@ -1038,6 +1054,10 @@ __device__ __noinline__ void locate(const Args &a, int slot, int b_known, int l,
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
     if (b != b_known) cp_async_wait_all();   // never (a slot names one sequence): restage safely
+    if (!SV_OK(a, b >= 0 && b < a.B && b == b_known && d.n >= 0 && d.n <= a.K)) {
+        cp_async_wait_all();
+        return;
+    }
     int token = locate_scan<T, kTemp>(a, b, tr, dr, d, l, buf, b == b_known);
     if (token < 0 && dr != nullptr) {
         for (int s0 = 0; s0 < a.nslice; s0 += res_slices<T>()) unit_sums<T, kTemp>(a, b, s0, tr, nullptr, d, l, buf);
@@ -1049,7 +1069,7 @@ __device__ __noinline__ void locate(const Args &a, int slot, int b_known, int l,
         if (l == 0) raise_status(a, SPEC_ERR_BAD_ROW);
         token = 0;
     }
-    if (l == 0) a.out_tokens[(size_t)b * (K + 1) + d.n] = token;
+    if (l == 0 && SV_OK(a, token >= 0 && token < a.V)) a.out_tokens[(size_t)b * (K + 1) + d.n] = token;
 }
 
 // One residual unit: part t of the sequence published in slot id / nR. Lane
@@ -1067,6 +1087,14 @@ __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l,
     const int t = (int)(id - (unsigned)slot * (unsigned)a.nR);
     int b;
     const Draw d = decode_slot<kTemp>(a, slot, b);
+    if (!SV_OK(a, slot >= 0 && slot < a.B && b >= 0 && b < a.B && d.n >= 0 && d.n <= a.K &&
+                      t * res_slices<T>() < a.nslice)) {
+        ResDone bad;
+        bad.slot = slot;
+        bad.b = 0;
+        bad.old = 0xffffffffu;   // never the last unit: nothing follows
+        return bad;
+    }
     const T *tr = trow_ptr<T>(a, b, d.n);
     const T *dr = d.bonus ? nullptr : drow_ptr<T>(a, b, d.n);
     unit_sums<T, kTemp>(a, b, t * res_slices<T>(), tr, dr, d, l, buf);
@@ -1197,6 +1225,7 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
         }
         if (kind == JOB_DONE) break;
         if (kind == JOB_RESIDUAL) {
+            if (!SV_OK(a, unit < a.res_units)) continue;
             const ResDone r = residual_unit<T, kTemp>(a, unit, l, wbuf);
             due = DUE_RESIDUAL;
             due_id = r.slot;
@@ -1205,6 +1234,9 @@ __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a)
             continue;
         }
         const UnitGeo<T> g = unit_geo<T>(a, unit);
+        if (!SV_OK(a, unit < a.units && unit < a.part_cap && g.b >= 0 && g.b < a.B && g.r >= 0 && g.r < a.rows &&
+                          g.v0 >= 0 && g.head >= 0 && g.tail >= 0 && g.ve + g.tail <= a.V))
+            continue;
         if (a.gx && unit == seq_base(a, g.b)) gather_tokens<T>(a, g.b, l);
         // rows a pruned batch never verified are not read (their partial is
         // empty; the unit still counts toward its sequence's completion)
@@ -1453,6 +1485,7 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     a.res_done = reinterpret_cast<unsigned *>(base + p.done_off);
     a.slotrec = reinterpret_cast<float4 *>(base + p.rec_off);
     a.part = reinterpret_cast<float4 *>(base + p.part_off);
+    a.part_cap = (unsigned)((p.slice_off - p.part_off) / sizeof(float4));
     a.slices = reinterpret_cast<float *>(base + p.slice_off);
     // draft-token logits are gathered wherever the finalize forms log-ratios
     a.gx = (a.mode != MODE_CONF && a.nd_rows > 0) ? reinterpret_cast<float *>(base + p.gx_off) : nullptr;

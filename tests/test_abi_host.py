@@ -40,6 +40,17 @@ def test_every_declared_symbol_is_exported(L):
     assert "spec_internal_set_error" not in exported
 
 
+def test_checked_build_exports_the_same_calls(L):
+    """The checked variant (index checks in the kernels) exports every call
+    the header declares, like the default build."""
+    _native.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", _native.CHECKED_LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (spec_\w+)", out))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, f"declared but not exported by the checked build: {missing}"
+
+
 def test_params_struct_layout_matches_header():
     prog = r"""
 #include <stdio.h>
