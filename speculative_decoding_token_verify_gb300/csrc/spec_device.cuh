@@ -28,13 +28,19 @@
 // raw logit units (s does not move the argmax); R and T are sums over the
 // processed exponents y_v = (z_v - M) s log2e. Every function below takes the
 // exponent scale sL = s log2e (default log2e, s = 1); then lse = s M + ln(1+R)
-// and h and logit(q_max) keep their formulas. With kSub the exponents are
-// formed difference first, (z - ref) sL, instead of z sL - ref sL: the
-// latter rounds ref sL once per reference, an offset shared by every term
-// whose size grows with |s ref| (6e-5 at s = 100 and logits near 10), while
-// z - ref is exact near the maximum (Sterbenz). The temperature variant uses
-// kSub; at s = 1 with ordinary logits the fused form is as accurate and one
-// instruction shorter.
+// and h and logit(q_max) keep their formulas.
+//
+// Exponents in the streaming loop are one fused multiply-add each,
+// fma(z, sL, -fl(ref sL)): the product z sL is exact inside the FMA, so the
+// only error beyond the final rounding is the rounding of ref sL itself,
+// eps = ref sL - fl(ref sL), an offset shared by every term taken against
+// that reference (it grows with |s ref|: 6e-5 at s = 100 and logits near
+// 10). eps is exact by another FMA, fma(ref, sL, -fl(ref sL)), and the
+// accumulator folds it into the exponent of each change of reference and of
+// the final scale, so the sums come out as if every exponent had been exact:
+// the same accuracy as forming z - ref first, at one instruction per pair of
+// logits instead of two. With kSub the scalar folds (acc_chunk) form
+// differences first.
 #pragma once
 
 #include <cstdint>
@@ -245,7 +251,8 @@ constexpr float kMaskF32 = -1.0e30f;
 
 struct StreamAcc {
     float mr;    // reference logit
-    float mrL;   // mr * sL
+    float mrL;   // fl(mr * sL)
+    float eps;   // mr * sL - mrL, exact (the offset every exponent against mr carries)
     float mrh;   // mr + rs, rs = kRescale / s (a chunk max above it moves the reference)
     float S;     // sum of 2^{(z - mr) log2e} over chunks other than the best one
     float C;     // the same sum over the best chunk
@@ -259,6 +266,7 @@ __device__ __forceinline__ StreamAcc stream_init(float sL = kLog2e, float rs = k
     StreamAcc s;
     s.mr = kMaskFloor;
     s.mrL = kMaskFloor * sL;
+    s.eps = fmaf(kMaskFloor, sL, -s.mrL);
     s.mrh = kMaskFloor + rs;
     s.S = 0.f;
     s.C = 0.f;
@@ -269,20 +277,26 @@ __device__ __forceinline__ StreamAcc stream_init(float sL = kLog2e, float rs = k
     return s;
 }
 
+// Move the reference to c. The sums carry 2^eps_old (and T also eps_old S);
+// rescaled with the exponent d = (mr - c) sL + eps_c - eps_old they carry
+// 2^eps_c, like the terms taken against c from now on.
 __device__ __forceinline__ void stream_rescale(StreamAcc &s, float c, float sL, float rs) {
-    const float d = (s.mr - c) * sL;
+    const float cL = c * sL;
+    const float ce = fmaf(c, sL, -cL);
+    const float d = fmaf(s.mr - c, sL, ce - s.eps);
     const float al = ex2(d);
     const float t = al * fmaf(d, s.S + s.C, s.T.x + s.T.y);
     s.T = make_float2(t, 0.f);
     s.S *= al;
     s.C *= al;
     s.mr = c;
-    s.mrL = c * sL;
+    s.mrL = cL;
+    s.eps = ce;
     s.mrh = c + rs;
 }
 
 // fold the exponentials of one chunk given as fp32 pairs
-template <int NP, bool kEnt, bool kSub>
+template <int NP, bool kEnt>
 __device__ __forceinline__ void stream_fold(StreamAcc &s, const float2 (&z)[NP], float c, int k, float sL,
                                             float rs) {
     if (c > s.mrh) stream_rescale(s, c, sL, rs);
@@ -295,8 +309,7 @@ __device__ __forceinline__ void stream_fold(StreamAcc &s, const float2 (&z)[NP],
     float2 y[NP];
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        if constexpr (kSub) y[p] = pfma(padd(z[p], make_float2(-s.mr, -s.mr)), L2, make_float2(0.f, 0.f));
-        else y[p] = pfma(z[p], L2, ml);
+        y[p] = pfma(z[p], L2, ml);
         e[p] = make_float2(ex2(y[p].x), ex2(y[p].y));
     }
     float2 a = e[0];
@@ -311,7 +324,7 @@ __device__ __forceinline__ void stream_fold(StreamAcc &s, const float2 (&z)[NP],
     s.C = nb ? cs : s.C;
 }
 
-template <typename T, bool kEnt, bool kSub = false>
+template <typename T, bool kEnt>
 __device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k, float sL = kLog2e,
                                              float rs = kRescale) {
     if constexpr (sizeof(T) == 2) {
@@ -328,7 +341,7 @@ __device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k, float
         z[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
         z[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
         z[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
-        stream_fold<4, kEnt, kSub>(s, z, c, k, sL, rs);
+        stream_fold<4, kEnt>(s, z, c, k, sL, rs);
     } else {
         float2 z[2];
         z[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
@@ -340,7 +353,7 @@ __device__ __forceinline__ void stream_chunk(StreamAcc &s, uint4 w, int k, float
             z[1].y = fmaxf(z[1].y, kMaskF32);
         }
         const float c = fmaxf(fmaxf(z[0].x, z[0].y), fmaxf(z[1].x, z[1].y));
-        stream_fold<2, kEnt, kSub>(s, z, c, k, sL, rs);
+        stream_fold<2, kEnt>(s, z, c, k, sL, rs);
     }
 }
 
@@ -411,7 +424,8 @@ __device__ __forceinline__ void load8(const T *row, int v, int V, bool vec_ok, f
 
 // Canonical RowAcc of one thread's streamed chunks; vector 0 of the tile has
 // row index `vb`.
-template <typename T, bool kSub = false>
+// The final scale's exponent d = (mr - bv) sL - eps takes the offset out.
+template <typename T>
 __device__ __forceinline__ RowAcc stream_finish(const StreamAcc &s, int vb, float sL = kLog2e) {
     constexpr int E = Elem<T>::kPerVec;
     RowAcc a = acc_empty();
@@ -425,8 +439,8 @@ __device__ __forceinline__ RowAcc stream_finish(const StreamAcc &s, int vb, floa
     float crest = 0.f;
 #pragma unroll
     for (int j = 0; j < E; ++j)
-        if (j != jf) crest += ex2(kSub ? (z[j] - s.mr) * sL : fmaf(z[j], sL, -s.mrL));
-    const float d = (s.mr - s.bv) * sL;          // <= 0: mr is some chunk max <= bv
+        if (j != jf) crest += ex2(fmaf(z[j], sL, -s.mrL));
+    const float d = fmaf(s.mr - s.bv, sL, -s.eps);   // <= 0 (up to eps): mr is some chunk max <= bv
     const float al = ex2(d);
     a.M = s.bv;
     a.R = al * (s.S + crest);

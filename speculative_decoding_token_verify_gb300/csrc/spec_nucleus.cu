@@ -267,13 +267,13 @@ __global__ void __launch_bounds__(NT, SV_NUC_CTAS) nucleus_kernel(const NucleusA
                 for (int u = 0; u < 4; ++u) {
                     const int k = k0 + u * NT;
                     if (k < nvec) {
-                        stream_chunk<T, false, true>(acc, wv[u], k, sL, __fdiv_rn(kRescale, s));
+                        stream_chunk<T, false>(acc, wv[u], k, sL, __fdiv_rn(kRescale, s));
                         if (acc.bk == k) acc.bw = wv[u];
                         cmin = fminf(cmin, chunk_min<T>(wv[u]));
                     }
                 }
             }
-            ra = stream_finish<T, true>(acc, 0, sL);
+            ra = stream_finish<T>(acc, 0, sL);
         } else {
             for (int v = t; v < a.V; v += NT) {
                 float z[1] = {Elem<T>::load(p + v)};

@@ -342,7 +342,8 @@ __device__ __forceinline__ UnitGeo<T> unit_geo(const Args &a, unsigned unit) {
 
 // Fold one unit. Returns the warp-merged accumulator (identical in every lane).
 // sL, rs: exponent scale and rescale margin (log2e and kRescale at s = 1);
-// kSub: difference-first exponents (the temperature variant).
+// kSub: difference-first exponents in the scalar head and tail folds (the
+// temperature variant).
 template <typename T, bool kEnt, bool kSub = false, bool kRing = false>
 __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float4 *ring, float sL = kLog2e,
                                                float rs = kRescale) {
@@ -394,7 +395,7 @@ __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float
                 cp_async_commit();
     #pragma unroll
                 for (int q = 0; q < kUnroll; ++q) {
-                    stream_chunk<T, kEnt, kSub>(s, w[q], k + q * 32, sL, rs);
+                    stream_chunk<T, kEnt>(s, w[q], k + q * 32, sL, rs);
                     if (s.bk == k + q * 32) s.bw = w[q];
                 }
             }
@@ -407,17 +408,17 @@ __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float
         for (int q = 0; q < kUnroll; ++q) w[q] = ldg_stream(vp + k + q * 32);
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
-            stream_chunk<T, kEnt, kSub>(s, w[q], k + q * 32, sL, rs);
+            stream_chunk<T, kEnt>(s, w[q], k + q * 32, sL, rs);
             // keep the bits of the lane's best chunk (no reload when finishing)
             if (s.bk == k + q * 32) s.bw = w[q];
         }
     }
     for (; k < nvec; k += 32) {
         const uint4 w = ldg_stream(vp + k);
-        stream_chunk<T, kEnt, kSub>(s, w, k, sL, rs);
+        stream_chunk<T, kEnt>(s, w, k, sL, rs);
         if (s.bk == k) s.bw = w;
     }
-    const RowAcc vs = stream_finish<T, kSub>(s, g.vb, sL);
+    const RowAcc vs = stream_finish<T>(s, g.vb, sL);
     return warp_merge(acc_merge(acc_merge(hs, vs, sL), ts, sL), sL);
 }
 
