@@ -8,14 +8,13 @@
 // logit value whose upper mass (the tokens with logit >= z*) reaches top_p of
 // the row's mass under p = softmax(s z); tokens tied at z* are all kept.
 //
-// Two kernels find z* by the same mass-weighted radix select:
-//  * nucleus_cluster_kernel (used when rows are 16-byte aligned and a
-//    cluster of at most 8 CTAs holds one in 32 or 64 KB slices): the row is
-//    read from HBM once into the cluster's distributed shared memory, and
-//    every pass below reads shared memory; see the comment above it.
-//  * nucleus_kernel (every other row): one CTA takes one row at a time
-//    (persistent over rows), re-reading the row between passes (L2-resident:
-//    two CTAs per SM keep under 100 MB of rows in flight).
+// Two kernels find z*. Both take one row per CTA at a time (persistent over
+// rows) and re-read the row from L2 between passes, with two CTAs per SM so
+// that the rows in flight stay L2-resident:
+//  * nucleus_row_kernel (V up to 256 K): bins the weights by their float
+//    encoding (see the comments above it);
+//  * nucleus_kernel (larger V, where 32-bit bin counters would lose
+//    precision): the passes below.
 //
 // The passes of one row:
 //
@@ -40,7 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <cooperative_groups.h>
+#include <algorithm>
 #include <cstdint>
 
 #include "spec_device.cuh"
@@ -469,221 +468,239 @@ __global__ void __launch_bounds__(NT, SV_NUC_CTAS) nucleus_kernel(const NucleusA
 }
 
 // ---------------------------------------------------------------------------
-// Cluster variant. A thread-block cluster of C CTAs holds one row in its
-// distributed shared memory: CTA c keeps elements [c S, (c + 1) S), loaded
-// once from HBM by the bulk-copy engine (cp.async.bulk, completion on an
-// mbarrier). Every pass then reads shared memory, and the per-row merges
-// (row statistics, histograms, key ranges, nucleus sums) go through DSMEM:
-// each CTA publishes its part in an exchange slot, one cluster barrier, and
-// every CTA reads all parts in rank order, so all of them hold identical
-// results. Exchange slots alternate between two buffers: a slot is written
-// again only after the cluster barrier that follows every read of it.
+// Mass bins. A token's weight e = 2^(z s log2e - R), R = ceil(M s log2e) an
+// integer reference (e <= 1 up to rounding), is binned by the top bits of its
+// float encoding -- the exponent and 3 mantissa bits: 8 bins a binade over
+// [2^-47, 2) -- and its bin adds the token's 24-bit significand shifted right
+// by `ushift`. The sums are integers (exact, independent of order), and a
+// bin's mass is its sum times a power of two. Weights below 2^-47 go to bin 0
+// (at most V 2^-46 of mass, which only enters the total).
 // ---------------------------------------------------------------------------
-constexpr int kSliceBytes = 65536;        // row bytes a CTA holds, at most
-constexpr int kSliceSmall = 32768;        // ... preferred: four CTAs per SM
-constexpr int kMaxCluster = 8;            // portable cluster size
-constexpr unsigned kWaitLimit = 1u << 20; // mbarrier polls before giving up
-constexpr int kX = kBins + 8;             // u64 words per exchange slot
+constexpr int kSub = 3;                                               // mantissa bits in a bin index
+constexpr int kBinades = 48;
+constexpr int NB = kBinades << kSub;                                  // 384 bins
+constexpr uint32_t kLoBits = (uint32_t)(127 - (kBinades - 1)) << 23; // 2^-47
+constexpr uint32_t kHiBits = (128u << 23) - 1u;                       // the largest float below 2
+constexpr int kBinBase = (int)(kLoBits >> (23 - kSub));
+constexpr int kKeyBins = 256;
 
-constexpr int kCandC = 64;                // boundary-bin tokens kept per warp
-constexpr float kBinUnit = 0x1p19f;       // histogram unit: 2^-19 of a bin's top weight
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }   // k in [-126, 127]
 
-struct CShared {
-    unsigned long long bar;       // mbarrier of the slice load
-    uint32_t hist[NW][kBins];     // per-warp histograms (kBinUnit units, <= 4096 tokens a warp)
-    u64 xbuf[2][kX];              // exchange slots, read by the peers
-    uint32_t ckey[NW][kCandC];    // boundary-bin tokens: logit key,
-    uint32_t cfix[NW][kCandC];    // ... mass in kBinUnit units of the bin's top weight,
-    int cv[NW][kCandC];           // ... vocabulary index
-    int cnt[NW];
-    float bscale[kBins];          // 2^-y_hi(j): a bin-j weight in units of its top weight
-    float dsum[NW];
-    float4 acc[NW];
-    float fw[NW][2];
-    uint32_t kw[NW][2];
-    int sel;
-    float sel_above;
-};
-constexpr int kCSharedBytes = (int)((sizeof(CShared) + 127) & ~(size_t)127);
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(unsigned long long *bar) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+// the encoding of a weight, clamped into the binned range (NaN: the top)
+__device__ __forceinline__ uint32_t wbits(float e) { return min(max(__float_as_uint(e), kLoBits), kHiBits); }
+// the same for a weight of a token at or below the max (e < 2 up to rounding):
+// only the lower clamp, in float (a NaN weight goes to bin 0)
+__device__ __forceinline__ uint32_t wbits_low(float e) { return __float_as_uint(fmaxf(e, __uint_as_float(kLoBits))); }
+__device__ __forceinline__ int bin_of(uint32_t b) { return (int)(b >> (23 - kSub)) - kBinBase; }
+// mass of one significand unit in bin g (2^(E - 150 + ushift), E = the bin's exponent)
+__device__ __forceinline__ float bin_scale(int g, int ushift) { return pow2i((g >> kSub) - 70 + ushift); }
+// log2 of bin g's lower edge; g = NB gives the top edge
+__device__ __forceinline__ float bin_edge(int g) {
+    return (float)((g >> kSub) - (kBinades - 1)) + log2f(1.f + (float)(g & ((1 << kSub) - 1)) * (1.f / (1 << kSub)));
 }
 
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long *bar, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// Wait, with a bounded number of polls, for the phase of parity `par` to
-// complete. Returns false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, unsigned par) {
-    unsigned ns = 32;
-    for (unsigned it = 0; it < kWaitLimit; ++it) {
-        unsigned done;
-        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done)
-                     : "r"(smem_u32(bar)), "r"(par)
-                     : "memory");
-        if (done) return true;
-        __nanosleep(ns);
-        ns = min(ns * 2u, 256u);
-    }
-    return false;
-}
-
-// bytes (a multiple of 16; both addresses 16-byte aligned) from global to
-// this CTA's shared memory, completing on `bar`
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes, unsigned long long *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-// order this CTA's earlier generic-proxy accesses of shared memory before
-// later async-proxy (bulk copy) writes
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-namespace cg = cooperative_groups;
-
-__device__ __forceinline__ float elem_f(float x) { return x; }
-__device__ __forceinline__ float elem_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-__device__ __forceinline__ u64 pack2(float x, float y) {
-    return (u64)__float_as_uint(x) | ((u64)__float_as_uint(y) << 32);
-}
-__device__ __forceinline__ float lo_f(u64 v) { return __uint_as_float((uint32_t)v); }
-__device__ __forceinline__ float hi_f(u64 v) { return __uint_as_float((uint32_t)(v >> 32)); }
-
-__device__ __forceinline__ u64 fixed40(float y) { return __float2ull_rn(ex2(y) * 0x1p40f); }
-
-// Sum the per-warp histograms of every CTA of the cluster (thread t owns bin
-// t; CTAs added in rank order, exact 64-bit integers); this CTA's histograms
-// are cleared.
-// With `ztot`, the per-warp partial sums in sh.fw[.][0] travel along: the
-// CTA's sum (warp order), then the cluster's (rank order) lands in *ztot.
-__device__ __forceinline__ u64 cluster_bins(CShared &sh, cg::cluster_group &cl, int C, int &par,
-                                            float *ztot = nullptr) {
-    const int t = threadIdx.x;
-    __syncthreads();
-    u64 h = 0;
+// Does one of a vector's elements lie in [zl, zh] (exact element values)?
+template <typename T>
+__device__ __forceinline__ bool vec_in_range(const uint4 &x, float zl, float zh) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t lo2 = (__float_as_uint(zl) >> 16) * 0x10001u, hi2 = (__float_as_uint(zh) >> 16) * 0x10001u;
+        const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+        uint32_t any = 0u;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-        h += sh.hist[w][t];
-        sh.hist[w][t] = 0u;
+        for (int i = 0; i < 4; ++i) {
+            uint32_t ge, le;
+            asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(ge) : "r"(wv[i]), "r"(lo2));
+            asm("set.le.u32.bf16x2 %0, %1, %2;" : "=r"(le) : "r"(wv[i]), "r"(hi2));
+            any |= ge & le;
+        }
+        return any != 0u;
+    } else {
+        const float z[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)};
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) any |= (z[i] >= zl) & (z[i] <= zh);
+        return any;
     }
-    sh.xbuf[par][t] = h;
-    if (ztot && t == 0) {
-        float zs = 0.f;
-        for (int i = 0; i < NW; ++i) zs += sh.fw[i][0];
-        sh.xbuf[par][kBins] = pack2(zs, 0.f);
-    }
-    cl.sync();
-    u64 H = 0;
-    float Z = 0.f;
-    for (int c = 0; c < C; ++c) {
-        const u64 *x = cl.map_shared_rank(&sh.xbuf[par][0], c);
-        H += x[t];
-        if (ztot) Z += lo_f(x[kBins]);
-    }
-    if (ztot) *ztot = Z;
-    par ^= 1;
-    return H;
 }
 
-// Thread t holds the mass h >= 0 of bin t (fp32): the running sums in bin
-// order, in a fixed association; the selected bin is the lowest whose
-// running sum plus `above` reaches tgt (the last bin with mass if rounding
-// leaves all short). `above` becomes the running sum before it.
-__device__ __forceinline__ int select_f(CShared &sh, float h, float tgt, float &above) {
+// Positions in order, thread t holding positions P t .. P t + P - 1 (the
+// first n valid) with masses a[] and r[]: the first position with mass whose
+// running a-mass, on top of base_a, reaches tgt; when none does (rounding),
+// the last position with mass, else 0. Sets the running a- and r-masses
+// before it (on top of base_a, base_r) and its own r-mass. Sums in a fixed
+// association.
+template <int P, int NWARP, typename SH>
+__device__ __forceinline__ int select_pos(SH &sh, const float (&a)[P], const float (&r)[P], int n, float tgt,
+                                          float base_a, float base_r, float &above_a, float &above_r, float &r_sel) {
     const int t = threadIdx.x, l = t & 31, w = t >> 5;
-    float v = h;
+    float sa = 0.f, sr = 0.f;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        sa += a[p];
+        sr += r[p];
+    }
+    float ia = sa, ir = sr;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(kFull, v, o);
-        if (l >= o) v += u;
-    }
-    if (l == 31) sh.dsum[w] = v;
-    if (t == 0) sh.sel = kBins;
-    __syncthreads();
-    float pre = above;
-    for (int i = 0; i < w; ++i) pre += sh.dsum[i];
-    const float incl = pre + v;
-    if (incl >= tgt) atomicMin(&sh.sel, t);
-    __syncthreads();
-    if (sh.sel == kBins) {   // only through rounding: the last bin with mass
-        if (h > 0.f) atomicMax(&sh.sel, kBins + 1 + t);
-        __syncthreads();
-        if (t == 0) sh.sel = sh.sel > kBins ? sh.sel - kBins - 1 : kBins - 1;
-        __syncthreads();
-    }
-    const int j = sh.sel;
-    if (t == j) sh.sel_above = incl - h;
-    __syncthreads();
-    above = sh.sel_above;
-    __syncthreads();
-    return j;
-}
-
-// Visit the slice in shared memory: vectors k = t, t + NT, ... (element
-// v0 + k E + j), then the tail scalars (warp 0, lane < tail); the same fixed
-// order every pass. Warp-uniform: every lane of a warp makes the same calls
-// (past the slice, z is -inf), so f may use warp-collective operations.
-template <typename T, typename F>
-__device__ __forceinline__ void for_slice(const T *slice, int nvec, int tail, int v0, F &&f) {
-    constexpr int E = Elem<T>::kPerVec;
-    const uint4 *sv = reinterpret_cast<const uint4 *>(slice);
-    const int lane = threadIdx.x & 31;
-    for (int k0 = (int)threadIdx.x - lane; k0 < nvec; k0 += NT) {
-        const int k = k0 + lane;
-        float z[E];
-        if (k < nvec) {
-            Elem<T>::unpack(sv[k], z);
-        } else {
-#pragma unroll
-            for (int j = 0; j < E; ++j) z[j] = neg_inf();
+        const float ua = __shfl_up_sync(kFull, ia, o), ur = __shfl_up_sync(kFull, ir, o);
+        if (l >= o) {
+            ia += ua;
+            ir += ur;
         }
-#pragma unroll
-        for (int j = 0; j < E; ++j) f(v0 + k * E + j, z[j]);
     }
-    if (threadIdx.x < 32) f(v0 + nvec * E + lane, lane < tail ? elem_f(slice[nvec * E + lane]) : neg_inf());
+    float ea = __shfl_up_sync(kFull, ia, 1), er = __shfl_up_sync(kFull, ir, 1);
+    if (l == 0) ea = er = 0.f;
+    if (l == 31) {
+        sh.wa[w] = ia;
+        sh.wr[w] = ir;
+    }
+    if (t == 0) {
+        sh.sel = 0x7fffffff;
+        sh.sel_last = -1;
+    }
+    __syncthreads();
+    float pa = base_a, pr = base_r;
+    for (int i = 0; i < w; ++i) {
+        pa += sh.wa[i];
+        pr += sh.wr[i];
+    }
+    pa += ea;
+    pr += er;
+    int first = 0x7fffffff, last = -1;
+    {
+        float x = pa;
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int pos = P * t + p;
+            x += a[p];
+            if (pos < n && a[p] > 0.f) {
+                if (x >= tgt && first == 0x7fffffff) first = pos;
+                last = pos;
+            }
+        }
+    }
+    if (first != 0x7fffffff) atomicMin(&sh.sel, first);
+    if (last >= 0) atomicMax(&sh.sel_last, last);
+    __syncthreads();
+    const int s = sh.sel != 0x7fffffff ? sh.sel : max(sh.sel_last, 0);
+    if (s / P == t) {
+        float xa = pa, xr = pr;
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            if (p < s - P * t) {
+                xa += a[p];
+                xr += r[p];
+            }
+        float rs = 0.f;
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            if (p == s - P * t) rs = r[p];
+        sh.sel_a = xa;
+        sh.sel_r = xr;
+        sh.sel_rs = rs;
+    }
+    __syncthreads();
+    above_a = sh.sel_a;
+    above_r = sh.sel_r;
+    r_sel = sh.sel_rs;
+    __syncthreads();
+    return s;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(NT, 4) nucleus_cluster_kernel(const NucleusArgs a, int S) {
-    extern __shared__ __align__(128) unsigned char dsm[];
-    CShared &sh = *reinterpret_cast<CShared *>(dsm);
-    T *slice = reinterpret_cast<T *>(dsm + kCSharedBytes);
-    cg::cluster_group cl = cg::this_cluster();
-    const int C = (int)cl.num_blocks();
-    const int rank = (int)cl.block_rank();
-    const int t = threadIdx.x, l = t & 31, w = t >> 5;
-    constexpr int E = Elem<T>::kPerVec;
-    for (int i = t; i < NW * kBins; i += NT) (&sh.hist[0][0])[i] = 0ull;
-    if (t == 0) mbar_init(&sh.bar);
+// Block sum of one float per thread (warp order, then warp sums in order);
+// the result in every thread.
+template <int NWARP, typename SH>
+__device__ __forceinline__ float block_sum(SH &sh, float v) {
+    const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    if (l == 0) sh.wa[w] = v;
     __syncthreads();
-    unsigned phase = 0;
-    bool pending = false;   // a slice load whose wait gave up
-    int par = 0;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < NWARP; ++i) s += sh.wa[i];
+    __syncthreads();
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// Row variant (nucleus_row_kernel): one CTA of 512 threads per row,
+// persistent over rows, two CTAs per SM. Pass A reads the row from HBM, the
+// later passes re-read it from L2 (two rows per SM in flight: under 80 MB at
+// V = 128256 bf16). The passes of one row:
+//
+//  A. the max M and its lowest index I; R = ceil(M s log2e);
+//  B. the weights' significands into the mass bins above, a column of
+//     counters per lane; the first bin j1, from the top, whose running mass
+//     reaches top_p of the total;
+//  C. the tokens of bin j1 -- a prefilter on the logit range the bin can hold
+//     (packed bf16x2 compares; units with a hit queued per warp), then pass
+//     B's exact bin test -- add their significands to a histogram over their
+//     keys: one bin per key while the range holds at most 256 keys, else 256
+//     sub-ranges, of which the selected one narrows the range for another
+//     round (bf16: at most two rounds; fp32: at most five). The first key
+//     whose running mass, on top of the bins above j1, reaches the target is
+//     z*;
+//  -- R, the nucleus mass other than I's, comes from the same integer sums;
+//     when the entropy moment is wanted, one more pass sums e y over the
+//     tokens with z >= z*.
+// ---------------------------------------------------------------------------
+constexpr int RT = 512;
+constexpr int RW = RT / 32;
+constexpr int kRQueue = 512;    // groups a warp queues before it processes them
+
+struct RShared {
+    union {
+        uint32_t hist[NB][32];              // pass B: bins, a column per lane (no bank conflicts)
+        struct {
+            uint32_t key[RW][kKeyBins];     // pass C: per-warp key histograms
+            uint32_t queue[RW][kRQueue];    // ... units holding a candidate
+        } c;
+    } u;
+    float wa[RW], wr[RW];
+    int wi[RW];
+    int sel, sel_last;
+    float sel_a, sel_r, sel_rs;
+};
+constexpr int kRUnionWords = (int)(sizeof(RShared::u) / 4);
+
+// the largest element of a 16-byte vector
+template <typename T>
+__device__ __forceinline__ float vec_max(const uint4 &x) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t m = bmax2(bmax2(x.x, x.y), bmax2(x.z, x.w));
+        return fmaxf(bf16_lo(m), bf16_hi(m));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                     fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)));
+    }
+}
+
+// kAl: rows start on 16-byte boundaries; a unit is then one 16-byte vector
+// (EU = 8 bf16 or 4 fp32 elements, four in flight per thread), else a group
+// of 8 elements read one by one. Units k = t, t + 512, ... go to thread t;
+// the V mod EU last elements to the last warp.
+template <typename T, bool kAl>
+__global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a, int ushift) {
+    extern __shared__ __align__(16) unsigned char rsm[];
+    RShared &sh = *reinterpret_cast<RShared *>(rsm);
+    const int t = threadIdx.x, l = t & 31, w = t >> 5;
+    constexpr int EU = kAl ? Elem<T>::kPerVec : 8;   // elements of a unit
+    constexpr int UF = kAl ? 4 : 1;                  // units in flight per thread
+    for (int i = t; i < kRUnionWords; i += RT) (&sh.u.hist[0][0])[i] = 0u;
+    __syncthreads();
     const int rows = a.nt_rows + a.nd_rows;
     const int nrow = a.B * rows;
-    const int ncl = (int)(gridDim.x / (unsigned)C), cid = (int)(blockIdx.x / (unsigned)C);
-    const int v0 = rank * S;
-    const int len = max(0, min(a.V, v0 + S) - v0);
-    const int nvec = len / E, tail = len - nvec * E;
-    const float Drel = logf((float)a.V / (1.f - a.top_p)) + 1.f;
-    for (int row = cid; row < nrow; row += ncl) {
+    const int V = a.V, nu = V / EU, ut = V - nu * EU;
+    const uint32_t umask = (1u << (23 - ushift)) - 1u, uimpl = 1u << (23 - ushift);
+    auto unit = [&](uint32_t b) -> uint32_t { return ((b >> ushift) & umask) | uimpl; };
+    for (int row = blockIdx.x; row < nrow; row += gridDim.x) {
         const int b = row / rows, r = row - b * rows;
         const bool target = r < a.nt_rows;
         const int kb = a.draft_len ? min(max(__ldg(a.draft_len + b), 0), a.K) : a.K;
         const bool verified = target ? r <= kb : r - a.nt_rows < kb;
-        if (!verified) {   // uniform over the cluster: no barrier is skipped unevenly
-            if (rank == 0 && t == 0) {
+        if (!verified) {
+            if (t == 0) {
                 a.rec[row] = acc_pack(acc_empty());
                 a.zth[row] = __int_as_float(0x7f800000);
             }
@@ -691,71 +708,62 @@ __global__ void __launch_bounds__(NT, 4) nucleus_cluster_kernel(const NucleusArg
         }
         const T *p = target ? static_cast<const T *>(a.zt) + ((long long)b * (a.K + 1) + r) * a.ts
                             : static_cast<const T *>(a.zd) + ((long long)b * a.K + (r - a.nt_rows)) * a.ds;
+        const uint4 *vp = reinterpret_cast<const uint4 *>(p);
+        auto load_unit = [&](int k, float (&z)[EU]) {
+            if constexpr (kAl) Elem<T>::unpack(__ldg(vp + k), z);
+            else load8<T>(p, 8 * k, V, false, z);
+        };
         float s = 1.f;
         if (a.inv_temp) {
             const float si = __ldg(a.inv_temp + b);
             s = (si >= SPEC_MIN_INV_TEMPERATURE && si <= SPEC_MAX_INV_TEMPERATURE) ? si : 1.f;
         }
         const float sL = s * kLog2e;
-        const float rs = __fdiv_rn(kRescale, s);
 
-        // ---- load this CTA's slice once (the previous row's reads are done)
-        __syncthreads();
-        if (t == 0 && nvec > 0) {
-            fence_proxy_async();
-            mbar_expect_tx(&sh.bar, (unsigned)nvec * 16u);
-            bulk_load(slice, p + v0, (unsigned)nvec * 16u, &sh.bar);
-        }
-        if (t < tail) slice[nvec * E + t] = p[v0 + nvec * E + t];
-        if (nvec > 0) {
-            pending = !mbar_wait(&sh.bar, phase);
-            if (pending && t == 0) atomicMax(a.status, (unsigned)SPEC_ERR_TIMEOUT);
-            phase ^= 1u;
-        }
-        __syncthreads();
-
-        // ---- A: max M, its lowest index I and the smallest logit (chunk
-        // maxima on packed bf16 / fp32 compares), merged over the cluster in
-        // rank order
-        float M = neg_inf(), cmin = __int_as_float(0x7f800000);
+        // ---- A: the max and its lowest index (the first unit holding the
+        // thread's max is read again for the index)
+        float M = neg_inf();
         int I = 0x7fffffff;
         {
-            const uint4 *sv = reinterpret_cast<const uint4 *>(slice);
             int bk = -1;
-            uint4 bw = make_uint4(0u, 0u, 0u, 0u);
-            for (int k = t; k < nvec; k += NT) {
-                const uint4 wv = sv[k];
-                float c;
-                if constexpr (sizeof(T) == 2) {
-                    const uint32_t m = bmax2(bmax2(wv.x, wv.y), bmax2(wv.z, wv.w));
-                    c = fmaxf(bf16_lo(m), bf16_hi(m));
+            for (int k0 = t; k0 < nu; k0 += UF * RT) {
+                float c[UF];
+                if constexpr (kAl) {
+                    uint4 x[UF];
+#pragma unroll
+                    for (int u = 0; u < UF; ++u)
+                        if (k0 + u * RT < nu) x[u] = __ldg(vp + k0 + u * RT);
+#pragma unroll
+                    for (int u = 0; u < UF; ++u) c[u] = k0 + u * RT < nu ? vec_max<T>(x[u]) : neg_inf();
                 } else {
-                    c = fmaxf(fmaxf(__uint_as_float(wv.x), __uint_as_float(wv.y)),
-                              fmaxf(__uint_as_float(wv.z), __uint_as_float(wv.w)));
+                    float z[8];
+                    load_unit(k0, z);
+                    c[0] = neg_inf();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) c[0] = fmaxf(c[0], z[j]);
                 }
-                if (c > M) {   // strict: the first chunk holding the maximum
-                    M = c;
-                    bk = k;
-                    bw = wv;
-                }
-                cmin = fminf(cmin, chunk_min<T>(wv));
+#pragma unroll
+                for (int u = 0; u < UF; ++u)
+                    if (c[u] > M) {   // strict: the first unit holding the maximum
+                        M = c[u];
+                        bk = k0 + u * RT;
+                    }
             }
             if (bk >= 0) {
-                float z[E];
-                Elem<T>::unpack(bw, z);
-                int jf = E - 1;
+                float z[EU];
+                load_unit(bk, z);
+                int jf = EU - 1;
 #pragma unroll
-                for (int q = E - 1; q >= 0; --q)
-                    if (z[q] == M) jf = q;
-                I = v0 + bk * E + jf;
+                for (int j = EU - 1; j >= 0; --j)
+                    if (z[j] == M) jf = j;
+                I = bk * EU + jf;
             }
-            if (t < tail) {
-                const float z = elem_f(slice[nvec * E + t]);
+            if (t < ut) {
+                const float z = Elem<T>::load(p + nu * EU + t);
                 if (z > M) {
                     M = z;
-                    I = v0 + nvec * E + t;
+                    I = nu * EU + t;
                 }
-                cmin = fminf(cmin, z);
             }
         }
 #pragma unroll
@@ -766,313 +774,287 @@ __global__ void __launch_bounds__(NT, 4) nucleus_cluster_kernel(const NucleusArg
                 M = om;
                 I = oi;
             }
-            cmin = fminf(cmin, __shfl_xor_sync(kFull, cmin, o));
         }
         if (l == 0) {
-            sh.fw[w][0] = M;
-            sh.fw[w][1] = cmin;
-            sh.kw[w][0] = (uint32_t)I;
+            sh.wa[w] = M;
+            sh.wi[w] = I;
         }
         __syncthreads();
-        if (t == 0) {
-            float m = sh.fw[0][0], cm = sh.fw[0][1];
-            int ii = (int)sh.kw[0][0];
-            for (int q = 1; q < NW; ++q) {
-                if (sh.fw[q][0] > m || (sh.fw[q][0] == m && (int)sh.kw[q][0] < ii)) {
-                    m = sh.fw[q][0];
-                    ii = (int)sh.kw[q][0];
-                }
-                cm = fminf(cm, sh.fw[q][1]);
+        M = sh.wa[0];
+        I = sh.wi[0];
+#pragma unroll
+        for (int q = 1; q < RW; ++q)
+            if (sh.wa[q] > M || (sh.wa[q] == M && sh.wi[q] < I)) {
+                M = sh.wa[q];
+                I = sh.wi[q];
             }
-            sh.xbuf[par][0] = pack2(m, __int_as_float(ii));
-            sh.xbuf[par][1] = pack2(cm, 0.f);
-        }
-        cl.sync();
-        M = neg_inf();
-        I = 0x7fffffff;
-        cmin = __int_as_float(0x7f800000);
-        for (int c = 0; c < C; ++c) {
-            const u64 *xc = cl.map_shared_rank(&sh.xbuf[par][0], c);
-            const float om = lo_f(xc[0]);
-            const int oi = __float_as_int(hi_f(xc[0]));
-            if (om > M || (om == M && oi < I)) {
-                M = om;
-                I = oi;
-            }
-            cmin = fminf(cmin, lo_f(xc[1]));
-        }
-        par ^= 1;
+        __syncthreads();
         if (!(M > neg_inf()) || M == __int_as_float(0x7f800000)) {
-            // no finite logit (the verification kernel reports the bad row);
-            // M is the cluster's, so every CTA leaves the row here
-            if (rank == 0 && t == 0) {
+            // no finite logit, or an infinite one: the verification kernel
+            // reports the bad row
+            if (t == 0) {
                 a.rec[row] = acc_pack(acc_empty());
                 a.zth[row] = __int_as_float(0x7f800000);
             }
             continue;
         }
-
-        // ---- B: every token's weight e = 2^y, y = (z - M) s log2e, summed
-        // (fixed order) into the total Z; those within Dr nats of M also go
-        // to a histogram of Dr/256-nat bins, a token of bin j counting
-        // ex2(y - y_hi(j)) in kBinUnit units of the bin's top weight 2^y_hi(j)
-        // (32 bits keep ~2^-20 relative precision); bin masses in fp32
-        // (bin and unit conversions by the 2^23 magic-number rounding on the
-        // FMA pipe: bin j holds y * ybin in [j - 1/2, j + 1/2), its top is
-        // y_hi(j) = (j - 1/2) ystep; rounding keeps the bin monotone in z,
-        // which is all the search needs)
-        const float Dr = fminf((M - cmin) * s, Drel);
-        const float ylim = -Dr * kLog2e;                                   // y >= ylim <=> binned
-        const float ybin = Dr > 0.f ? -(float)kBins * kLn2 / Dr : 0.f;
-        const float ystep = Dr > 0.f ? 1.f / ybin : 0.f;
-        auto bin_of = [&](float y) -> int {
-            return min(kBins - 1, __float_as_int(fmaf(y, ybin, 0x1p23f)) - 0x4B000000);
+        const float Rf = ceilf(M * sL), nR = -Rf;
+        auto bin_add = [&](float z) {
+            const uint32_t bb = wbits_low(ex2(fmaf(z, sL, nR)));
+            atomicAdd(&sh.u.hist[bin_of(bb)][l], unit(bb));
         };
-        auto unit_of = [&](float e, int j) -> uint32_t {   // e = 2^y of a bin-j token
-            return (uint32_t)(__float_as_int(fmaf(e * sh.bscale[j], kBinUnit, 0x1p23f)) - 0x4B000000);
-        };
-        sh.bscale[t] = ex2(-((float)t - 0.5f) * ystep);
-        const float tmass = ex2(((float)t - 0.5f) * ystep) * (1.f / kBinUnit);   // thread t: bin t's unit mass
-        __syncthreads();
-        float Zs = 0.f;
-        for_slice<T>(slice, nvec, tail, v0, [&](int v, float z) {
-            const float y = (z - M) * sL;
-            const float e = ex2(y);
-            Zs += e;
-            if (y >= ylim) {
-                const int j = bin_of(y);
-                atomicAdd(&sh.hist[w][j], unit_of(e, j));
-            }
-        });
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) Zs += __shfl_xor_sync(kFull, Zs, o);
-        if (l == 0) sh.fw[w][0] = Zs;
-        float Z = 0.f;
-        const u64 H1 = cluster_bins(sh, cl, C, par, &Z);
-        const float tgt = a.top_p * Z;
-        float above = 0.f;
-        const int j1 = select_f(sh, (float)H1 * tmass, tgt, above);
-        const float j1mass = ex2(((float)j1 - 0.5f) * ystep) * (1.f / kBinUnit);   // unit mass of bin j1
 
-        // ---- C: tokens above bin j1 are in the nucleus: their mass (other
-        // than I) and entropy moment accumulate per thread; bin j1's tokens
-        // (a contiguous key range: y is monotone in z) are copied to this
-        // warp's list in a fixed order, and their key range is merged over
-        // the cluster
-        float Ra = 0.f, Ta = 0.f;
-        uint32_t klo = 0xffffffffu, khi = 0u;
-        int wc = 0;   // warp-uniform count of bin-j1 tokens this warp met
-        for_slice<T>(slice, nvec, tail, v0, [&](int v, float z) {
-            const float y = (z - M) * sL;
-            const int bn = y >= ylim ? bin_of(y) : kBins;
-            if (bn < j1) {
-                const float e = ex2(y);
-                if (v != I) Ra += e;
-                Ta = fmaf(e, y, Ta);
-            }
-            const bool cand = bn == j1;
-            const unsigned m = __ballot_sync(kFull, cand);
-            if (m) {
-                if (cand) {
-                    const uint32_t k = Key<T>::of(z);
-                    klo = min(klo, k);
-                    khi = max(khi, k);
-                    const int slot = wc + __popc(m & ((1u << l) - 1u));
-                    if (slot < kCandC) {
-                        sh.ckey[w][slot] = k;
-                        sh.cfix[w][slot] = unit_of(ex2(y), j1);
-                        sh.cv[w][slot] = v;
-                    }
-                }
-                wc += __popc(m);
-            }
-        });
+        // ---- B: the weights' significands into their bins
+        for (int k0 = t; k0 < nu; k0 += UF * RT) {
+            if constexpr (kAl) {
+                uint4 x[UF];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            klo = min(klo, __shfl_xor_sync(kFull, klo, o));
-            khi = max(khi, __shfl_xor_sync(kFull, khi, o));
-        }
-        if (l == 0) {
-            sh.kw[w][0] = klo;
-            sh.kw[w][1] = khi;
-            sh.cnt[w] = wc;
-        }
-        __syncthreads();
-        bool fits = true;   // this CTA's bin-j1 tokens are all in the lists
-        if (t == 0) {
-            uint32_t lo = sh.kw[0][0], hi = sh.kw[0][1];
-            for (int i = 1; i < NW; ++i) {
-                lo = min(lo, sh.kw[i][0]);
-                hi = max(hi, sh.kw[i][1]);
-            }
-            sh.xbuf[par][0] = (u64)lo | ((u64)hi << 32);
-        }
+                for (int u = 0; u < UF; ++u)
+                    if (k0 + u * RT < nu) x[u] = __ldg(vp + k0 + u * RT);
 #pragma unroll
-        for (int i = 0; i < NW; ++i) fits &= sh.cnt[i] <= kCandC;
-        cl.sync();
-        klo = 0xffffffffu;
-        khi = 0u;
-        for (int c = 0; c < C; ++c) {
-            const u64 xv = cl.map_shared_rank(&sh.xbuf[par][0], c)[0];
-            klo = min(klo, (uint32_t)xv);
-            khi = max(khi, (uint32_t)(xv >> 32));
-        }
-        par ^= 1;
-
-        // ---- D: refine the key range to one key, 256 sub-ranges a round
-        // (over the lists; over the slice where a list overflowed)
-        int it = 0;
-        while (klo < khi && it < kMaxRefine) {
-            const u64 W = (u64)(khi - klo) + 1ull;
-            if (fits) {
-                for (int i = t; i < NW * kCandC; i += NT) {
-                    const int wi = i / kCandC, si = i - wi * kCandC;
-                    if (si < sh.cnt[wi]) {
-                        const uint32_t k = sh.ckey[wi][si];
-                        if (k >= klo && k <= khi) atomicAdd(&sh.hist[w][(int)(((u64)(khi - k) << 8) / W)], sh.cfix[wi][si]);
+                for (int u = 0; u < UF; ++u)
+                    if (k0 + u * RT < nu) {
+                        float z[EU];
+                        Elem<T>::unpack(x[u], z);
+#pragma unroll
+                        for (int j = 0; j < EU; ++j) bin_add(z[j]);
                     }
-                }
             } else {
-                const float zlo = Key<T>::value(klo), zhi = Key<T>::value(khi);
-                for_slice<T>(slice, nvec, tail, v0, [&](int v, float z) {
-                    if (z >= zlo && z <= zhi) {
-                        const uint32_t k = Key<T>::of(z);
-                        atomicAdd(&sh.hist[w][(int)(((u64)(khi - k) << 8) / W)], unit_of(ex2((z - M) * sL), j1));
-                    }
-                });
+                float z[8];
+                load_unit(k0, z);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) bin_add(z[j]);
             }
-            const int j = select_f(sh, (float)cluster_bins(sh, cl, C, par) * j1mass, tgt, above);
-            // keys of sub-range j: khi - k in [ceil(j W / 256), ceil((j + 1) W / 256) - 1]
-            const u64 lo_off = ((u64)j * W + 255ull) >> 8;
-            const u64 hi_off = (((u64)(j + 1) * W + 255ull) >> 8) - 1ull;
-            const uint32_t nkhi = khi - (uint32_t)lo_off;
-            const uint32_t nklo = khi - (uint32_t)hi_off;
-            khi = nkhi;
-            klo = nklo;
-            ++it;
         }
-        if (klo < khi && rank == 0 && t == 0) atomicMax(a.status, (unsigned)SPEC_ERR_BAD_ROW);   // not reached
-        const uint32_t kstar = khi;
+        if (w == RW - 1 && l < ut) bin_add(Elem<T>::load(p + nu * EU + l));
+        __syncthreads();
+        // thread t takes position t from the top: bin NB - 1 - t
+        const int g = NB - 1 - t;
+        float m = 0.f;
+        if (g >= 0) {
+            u64 h = 0;
+#pragma unroll 8
+            for (int q = 0; q < 32; ++q) {
+                const int c = (q + l) & 31;
+                h += sh.u.hist[g][c];
+                sh.u.hist[g][c] = 0u;
+            }
+            m = (float)h * bin_scale(g, ushift);
+        }
+        const float Z = block_sum<RW>(sh, m);
+        const uint32_t bI = wbits_low(ex2(fmaf(M, sL, nR)));   // I, binned as pass B binned it
+        const int gI = bin_of(bI);
+        const float mI = (float)unit(bI) * bin_scale(gI, ushift);
+        const float tgt = a.top_p * Z;
+        float above_a, above_r, rsel;
+        const float ma[1] = {g >= 1 ? m : 0.f};
+        const float mr[1] = {g >= 1 ? (g == gI ? m - mI : m) : 0.f};
+        const int j1 = NB - 1 - select_pos<1, RW>(sh, ma, mr, NB - 1, tgt, 0.f, 0.f, above_a, above_r, rsel);
+
+        // ---- the logit range bin j1 can hold (its weight range, widened past
+        // the exponential's and the roundings' errors), as keys
+        uint32_t klo, khi;
+        {
+            float zlo = (bin_edge(j1) - 0x1p-12f + Rf) / sL, zhi = (bin_edge(j1 + 1) + 0x1p-12f + Rf) / sL;
+            zlo -= fabsf(zlo) * 0x1p-16f + 0x1p-120f;
+            zhi = fminf(zhi + fabsf(zhi) * 0x1p-16f + 0x1p-120f, M);
+            if constexpr (sizeof(T) == 2) {
+                zlo = __bfloat162float(__float2bfloat16_rd(zlo));
+                zhi = __bfloat162float(__float2bfloat16_ru(zhi));
+            }
+            klo = Key<T>::of(zlo);
+            khi = Key<T>::of(zhi);
+            klo = min(klo, khi);   // an empty bin (only when no bin holds mass)
+        }
+
+        // ---- C (rounds): the candidates' significands by key
+        const uint32_t jsel = (uint32_t)(j1 + kBinBase);
+        const float scj = bin_scale(j1, ushift);
+        uint32_t kstar = khi;
+        float Rn = 0.f;   // nucleus mass other than I, relative to 2^R
+        for (int it = 0;; ++it) {
+            const u64 W = (u64)(khi - klo) + 1ull;
+            const bool exact = W <= (u64)kKeyBins;
+            const float zl = Key<T>::value(klo), zh = Key<T>::value(khi);
+            auto candidate = [&](int idx, float z) {
+                if (z >= zl && z <= zh && idx != I) {
+                    const uint32_t bb = wbits_low(ex2(fmaf(z, sL, nR)));
+                    if ((bb >> (23 - kSub)) == jsel) {
+                        const uint32_t d = khi - Key<T>::of(z);
+                        const int sub = exact ? (int)d : (int)(((u64)d << 8) / W);
+                        atomicAdd(&sh.u.c.key[w][sub], unit(bb));
+                    }
+                }
+            };
+            auto flush = [&](int qn) {
+                __syncwarp();
+                for (int i = l; i < qn; i += 32) {
+                    const int k = (int)sh.u.c.queue[w][i];
+                    float z[EU];
+                    load_unit(k, z);
+#pragma unroll
+                    for (int j = 0; j < EU; ++j) candidate(k * EU + j, z[j]);
+                }
+                __syncwarp();
+            };
+            int qn = 0;   // warp-uniform
+            for (int k0 = t - l; k0 < nu; k0 += UF * RT) {
+                bool hit[UF];
+                if constexpr (kAl) {
+                    uint4 x[UF];
+#pragma unroll
+                    for (int u = 0; u < UF; ++u)
+                        if (k0 + l + u * RT < nu) x[u] = __ldg(vp + k0 + l + u * RT);
+#pragma unroll
+                    for (int u = 0; u < UF; ++u) hit[u] = k0 + l + u * RT < nu && vec_in_range<T>(x[u], zl, zh);
+                } else {
+                    bool any = false;
+                    if (k0 + l < nu) {
+                        float z[8];
+                        load_unit(k0 + l, z);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) any |= (z[j] >= zl) & (z[j] <= zh);
+                    }
+                    hit[0] = any;
+                }
+#pragma unroll
+                for (int u = 0; u < UF; ++u) {
+                    const unsigned mk = __ballot_sync(kFull, hit[u]);
+                    if (mk) {
+                        if (hit[u]) sh.u.c.queue[w][qn + __popc(mk & ((1u << l) - 1u))] = (uint32_t)(k0 + l + u * RT);
+                        qn += __popc(mk);
+                    }
+                }
+                if (qn > kRQueue - UF * 32) {
+                    flush(qn);
+                    qn = 0;
+                }
+            }
+            flush(qn);
+            if (w == RW - 1 && l < ut) candidate(nu * EU + l, Elem<T>::load(p + nu * EU + l));
+            // I, left out above, with its key
+            float uI = 0.f;
+            int sI = -1;
+            if (M >= zl && M <= zh && (bI >> (23 - kSub)) == jsel) {
+                const uint32_t d = khi - Key<T>::of(M);
+                uI = (float)unit(bI);
+                sI = exact ? (int)d : (int)(((u64)d << 8) / W);
+            }
+            __syncthreads();
+            float us = 0.f;
+            if (t < kKeyBins) {
+                u64 h = 0;
+#pragma unroll
+                for (int q = 0; q < RW; ++q) {
+                    h += sh.u.c.key[q][t];
+                    sh.u.c.key[q][t] = 0u;
+                }
+                us = (float)h;
+            }
+            const float ka[1] = {(t == sI ? us + uI : us) * scj};
+            const float kr[1] = {us * scj};
+            float aa, ar, rs;
+            const int sk = select_pos<1, RW>(sh, ka, kr, kKeyBins, tgt, above_a, above_r, aa, ar, rs);
+            if (exact) {
+                kstar = khi - (uint32_t)sk;
+                Rn = ar + rs;
+                break;
+            }
+            // keys of sub-range sk: khi - k in [ceil(sk W / 256), ceil((sk + 1) W / 256) - 1]
+            const u64 lo_off = ((u64)sk * W + 255ull) >> 8;
+            const u64 hi_off = (((u64)(sk + 1) * W + 255ull) >> 8) - 1ull;
+            const uint32_t nkhi = khi - (uint32_t)lo_off;
+            klo = khi - (uint32_t)hi_off;
+            khi = nkhi;
+            above_a = aa;
+            above_r = ar;
+            if (it + 1 >= kMaxRefine) {   // not reached: 32-bit keys need at most five rounds
+                if (t == 0) atomicMax(a.status, (unsigned)SPEC_ERR_BAD_ROW);
+                kstar = khi;
+                Rn = ar;
+                break;
+            }
+        }
+        // the queue overlapped pass B's bins: clear it for the next row
+        for (int i = RW * kKeyBins + t; i < NB * 32; i += RT) (&sh.u.hist[0][0])[i] = 0u;
         const float zstar = Key<T>::value(kstar);
 
-        // ---- E: nucleus statistics in a fixed order: the tokens above bin j1
-        // (per thread) and this warp's listed tokens at or above z*
-        // (lane-strided, slot order); where a list overflowed, a pass over
-        // the slice instead
-        float R = 0.f, Tm = 0.f;
-        if (fits) {
-            R = Ra;
-            Tm = Ta;
-            const int n = sh.cnt[w];
-            for (int i = l; i < n; i += 32) {
-                if (sh.ckey[w][i] >= kstar) {
-                    const float y = (Key<T>::value(sh.ckey[w][i]) - M) * sL;
-                    const float e = ex2(y);
-                    if (sh.cv[w][i] != I) R += e;
-                    Tm = fmaf(e, y, Tm);
-                }
-            }
-        } else {
-            for_slice<T>(slice, nvec, tail, v0, [&](int v, float z) {
+        // ---- the entropy moment over the nucleus, when wanted
+        float Tn = 0.f;
+        if (a.need_ent) {
+            float tc = 0.f;
+            auto add = [&](float z) {
                 if (z >= zstar) {
-                    const float y = (z - M) * sL;
-                    const float e = ex2(y);
-                    if (v != I) R += e;
-                    Tm = fmaf(e, y, Tm);
+                    const float y = fmaf(z, sL, nR);
+                    tc = fmaf(ex2(y), y, tc);
                 }
-            });
-        }
+            };
+            for (int k0 = t; k0 < nu; k0 += RT) {
+                float z[EU];
+                load_unit(k0, z);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            R += __shfl_xor_sync(kFull, R, o);
-            Tm += __shfl_xor_sync(kFull, Tm, o);
+                for (int j = 0; j < EU; ++j) add(z[j]);
+            }
+            if (t < ut) add(Elem<T>::load(p + nu * EU + t));
+            Tn = block_sum<RW>(sh, tc);
         }
-        if (l == 0) {
-            sh.fw[w][0] = R;
-            sh.fw[w][1] = Tm;
-        }
-        __syncthreads();
         if (t == 0) {
-            float Rs = 0.f, Ts = 0.f;
-            for (int i = 0; i < NW; ++i) {
-                Rs += sh.fw[i][0];
-                Ts += sh.fw[i][1];
-            }
-            sh.xbuf[par][0] = pack2(Rs, Ts);
-        }
-        cl.sync();
-        if (rank == 0 && t == 0) {
-            float Rc = 0.f, Tc = 0.f;
-            for (int c = 0; c < C; ++c) {
-                const u64 xv = cl.map_shared_rank(&sh.xbuf[par][0], c)[0];
-                Rc += lo_f(xv);
-                Tc += hi_f(xv);
-            }
+            // from the reference 2^R to the max: weights times 2^dl
+            const float dl = Rf - M * sL;
+            const float f = ex2(dl);
             RowAcc acc;
             acc.M = M;
-            acc.R = Rc;
-            acc.T = Tc;
+            acc.R = Rn * f;
+            acc.T = a.need_ent ? f * fmaf(dl, Rn + mI, Tn) : 0.f;
             acc.I = I;
             a.rec[row] = acc_pack(acc);
             a.zth[row] = zstar;
         }
-        par ^= 1;
+        __syncthreads();
     }
-    // a load whose wait gave up is waited for again (bounded) before the CTA
-    // leaves; and no CTA leaves while a peer may still read its exchange slots
-    if (pending) (void)mbar_wait(&sh.bar, phase ^ 1u);
-    cl.sync();
 }
 
 }  // namespace nuc
 
 namespace {
 
-// The cluster variant when the rows are 16-byte aligned and a cluster of at
-// most 8 CTAs holds one in 64 KB slices; `launched` says whether it ran.
+// The row variant (every row layout, V up to 256 K elements); `launched`
+// says whether it ran.
 template <typename T>
-cudaError_t launch_cluster(const NucleusArgs &a, cudaStream_t stream, int sms, long long nrow, bool &launched) {
+cudaError_t launch_row(const NucleusArgs &a, cudaStream_t stream, int sms, long long nrow, bool &launched) {
     launched = false;
-    constexpr int es = (int)sizeof(T), E = 16 / es;
-    if (!a.t_vec_ok || (a.nd_rows > 0 && !a.d_vec_ok)) return cudaSuccess;
-    // the smallest cluster whose slices fit 32 KB (four CTAs per SM), else
-    // 64 KB (two per SM)
-    int C = 1, S = 0, per_sm = 4;
-    for (int lim : {nuc::kSliceSmall, nuc::kSliceBytes}) {
-        for (C = 1; C <= nuc::kMaxCluster; C *= 2) {
-            S = ((a.V + C - 1) / C + E - 1) / E * E;
-            if (S * es <= lim) break;
-        }
-        if (C <= nuc::kMaxCluster) break;
-        per_sm = 2;
+    // the most tokens one 32-bit counter can receive -- a lane's column of
+    // pass B's bins (that lane of every warp), a warp's key histogram in
+    // pass C -- with the scalar tail on the last warp: significands are
+    // shifted so that no counter overflows, by at most 6 bits (2^-18
+    // relative)
+    const bool al = a.t_vec_ok && (a.nd_rows == 0 || a.d_vec_ok);
+    const int eu = al ? 16 / (int)sizeof(T) : 8;   // elements of a unit
+    const int nu = a.V / eu, tail = a.V % eu;
+    auto units = [&](int t) -> long long { return t < nu ? (nu - 1 - t) / nuc::RT + 1 : 0; };
+    long long tw = 0;
+    for (int i = 0; i < 32; ++i) {
+        long long col = 0;
+        for (int w = 0; w < nuc::RW; ++w) col += units(32 * w + i);
+        tw = std::max(tw, col * eu + (i < tail ? 1 : 0));
     }
-    if (C > nuc::kMaxCluster) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(nuc::nucleus_cluster_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         nuc::kCSharedBytes + nuc::kSliceBytes);
+    for (int w = 0; w < nuc::RW; ++w) {
+        long long gw = 0;
+        for (int i = 0; i < 32; ++i) gw += units(32 * w + i);
+        tw = std::max(tw, gw * eu + (w == nuc::RW - 1 ? tail : 0));
+    }
+    int ushift = 3;
+    while (ushift <= 6 && tw * (long long)((1u << (24 - ushift)) - 1u) > 0xffffffffLL) ++ushift;
+    if (ushift > 6) return cudaSuccess;
+    void (*kern)(const NucleusArgs, int) = al ? nuc::nucleus_row_kernel<T, true> : nuc::nucleus_row_kernel<T, false>;
+    const int smem = (int)sizeof(nuc::RShared);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)C);
-    cfg.blockDim = dim3(nuc::NT);
-    cfg.dynamicSmemBytes = (size_t)(nuc::kCSharedBytes + S * es);
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, nuc::nucleus_cluster_kernel<T>, &cfg) != cudaSuccess || ncl < 1) {
-        (void)cudaGetLastError();   // not schedulable here: the caller takes the other variant
-        return cudaSuccess;
-    }
-    long long want = (long long)per_sm * sms / C;
-    if (want > ncl) want = ncl;
-    if (want > nrow) want = nrow;
-    if (want < 1) want = 1;
-    cfg.gridDim = dim3((unsigned)(want * C));
-    e = cudaLaunchKernelEx(&cfg, nuc::nucleus_cluster_kernel<T>, a, S);
+    long long grid = 2LL * sms;
+    if (grid > nrow) grid = nrow;
+    if (grid < 1) grid = 1;
+    kern<<<(unsigned)grid, nuc::RT, smem, stream>>>(a, ushift);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     launched = true;
     return cudaSuccess;
@@ -1088,8 +1070,8 @@ cudaError_t launch_nucleus(const NucleusArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long nrow = (long long)a.B * (a.nt_rows + a.nd_rows);
     bool launched = false;
-    e = a.bf16 ? launch_cluster<__nv_bfloat16>(a, stream, sms, nrow, launched)
-               : launch_cluster<float>(a, stream, sms, nrow, launched);
+    e = a.bf16 ? launch_row<__nv_bfloat16>(a, stream, sms, nrow, launched)
+               : launch_row<float>(a, stream, sms, nrow, launched);
     if (e != cudaSuccess || launched) return e;
     // rows not 16-byte aligned, or larger than 8 slices: one CTA per row, the
     // row re-read from L2 between passes

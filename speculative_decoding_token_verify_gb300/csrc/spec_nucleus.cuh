@@ -20,6 +20,7 @@ struct NucleusArgs {
     const int32_t *draft_len;  // [B] or null (all K verified)
     const float *inv_temp;     // [B] or null (s = 1)
     float top_p;               // in (0, 1)
+    int need_ent;              // the entropy moment T is wanted (else recorded as 0)
     float4 *rec;               // [B][rows] out: (M, R, T, I) of each row's nucleus
     float *zth;                // [B][rows] out: the nucleus threshold z* (raw logit)
     unsigned *status;          // device status word (atomicMax)

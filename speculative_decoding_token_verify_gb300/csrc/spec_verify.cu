@@ -1550,6 +1550,7 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
         n.draft_len = a.draft_len;
         n.inv_temp = a.inv_temp;
         n.top_p = top_p;
+        n.need_ent = a.need_ent;
         n.rec = a.part;
         n.zth = const_cast<float *>(a.zth);
         n.status = a.ctr + CTR_STATUS;
