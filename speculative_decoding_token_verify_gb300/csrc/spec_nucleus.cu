@@ -41,6 +41,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 
 #include "spec_device.cuh"
 #include "spec_nucleus.cuh"
@@ -477,23 +478,24 @@ __global__ void __launch_bounds__(NT, SV_NUC_CTAS) nucleus_kernel(const NucleusA
 // (at most V 2^-46 of mass, which only enters the total).
 // ---------------------------------------------------------------------------
 constexpr int kSub = 3;                                               // mantissa bits in a bin index
-constexpr int kBinades = 48;
-constexpr int NB = kBinades << kSub;                                  // 384 bins
-constexpr uint32_t kLoBits = (uint32_t)(127 - (kBinades - 1)) << 23; // 2^-47
+constexpr int kBinades = 64;
+constexpr int NB = kBinades << kSub;                                  // 512 bins
+constexpr uint32_t kLoBits = (uint32_t)(127 - (kBinades - 1)) << 23; // 2^-63
 constexpr uint32_t kHiBits = (128u << 23) - 1u;                       // the largest float below 2
 constexpr int kBinBase = (int)(kLoBits >> (23 - kSub));
 constexpr int kKeyBins = 256;
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }   // k in [-126, 127]
 
-// the encoding of a weight, clamped into the binned range (NaN: the top)
-__device__ __forceinline__ uint32_t wbits(float e) { return min(max(__float_as_uint(e), kLoBits), kHiBits); }
-// the same for a weight of a token at or below the max (e < 2 up to rounding):
-// only the lower clamp, in float (a NaN weight goes to bin 0)
-__device__ __forceinline__ uint32_t wbits_low(float e) { return __float_as_uint(fmaxf(e, __uint_as_float(kLoBits))); }
+// the encoding of a weight, clamped into the binned range [2^-63, 2) (a NaN
+// weight goes to bin 0)
+__device__ __forceinline__ uint32_t wbits_f(float e) {
+    return __float_as_uint(fminf(fmaxf(e, __uint_as_float(kLoBits)), __uint_as_float(kHiBits)));
+}
 __device__ __forceinline__ int bin_of(uint32_t b) { return (int)(b >> (23 - kSub)) - kBinBase; }
-// mass of one significand unit in bin g (2^(E - 150 + ushift), E = the bin's exponent)
-__device__ __forceinline__ float bin_scale(int g, int ushift) { return pow2i((g >> kSub) - 70 + ushift); }
+// mass of one significand unit in bin g: 2^(E - 150 + ushift), E = the bin's
+// biased exponent, 128 - kBinades + g / 8
+__device__ __forceinline__ float bin_scale(int g, int ushift) { return pow2i((g >> kSub) - kBinades - 22 + ushift); }
 // log2 of bin g's lower edge; g = NB gives the top edge
 __device__ __forceinline__ float bin_edge(int g) {
     return (float)((g >> kSub) - (kBinades - 1)) + log2f(1.f + (float)(g & ((1 << kSub) - 1)) * (1.f / (1 << kSub)));
@@ -503,15 +505,15 @@ __device__ __forceinline__ float bin_edge(int g) {
 template <typename T>
 __device__ __forceinline__ bool vec_in_range(const uint4 &x, float zl, float zh) {
     if constexpr (sizeof(T) == 2) {
-        const uint32_t lo2 = (__float_as_uint(zl) >> 16) * 0x10001u, hi2 = (__float_as_uint(zh) >> 16) * 0x10001u;
+        // per-half masks: 0xFFFF where the comparison holds
+        const __nv_bfloat162 lo2 = __bfloat162bfloat162(__float2bfloat16_rn(zl));
+        const __nv_bfloat162 hi2 = __bfloat162bfloat162(__float2bfloat16_rn(zh));
         const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
         uint32_t any = 0u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            uint32_t ge, le;
-            asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(ge) : "r"(wv[i]), "r"(lo2));
-            asm("set.le.u32.bf16x2 %0, %1, %2;" : "=r"(le) : "r"(wv[i]), "r"(hi2));
-            any |= ge & le;
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&wv[i]);
+            any |= __hge2_mask(v, lo2) & __hle2_mask(v, hi2);
         }
         return any != 0u;
     } else {
@@ -645,16 +647,25 @@ __device__ __forceinline__ float block_sum(SH &sh, float v) {
 //     when the entropy moment is wanted, one more pass sums e y over the
 //     tokens with z >= z*.
 // ---------------------------------------------------------------------------
-constexpr int RT = 512;
+#ifndef SV_NUC_RT
+#define SV_NUC_RT 512
+#endif
+#ifndef SV_NUC_PREFETCH
+#define SV_NUC_PREFETCH 0
+#endif
+constexpr int RT = SV_NUC_RT;
+constexpr int kRowCtas = RT >= 1024 ? 1 : 2;   // CTAs per SM
 constexpr int RW = RT / 32;
-constexpr int kRQueue = 512;    // groups a warp queues before it processes them
+constexpr int kRQueue = 256;    // units a warp queues before it processes them
+constexpr int kHead = 12;       // binades of headroom of the provisional reference
 
 struct RShared {
     union {
         uint32_t hist[NB][32];              // pass B: bins, a column per lane (no bank conflicts)
         struct {
             uint32_t key[RW][kKeyBins];     // pass C: per-warp key histograms
-            uint32_t queue[RW][kRQueue];    // ... units holding a candidate
+            uint4 qv[RW][kRQueue];          // ... units holding a candidate (aligned rows: their data)
+            uint32_t qk[RW][kRQueue];       // ... and their unit index
         } c;
     } u;
     float wa[RW], wr[RW];
@@ -681,7 +692,7 @@ __device__ __forceinline__ float vec_max(const uint4 &x) {
 // of 8 elements read one by one. Units k = t, t + 512, ... go to thread t;
 // the V mod EU last elements to the last warp.
 template <typename T, bool kAl>
-__global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a, int ushift) {
+__global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const NucleusArgs a, int ushift) {
     extern __shared__ __align__(16) unsigned char rsm[];
     RShared &sh = *reinterpret_cast<RShared *>(rsm);
     const int t = threadIdx.x, l = t & 31, w = t >> 5;
@@ -709,6 +720,25 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
         const T *p = target ? static_cast<const T *>(a.zt) + ((long long)b * (a.K + 1) + r) * a.ts
                             : static_cast<const T *>(a.zd) + ((long long)b * a.K + (r - a.nt_rows)) * a.ds;
         const uint4 *vp = reinterpret_cast<const uint4 *>(p);
+#if SV_NUC_PREFETCH
+        if constexpr (kAl) {
+            // the CTA's next row into L2 while this one is processed
+            const int nx = row + (int)gridDim.x;
+            if (t == 0 && nx < nrow) {
+                const int b2 = nx / rows, r2 = nx - b2 * rows;
+                const T *q = r2 < a.nt_rows
+                                 ? static_cast<const T *>(a.zt) + ((long long)b2 * (a.K + 1) + r2) * a.ts
+                                 : static_cast<const T *>(a.zd) + ((long long)b2 * a.K + (r2 - a.nt_rows)) * a.ds;
+                const long long bytes = (long long)nu * 16;
+                for (long long o = 0; o < bytes; o += 32768) {
+                    const unsigned n = (unsigned)min(32768LL, bytes - o);
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const char *>(q) + o),
+                                 "r"(n)
+                                 : "memory");
+                }
+            }
+        }
+#endif
         auto load_unit = [&](int k, float (&z)[EU]) {
             if constexpr (kAl) Elem<T>::unpack(__ldg(vp + k), z);
             else load8<T>(p, 8 * k, V, false, z);
@@ -720,34 +750,76 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
         }
         const float sL = s * kLog2e;
 
-        // ---- A: the max and its lowest index (the first unit holding the
-        // thread's max is read again for the index)
+        // ---- AB: one read of the row for the max, its lowest index (the first
+        // unit holding a thread's max is read again for it) and the mass bins.
+        // The weights are taken against a provisional reference, kHead
+        // binades above the largest element of the first RT units (one per
+        // thread); the bins reach 63 binades below 1, so the window that
+        // counts (47 binades below the max) fits unless the max lies more
+        // than kHead binades above that sample's -- then pass B takes the
+        // bins again against the max.
+        float Ms = neg_inf();
+        if (t < nu) {
+            float z[EU];
+            load_unit(t, z);
+#pragma unroll
+            for (int j = 0; j < EU; ++j) Ms = fmaxf(Ms, z[j]);
+        }
+        if (t < ut) Ms = fmaxf(Ms, Elem<T>::load(p + nu * EU + t));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(kFull, Ms, o));
+        if (l == 0) sh.wa[w] = Ms;
+        __syncthreads();
+        Ms = sh.wa[0];
+#pragma unroll
+        for (int q = 1; q < RW; ++q) Ms = fmaxf(Ms, sh.wa[q]);
+        __syncthreads();
+        const bool fused = Ms > neg_inf() && Ms < __int_as_float(0x7f800000);
+        float Rf = fused ? ceilf(Ms * sL) + (float)kHead : 0.f;
+        float nR = -Rf;
+        auto bin_add = [&](float z) {
+            const uint32_t bb = wbits_f(ex2(fmaf(z, sL, nR)));
+            atomicAdd(&sh.u.hist[bin_of(bb)][l], unit(bb));
+        };
         float M = neg_inf();
         int I = 0x7fffffff;
         {
             int bk = -1;
             for (int k0 = t; k0 < nu; k0 += UF * RT) {
-                float c[UF];
                 if constexpr (kAl) {
                     uint4 x[UF];
 #pragma unroll
                     for (int u = 0; u < UF; ++u)
                         if (k0 + u * RT < nu) x[u] = __ldg(vp + k0 + u * RT);
 #pragma unroll
-                    for (int u = 0; u < UF; ++u) c[u] = k0 + u * RT < nu ? vec_max<T>(x[u]) : neg_inf();
+                    for (int u = 0; u < UF; ++u)
+                        if (k0 + u * RT < nu) {
+                            const float c = vec_max<T>(x[u]);
+                            if (c > M) {   // strict: the first unit holding the maximum
+                                M = c;
+                                bk = k0 + u * RT;
+                            }
+                            if (fused) {
+                                float z[EU];
+                                Elem<T>::unpack(x[u], z);
+#pragma unroll
+                                for (int j = 0; j < EU; ++j) bin_add(z[j]);
+                            }
+                        }
                 } else {
                     float z[8];
                     load_unit(k0, z);
-                    c[0] = neg_inf();
+                    float c = neg_inf();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) c[0] = fmaxf(c[0], z[j]);
-                }
-#pragma unroll
-                for (int u = 0; u < UF; ++u)
-                    if (c[u] > M) {   // strict: the first unit holding the maximum
-                        M = c[u];
-                        bk = k0 + u * RT;
+                    for (int j = 0; j < 8; ++j) c = fmaxf(c, z[j]);
+                    if (c > M) {
+                        M = c;
+                        bk = k0;
                     }
+                    if (fused)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) bin_add(z[j]);
+                }
             }
             if (bk >= 0) {
                 float z[EU];
@@ -765,6 +837,7 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
                     I = nu * EU + t;
                 }
             }
+            if (fused && w == RW - 1 && l < ut) bin_add(Elem<T>::load(p + nu * EU + l));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -791,42 +864,48 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
         __syncthreads();
         if (!(M > neg_inf()) || M == __int_as_float(0x7f800000)) {
             // no finite logit, or an infinite one: the verification kernel
-            // reports the bad row
+            // reports the bad row (the bins are cleared for the next row)
+            for (int i = t; i < NB * 32; i += RT) (&sh.u.hist[0][0])[i] = 0u;
             if (t == 0) {
                 a.rec[row] = acc_pack(acc_empty());
                 a.zth[row] = __int_as_float(0x7f800000);
             }
+            __syncthreads();
             continue;
         }
-        const float Rf = ceilf(M * sL), nR = -Rf;
-        auto bin_add = [&](float z) {
-            const uint32_t bb = wbits_low(ex2(fmaf(z, sL, nR)));
-            atomicAdd(&sh.u.hist[bin_of(bb)][l], unit(bb));
-        };
 
-        // ---- B: the weights' significands into their bins
-        for (int k0 = t; k0 < nu; k0 += UF * RT) {
-            if constexpr (kAl) {
-                uint4 x[UF];
-#pragma unroll
-                for (int u = 0; u < UF; ++u)
-                    if (k0 + u * RT < nu) x[u] = __ldg(vp + k0 + u * RT);
-#pragma unroll
-                for (int u = 0; u < UF; ++u)
-                    if (k0 + u * RT < nu) {
-                        float z[EU];
-                        Elem<T>::unpack(x[u], z);
-#pragma unroll
-                        for (int j = 0; j < EU; ++j) bin_add(z[j]);
-                    }
-            } else {
-                float z[8];
-                load_unit(k0, z);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) bin_add(z[j]);
+        // ---- B (only when the sample's reference does not hold): the bins
+        // again, against R = ceil(M s log2e)
+        if (!fused || ceilf(M * sL) > Rf) {
+            if (fused) {
+                for (int i = t; i < NB * 32; i += RT) (&sh.u.hist[0][0])[i] = 0u;
+                __syncthreads();
             }
+            Rf = ceilf(M * sL);
+            nR = -Rf;
+            for (int k0 = t; k0 < nu; k0 += UF * RT) {
+                if constexpr (kAl) {
+                    uint4 x[UF];
+#pragma unroll
+                    for (int u = 0; u < UF; ++u)
+                        if (k0 + u * RT < nu) x[u] = __ldg(vp + k0 + u * RT);
+#pragma unroll
+                    for (int u = 0; u < UF; ++u)
+                        if (k0 + u * RT < nu) {
+                            float z[EU];
+                            Elem<T>::unpack(x[u], z);
+#pragma unroll
+                            for (int j = 0; j < EU; ++j) bin_add(z[j]);
+                        }
+                } else {
+                    float z[8];
+                    load_unit(k0, z);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) bin_add(z[j]);
+                }
+            }
+            if (w == RW - 1 && l < ut) bin_add(Elem<T>::load(p + nu * EU + l));
         }
-        if (w == RW - 1 && l < ut) bin_add(Elem<T>::load(p + nu * EU + l));
         __syncthreads();
         // thread t takes position t from the top: bin NB - 1 - t
         const int g = NB - 1 - t;
@@ -842,7 +921,7 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
             m = (float)h * bin_scale(g, ushift);
         }
         const float Z = block_sum<RW>(sh, m);
-        const uint32_t bI = wbits_low(ex2(fmaf(M, sL, nR)));   // I, binned as pass B binned it
+        const uint32_t bI = wbits_f(ex2(fmaf(M, sL, nR)));   // I, binned as pass B binned it
         const int gI = bin_of(bI);
         const float mI = (float)unit(bI) * bin_scale(gI, ushift);
         const float tgt = a.top_p * Z;
@@ -876,32 +955,52 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
             const u64 W = (u64)(khi - klo) + 1ull;
             const bool exact = W <= (u64)kKeyBins;
             const float zl = Key<T>::value(klo), zh = Key<T>::value(khi);
-            auto candidate = [&](int idx, float z) {
-                if (z >= zl && z <= zh && idx != I) {
-                    const uint32_t bb = wbits_low(ex2(fmaf(z, sL, nR)));
-                    if ((bb >> (23 - kSub)) == jsel) {
-                        const uint32_t d = khi - Key<T>::of(z);
-                        const int sub = exact ? (int)d : (int)(((u64)d << 8) / W);
-                        atomicAdd(&sh.u.c.key[w][sub], unit(bb));
+            // a candidate in the logit range: pass B's exact bin test, then
+            // its key (exact rounds) or sub-range (the 64-bit division only in
+            // the rare rounds that need it)
+            auto candidate = [&](auto ex, int idx, float z) {
+                if (idx == I) return;
+                const uint32_t bb = wbits_f(ex2(fmaf(z, sL, nR)));
+                if ((bb >> (23 - kSub)) == jsel) {
+                    const uint32_t d = khi - Key<T>::of(z);
+                    int sub;
+                    if constexpr (decltype(ex)::value) sub = (int)d;
+                    else sub = (int)(((u64)d << 8) / W);
+                    atomicAdd(&sh.u.c.key[w][sub], unit(bb));
+                }
+            };
+            // a queued unit: the mask of its elements in the logit range, then
+            // one candidate per set bit (usually one)
+            auto flush_as = [&](auto ex, int qn) {
+                for (int i = l; i < qn; i += 32) {
+                    const int k = (int)sh.u.c.qk[w][i];
+                    float z[EU];
+                    if constexpr (kAl) Elem<T>::unpack(sh.u.c.qv[w][i], z);
+                    else load_unit(k, z);
+                    unsigned m = 0u;
+#pragma unroll
+                    for (int j = 0; j < EU; ++j) m |= (unsigned)((z[j] >= zl) & (z[j] <= zh)) << j;
+                    while (m) {
+                        const int j = __ffs(m) - 1;
+                        m &= m - 1u;
+                        float zj = z[0];
+#pragma unroll
+                        for (int q = 1; q < EU; ++q) zj = q == j ? z[q] : zj;
+                        candidate(ex, k * EU + j, zj);
                     }
                 }
             };
             auto flush = [&](int qn) {
                 __syncwarp();
-                for (int i = l; i < qn; i += 32) {
-                    const int k = (int)sh.u.c.queue[w][i];
-                    float z[EU];
-                    load_unit(k, z);
-#pragma unroll
-                    for (int j = 0; j < EU; ++j) candidate(k * EU + j, z[j]);
-                }
+                if (exact) flush_as(std::true_type{}, qn);
+                else flush_as(std::false_type{}, qn);
                 __syncwarp();
             };
             int qn = 0;   // warp-uniform
             for (int k0 = t - l; k0 < nu; k0 += UF * RT) {
                 bool hit[UF];
+                uint4 x[UF];
                 if constexpr (kAl) {
-                    uint4 x[UF];
 #pragma unroll
                     for (int u = 0; u < UF; ++u)
                         if (k0 + l + u * RT < nu) x[u] = __ldg(vp + k0 + l + u * RT);
@@ -921,7 +1020,11 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
                 for (int u = 0; u < UF; ++u) {
                     const unsigned mk = __ballot_sync(kFull, hit[u]);
                     if (mk) {
-                        if (hit[u]) sh.u.c.queue[w][qn + __popc(mk & ((1u << l) - 1u))] = (uint32_t)(k0 + l + u * RT);
+                        if (hit[u]) {
+                            const int slot = qn + __popc(mk & ((1u << l) - 1u));
+                            sh.u.c.qk[w][slot] = (uint32_t)(k0 + l + u * RT);
+                            if constexpr (kAl) sh.u.c.qv[w][slot] = x[u];
+                        }
                         qn += __popc(mk);
                     }
                 }
@@ -931,7 +1034,13 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
                 }
             }
             flush(qn);
-            if (w == RW - 1 && l < ut) candidate(nu * EU + l, Elem<T>::load(p + nu * EU + l));
+            if (w == RW - 1 && l < ut) {
+                const float z = Elem<T>::load(p + nu * EU + l);
+                if (z >= zl && z <= zh) {
+                    if (exact) candidate(std::true_type{}, nu * EU + l, z);
+                    else candidate(std::false_type{}, nu * EU + l, z);
+                }
+            }
             // I, left out above, with its key
             float uI = 0.f;
             int sI = -1;
@@ -979,13 +1088,16 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
         for (int i = RW * kKeyBins + t; i < NB * 32; i += RT) (&sh.u.hist[0][0])[i] = 0u;
         const float zstar = Key<T>::value(kstar);
 
-        // ---- the entropy moment over the nucleus, when wanted
+        // ---- the entropy moment over the nucleus, when wanted: exponents
+        // taken against the max itself (the reference R may lie binades above
+        // it, and converting would cancel)
         float Tn = 0.f;
         if (a.need_ent) {
             float tc = 0.f;
+            const float nM = -(M * sL);
             auto add = [&](float z) {
                 if (z >= zstar) {
-                    const float y = fmaf(z, sL, nR);
+                    const float y = fmaf(z, sL, nM);
                     tc = fmaf(ex2(y), y, tc);
                 }
             };
@@ -1005,7 +1117,7 @@ __global__ void __launch_bounds__(RT, 2) nucleus_row_kernel(const NucleusArgs a,
             RowAcc acc;
             acc.M = M;
             acc.R = Rn * f;
-            acc.T = a.need_ent ? f * fmaf(dl, Rn + mI, Tn) : 0.f;
+            acc.T = Tn;
             acc.I = I;
             a.rec[row] = acc_pack(acc);
             a.zth[row] = zstar;
@@ -1050,7 +1162,7 @@ cudaError_t launch_row(const NucleusArgs &a, cudaStream_t stream, int sms, long 
     const int smem = (int)sizeof(nuc::RShared);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    long long grid = 2LL * sms;
+    long long grid = (long long)nuc::kRowCtas * sms;
     if (grid > nrow) grid = nrow;
     if (grid < 1) grid = 1;
     kern<<<(unsigned)grid, nuc::RT, smem, stream>>>(a, ushift);
