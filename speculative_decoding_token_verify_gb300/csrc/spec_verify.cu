@@ -1316,16 +1316,23 @@ struct Plan {
 // stream units aimed at: stochastic mode (a draw chain follows the stream),
 // and the other modes (the stream ends the launch)
 #ifndef SV_TARGET_UNITS_DRAW
-#define SV_TARGET_UNITS_DRAW 4096
+#define SV_TARGET_UNITS_DRAW 3072
 #endif
 #ifndef SV_TARGET_UNITS
 #define SV_TARGET_UNITS 16384
 #endif
-// in stochastic mode the queue's last ~SV_TAIL_BYTES of logits (whole
-// sequences, at most half the batch) stream in tiles of SV_TAIL_TILE_BYTES;
-// 0 turns the tail off
+// in stochastic mode the queue's last 1/SV_TAIL_DIV of the logits, kept
+// within [SV_TAIL_MIN, SV_TAIL_BYTES] (whole sequences, at most half the
+// batch), stream in tiles of SV_TAIL_TILE_BYTES; SV_TAIL_BYTES 0 turns the
+// tail off
 #ifndef SV_TAIL_BYTES
 #define SV_TAIL_BYTES (80ll << 20)
+#endif
+#ifndef SV_TAIL_MIN
+#define SV_TAIL_MIN (32ll << 20)
+#endif
+#ifndef SV_TAIL_DIV
+#define SV_TAIL_DIV 14
 #endif
 #ifndef SV_TAIL_TILE_BYTES
 #define SV_TAIL_TILE_BYTES 32768
@@ -1368,7 +1375,10 @@ static void plan_tiles(int B, int rows, int V, int esize, bool draw, Plan &p) {
     const int ts2 = SV_TAIL_TILE_BYTES / esize;
     if (draw && SV_TAIL_BYTES > 0 && ts2 >= SV_MIN_TILE && ts2 < p.TS) {
         const long long seq_bytes = (long long)rows * V * esize;
-        long long nt = (SV_TAIL_BYTES + seq_bytes - 1) / seq_bytes;
+        long long tail = (long long)B * seq_bytes / SV_TAIL_DIV;
+        if (tail < (long long)SV_TAIL_MIN) tail = SV_TAIL_MIN;
+        if (tail > (long long)SV_TAIL_BYTES) tail = SV_TAIL_BYTES;
+        long long nt = (tail + seq_bytes - 1) / seq_bytes;
         if (nt > B / 2) nt = B / 2;
         if (nt > 0) {
             split_row(V, (V + ts2 - 1) / ts2, p.nT2, p.TS2);
