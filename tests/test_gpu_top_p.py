@@ -114,13 +114,50 @@ def test_ties_at_the_boundary(dt):
 
 @pytest.mark.parametrize("V", [128256, 152064])
 def test_large_fp32_rows(V):
-    """fp32 rows of 501 KB (an 8-CTA cluster holds each) and of 594 KB (too
-    large for one cluster: the L2 re-read variant)."""
+    """fp32 rows of 501 KB and 594 KB: the row kernel's significand shift
+    grows with the tokens a warp bins (5 and 6 bits)."""
     w = _wl(6, 3, V, "f32", 0.5, 2.0)
     inp = workloads.make_inputs(w, 5450 + V % 97, DEV)
     g = _run(inp, "stochastic", 0.9, inp["inv_temp"], est=_est(3))
     r = _oracle(inp, oracle.STOCHASTIC, 0.9, est=np.r_[1.0, np.zeros(3)])
     print(V, _cmp(g, r, "f32", check_feature=True, check_conf=True))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_nucleus_reference_and_boundary_paths(dt):
+    """Rows that take each path of the nucleus selection, next to ordinary
+    rows: a spike far above the first units' maximum (the mass bins are taken
+    again against the row max), a masked head (no maximum in the first units:
+    the bins wait for the row max), and a narrow row centred on 0 (in bf16 the
+    boundary bin then spans far more than 256 keys: a coarse key round
+    first)."""
+    w = _wl(8, 3, 50000, dt)
+    inp = workloads.make_inputs(w, 5800, DEV)
+    zt, zd = inp["zt"], inp["zd"]
+    zt[0, :, 40000] = 45.0
+    zd[0, :, 40001] = 45.0
+    zt[1, :, :20000] = float("-inf")
+    zd[1, :, :20000] = float("-inf")
+    inp["x"][1] = 20000 + inp["x"][1] % 30000
+    zt[2] = (zt[2].float() * 0.05).to(zt.dtype)
+    zd[2] = (zd[2].float() * 0.05).to(zd.dtype)
+    for tp in (0.5, 0.95):
+        g = _run(inp, "stochastic", tp, est=_est(3))
+        r = _oracle(inp, oracle.STOCHASTIC, tp, est=np.r_[1.0, np.zeros(3)])
+        print(tp, _cmp(g, r, dt, check_feature=True, check_conf=True))
+        assert sv.device_status(g["_workspace"]) == 0
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_vocabularies_beyond_the_row_kernel(dt):
+    """V = 300000: a warp bins more tokens than 32-bit counters hold at a
+    2^-18 significand, so the pass takes the 64-bit histogram kernel."""
+    w = _wl(3, 2, 300000, dt, 0.5, 2.0)
+    inp = workloads.make_inputs(w, 5900, DEV)
+    g = _run(inp, "stochastic", 0.9, inp["inv_temp"], est=_est(2))
+    r = _oracle(inp, oracle.STOCHASTIC, 0.9, est=np.r_[1.0, np.zeros(2)])
+    print(_cmp(g, r, dt, check_feature=True, check_conf=True))
+    assert sv.device_status(g["_workspace"]) == 0
 
 
 def test_masked_and_flat_rows():
