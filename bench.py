@@ -636,7 +636,7 @@ def time_temperature(w, seed, out, est, ws, dev, stream, peak, logit_bytes, defa
            "kernel": "verify_kernel<T, 1, 0> (temperature variant)"}
     if top_p is not None:
         res["top_p"] = top_p
-        res["kernel"] = "nucleus_row_kernel<T> + verify_kernel<T, 1, 0> (precomputed rows)"
+        res["kernel"] = "nucleus_row_kernel<T> + verify_kernel<T, 2, 0> (precomputed rows)"
     return res
 
 

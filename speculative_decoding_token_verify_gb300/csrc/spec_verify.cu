@@ -422,21 +422,24 @@ __device__ __forceinline__ RowAcc unit_consume(const UnitGeo<T> &g, int l, float
     return warp_merge(acc_merge(acc_merge(hs, vs, sL), ts, sL), sL);
 }
 
-// one probability of the draw's distributions (see Draw)
-// (the temperature variant: zero outside the row's nucleus)
-template <bool kTemp>
+// one probability of the draw's distributions (see Draw). kTemp: 0 default,
+// 1 per-sequence temperatures, 2 temperatures and top-p (zero outside the
+// row's nucleus)
+template <int kTemp>
 __device__ __forceinline__ float prob_t(const Draw &d, float z) {
-    if constexpr (kTemp) return z >= d.th_t ? ex2(fmaf(z - d.m_t, d.sL, -d.lse_t)) : 0.f;
+    if constexpr (kTemp == 2) return z >= d.th_t ? ex2(fmaf(z - d.m_t, d.sL, -d.lse_t)) : 0.f;
+    else if constexpr (kTemp) return ex2(fmaf(z - d.m_t, d.sL, -d.lse_t));
     else return ex2((z - d.lse_t) * kLog2e);
 }
-template <bool kTemp>
+template <int kTemp>
 __device__ __forceinline__ float prob_d(const Draw &d, float z) {
-    if constexpr (kTemp) return z >= d.th_d ? ex2(fmaf(z - d.m_d, d.sL, -d.lse_d)) : 0.f;
+    if constexpr (kTemp == 2) return z >= d.th_d ? ex2(fmaf(z - d.m_d, d.sL, -d.lse_d)) : 0.f;
+    else if constexpr (kTemp) return ex2(fmaf(z - d.m_d, d.sL, -d.lse_d));
     else return ex2((z - d.lse_d) * kLog2e);
 }
 
 // r_v = max(0, p_v - q_v) (or p_v without a draft row) for v..v+7, fp32.
-template <typename T, bool kTemp>
+template <typename T, int kTemp>
 __device__ __forceinline__ void resid8(const T *trow, const T *drow, int v, int V, bool tv, bool dv,
                                        const Draw &d, float (&r)[8]) {
     float zt[8];
@@ -537,7 +540,7 @@ __device__ __noinline__ void gather_tokens(const Args &a, int b, int l) {
 // residual units. kTemp: the rows are processed at sequence b's inverse
 // temperature s (lse = s M + ln(1+R); the log-ratio is formed from z - M).
 // ---------------------------------------------------------------------------
-template <typename T, bool kTemp>
+template <typename T, int kTemp>
 __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) {
     const int K = a.K;
     if (!SV_OK(a, b >= 0 && b < a.B)) return;
@@ -704,7 +707,7 @@ __device__ __noinline__ void finalize(const Args &a, int b, int l, float4 *buf) 
 
 // Sum of slice s (elements 256s .. 256s+255) of the draw's weights, per lane
 // (8 elements each), in the fixed order every consumer of slice sums uses.
-template <typename T, bool kTemp>
+template <typename T, int kTemp>
 __device__ __forceinline__ float slice_lane_sum(const Args &a, const T *tr, const T *dr, int s, int l,
                                                const Draw &d, float (&r)[8]) {
     resid8<T, kTemp>(tr, dr, s * kSlice + l * 8, a.V, a.t_vec_ok != 0, a.d_vec_ok != 0, d, r);
@@ -777,7 +780,7 @@ __device__ __forceinline__ float warp_incl_scan_f(float v, int l) {
     return v;
 }
 
-template <typename T, bool kTemp>
+template <typename T, int kTemp>
 __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const Draw &d, int l, float4 *buf,
                            bool prestaged = false) {
     const float *ss = a.slices + (size_t)b * a.sstride;
@@ -887,7 +890,7 @@ __device__ int locate_scan(const Args &a, int b, const T *tr, const T *dr, const
 // Lane sums of kResBatch whole slices s0 .. of 16-byte aligned rows: every
 // load of the batch is issued before any arithmetic. Same per-lane order as
 // slice_lane_sum.
-template <typename T, bool kDraft, bool kTemp>
+template <typename T, bool kDraft, int kTemp>
 __device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int l, const Draw &d,
                                            float (&part)[kResBatch]) {
     constexpr int E = Elem<T>::kPerVec;
@@ -928,7 +931,7 @@ __device__ __forceinline__ void batch_fast(const T *tr, const T *dr, int s0, int
 // Lane sums of kResBatch whole slices s0 .. that lane l staged in the warp's
 // buffer (entry 64 i + l: target row, 64 i + 32 + l: draft row; each lane
 // reads only what it copied). Same per-lane order as slice_lane_sum.
-template <bool kDraft, bool kTemp>
+template <bool kDraft, int kTemp>
 __device__ __forceinline__ void batch_staged_bf16(const float4 *buf, int l, const Draw &d,
                                                   float (&part)[kResBatch]) {
 #pragma unroll
@@ -955,7 +958,7 @@ __device__ __forceinline__ void batch_staged_bf16(const float4 *buf, int l, cons
 // holding a whole unit of two batches, the second batch is copied to the
 // warp's staging buffer while the first is loaded to registers, so the
 // unit costs one memory round trip, not two.
-template <typename T, bool kTemp>
+template <typename T, int kTemp>
 __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T *tr, const T *dr, const Draw &d,
                                           int l, float4 *buf) {
     if constexpr (sizeof(T) == 2 && res_slices<T>() == 2 * kResBatch) {
@@ -1012,7 +1015,7 @@ __device__ __forceinline__ void unit_sums(const Args &a, int b, int s0, const T 
     }
 }
 
-template <bool kTemp>
+template <int kTemp>
 __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
     const float4 rec = __ldcg(a.slotrec + (kTemp ? 2 * slot : slot));
     const int bits = __float_as_int(rec.w);
@@ -1044,7 +1047,7 @@ __device__ __forceinline__ Draw decode_slot(const Args &a, int slot, int &b) {
 // The last residual unit of the sequence in `slot` completed: locate its
 // token. If the residual mass vanished (only possible through rounding) the
 // warp redraws from p.
-template <typename T, bool kTemp>
+template <typename T, int kTemp>
 __device__ __noinline__ void locate(const Args &a, int slot, int b_known, int l, float4 *buf) {
     // the sequence is known, so its slice sums are staged while the draw
     // record is read
@@ -1082,7 +1085,7 @@ struct ResDone {
     unsigned old;
 };
 
-template <typename T, bool kTemp>
+template <typename T, int kTemp>
 __device__ __noinline__ ResDone residual_unit(const Args &a, unsigned id, int l, float4 *buf) {
     const int slot = (int)(id / (unsigned)a.nR);
     const int t = (int)(id - (unsigned)slot * (unsigned)a.nR);
@@ -1185,7 +1188,7 @@ __device__ __forceinline__ int wait_job(const Args &a, Sched &q, unsigned &id) {
 // ---------------------------------------------------------------------------
 enum { DUE_NONE = 0, DUE_STREAM = 1, DUE_RESIDUAL = 2 };
 
-template <typename T, bool kTemp, bool kRing = false>
+template <typename T, int kTemp, bool kRing = false>
 __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a) {
     const int l = threadIdx.x & 31;
     __shared__ float4 s_stage[NWARP][kStage];   // per-warp staging for finalize and locate
@@ -1437,7 +1440,7 @@ static std::atomic<unsigned> g_wait_limit{kSpinLimit};
 
 constexpr size_t kDynSmem = 0;
 
-template <typename T, bool kTemp, bool kRing>
+template <typename T, int kTemp, bool kRing>
 static int occupancy() {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<T, kTemp, kRing>, NT, kDynSmem) != cudaSuccess)
@@ -1455,12 +1458,12 @@ static int grid_for(int dtype, int variant, unsigned long long units, int *grid)
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return fail(SPEC_ERR_CUDA, "cannot query the SM count");
-        d.occ[0][0] = occupancy<float, false, false>();
-        d.occ[1][0] = occupancy<__nv_bfloat16, false, false>();
-        d.occ[0][1] = occupancy<float, true, false>();
-        d.occ[1][1] = occupancy<__nv_bfloat16, true, false>();
-        d.occ[0][2] = occupancy<float, false, true>();
-        d.occ[1][2] = occupancy<__nv_bfloat16, false, true>();
+        d.occ[0][0] = occupancy<float, 0, false>();
+        d.occ[1][0] = occupancy<__nv_bfloat16, 0, false>();
+        d.occ[0][1] = occupancy<float, 1, false>();
+        d.occ[1][1] = occupancy<__nv_bfloat16, 1, false>();
+        d.occ[0][2] = occupancy<float, 0, true>();
+        d.occ[1][2] = occupancy<__nv_bfloat16, 0, true>();
         for (int i = 0; i < 2; ++i)
             for (int v = 0; v < 3; ++v)
                 if (d.occ[i][v] < 1)
@@ -1569,18 +1572,20 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
     }
     if (dtype == SPEC_BF16) {
         if (temp)
-            verify_kernel<__nv_bfloat16, true><<<grid, NT, kDynSmem, st>>>(a);
+            a.zth ? verify_kernel<__nv_bfloat16, 2><<<grid, NT, kDynSmem, st>>>(a)
+                  : verify_kernel<__nv_bfloat16, 1><<<grid, NT, kDynSmem, st>>>(a);
         else if (ring)
-            verify_kernel<__nv_bfloat16, false, true><<<grid, NT, kDynSmem, st>>>(a);
+            verify_kernel<__nv_bfloat16, 0, true><<<grid, NT, kDynSmem, st>>>(a);
         else
-            verify_kernel<__nv_bfloat16, false><<<grid, NT, kDynSmem, st>>>(a);
+            verify_kernel<__nv_bfloat16, 0><<<grid, NT, kDynSmem, st>>>(a);
     } else {
         if (temp)
-            verify_kernel<float, true><<<grid, NT, kDynSmem, st>>>(a);
+            a.zth ? verify_kernel<float, 2><<<grid, NT, kDynSmem, st>>>(a)
+                  : verify_kernel<float, 1><<<grid, NT, kDynSmem, st>>>(a);
         else if (ring)
-            verify_kernel<float, false, true><<<grid, NT, kDynSmem, st>>>(a);
+            verify_kernel<float, 0, true><<<grid, NT, kDynSmem, st>>>(a);
         else
-            verify_kernel<float, false><<<grid, NT, kDynSmem, st>>>(a);
+            verify_kernel<float, 0><<<grid, NT, kDynSmem, st>>>(a);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
