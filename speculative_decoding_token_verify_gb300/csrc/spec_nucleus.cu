@@ -781,6 +781,13 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
             const uint32_t bb = wbits_f(ex2(fmaf(z, sL, nR)));
             atomicAdd(&sh.u.hist[bin_of(bb)][l], unit(bb));
         };
+        // two tokens, their exponents by one packed FMA (rounded as the scalar one)
+        auto bin_add2 = [&](float z0, float z1) {
+            const float2 y = pfma(make_float2(z0, z1), make_float2(sL, sL), make_float2(nR, nR));
+            const uint32_t b0 = wbits_f(ex2(y.x)), b1 = wbits_f(ex2(y.y));
+            atomicAdd(&sh.u.hist[bin_of(b0)][l], unit(b0));
+            atomicAdd(&sh.u.hist[bin_of(b1)][l], unit(b1));
+        };
         float M = neg_inf();
         int I = 0x7fffffff;
         {
@@ -803,7 +810,7 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
                                 float z[EU];
                                 Elem<T>::unpack(x[u], z);
 #pragma unroll
-                                for (int j = 0; j < EU; ++j) bin_add(z[j]);
+                                for (int j = 0; j < EU; j += 2) bin_add2(z[j], z[j + 1]);
                             }
                         }
                 } else {
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
                     }
                     if (fused)
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) bin_add(z[j]);
+                        for (int j = 0; j < 8; j += 2) bin_add2(z[j], z[j + 1]);
                 }
             }
             if (bk >= 0) {
@@ -895,13 +902,13 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
                             float z[EU];
                             Elem<T>::unpack(x[u], z);
 #pragma unroll
-                            for (int j = 0; j < EU; ++j) bin_add(z[j]);
+                            for (int j = 0; j < EU; j += 2) bin_add2(z[j], z[j + 1]);
                         }
                 } else {
                     float z[8];
                     load_unit(k0, z);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) bin_add(z[j]);
+                    for (int j = 0; j < 8; j += 2) bin_add2(z[j], z[j + 1]);
                 }
             }
             if (w == RW - 1 && l < ut) bin_add(Elem<T>::load(p + nu * EU + l));
