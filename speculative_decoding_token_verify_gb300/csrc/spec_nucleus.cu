@@ -487,12 +487,14 @@ constexpr int kKeyBins = 256;
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }   // k in [-126, 127]
 
-// the encoding of a weight, clamped into the binned range [2^-63, 2) (a NaN
-// weight goes to bin 0)
-__device__ __forceinline__ uint32_t wbits_f(float e) {
-    return __float_as_uint(fminf(fmaxf(e, __uint_as_float(kLoBits)), __uint_as_float(kHiBits)));
-}
 __device__ __forceinline__ int bin_of(uint32_t b) { return (int)(b >> (23 - kSub)) - kBinBase; }
+// The same bin counted from the top (position 0: just below 2, NB - 1: bin 0),
+// from the unclamped encoding of a weight: one unsigned min sends weights
+// below 2^-63, zero and NaN to the bottom position. A weight of 2 or more
+// (only in a row whose bins are taken again) lands on some position.
+__device__ __forceinline__ uint32_t pos_of(uint32_t b) {
+    return min((kHiBits >> (23 - kSub)) - (b >> (23 - kSub)), (uint32_t)(NB - 1));
+}
 // mass of one significand unit in bin g: 2^(E - 150 + ushift), E = the bin's
 // biased exponent, 128 - kBinades + g / 8
 __device__ __forceinline__ float bin_scale(int g, int ushift) { return pow2i((g >> kSub) - kBinades - 22 + ushift); }
@@ -777,16 +779,17 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
         const bool fused = Ms > neg_inf() && Ms < __int_as_float(0x7f800000);
         float Rf = fused ? ceilf(Ms * sL) + (float)kHead : 0.f;
         float nR = -Rf;
+        // a token's significand into its bin, counted from the top
         auto bin_add = [&](float z) {
-            const uint32_t bb = wbits_f(ex2(fmaf(z, sL, nR)));
-            atomicAdd(&sh.u.hist[bin_of(bb)][l], unit(bb));
+            const uint32_t bb = __float_as_uint(ex2(fmaf(z, sL, nR)));
+            atomicAdd(&sh.u.hist[pos_of(bb)][l], unit(bb));
         };
         // two tokens, their exponents by one packed FMA (rounded as the scalar one)
         auto bin_add2 = [&](float z0, float z1) {
             const float2 y = pfma(make_float2(z0, z1), make_float2(sL, sL), make_float2(nR, nR));
-            const uint32_t b0 = wbits_f(ex2(y.x)), b1 = wbits_f(ex2(y.y));
-            atomicAdd(&sh.u.hist[bin_of(b0)][l], unit(b0));
-            atomicAdd(&sh.u.hist[bin_of(b1)][l], unit(b1));
+            const uint32_t b0 = __float_as_uint(ex2(y.x)), b1 = __float_as_uint(ex2(y.y));
+            atomicAdd(&sh.u.hist[pos_of(b0)][l], unit(b0));
+            atomicAdd(&sh.u.hist[pos_of(b1)][l], unit(b1));
         };
         float M = neg_inf();
         int I = 0x7fffffff;
@@ -922,14 +925,14 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
 #pragma unroll 8
             for (int q = 0; q < 32; ++q) {
                 const int c = (q + l) & 31;
-                h += sh.u.hist[g][c];
-                sh.u.hist[g][c] = 0u;
+                h += sh.u.hist[t][c];
+                sh.u.hist[t][c] = 0u;
             }
             m = (float)h * bin_scale(g, ushift);
         }
         const float Z = block_sum<RW>(sh, m);
-        const uint32_t bI = wbits_f(ex2(fmaf(M, sL, nR)));   // I, binned as pass B binned it
-        const int gI = bin_of(bI);
+        const uint32_t bI = __float_as_uint(ex2(fmaf(M, sL, nR)));   // I, binned as pass B binned it
+        const int gI = NB - 1 - (int)pos_of(bI);
         const float mI = (float)unit(bI) * bin_scale(gI, ushift);
         const float tgt = a.top_p * Z;
         float above_a, above_r, rsel;
@@ -967,7 +970,7 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
             // the rare rounds that need it)
             auto candidate = [&](auto ex, int idx, float z) {
                 if (idx == I) return;
-                const uint32_t bb = wbits_f(ex2(fmaf(z, sL, nR)));
+                const uint32_t bb = __float_as_uint(ex2(fmaf(z, sL, nR)));
                 if ((bb >> (23 - kSub)) == jsel) {
                     const uint32_t d = khi - Key<T>::of(z);
                     int sub;
