@@ -655,6 +655,9 @@ __device__ __forceinline__ float block_sum(SH &sh, float v) {
 #ifndef SV_NUC_PREFETCH
 #define SV_NUC_PREFETCH 0
 #endif
+#ifndef SV_NUC_UF
+#define SV_NUC_UF 4    // 16-byte vectors in flight per thread (aligned rows)
+#endif
 constexpr int RT = SV_NUC_RT;
 constexpr int kRowCtas = RT >= 1024 ? 1 : 2;   // CTAs per SM
 constexpr int RW = RT / 32;
@@ -699,7 +702,7 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
     RShared &sh = *reinterpret_cast<RShared *>(rsm);
     const int t = threadIdx.x, l = t & 31, w = t >> 5;
     constexpr int EU = kAl ? Elem<T>::kPerVec : 8;   // elements of a unit
-    constexpr int UF = kAl ? 4 : 1;                  // units in flight per thread
+    constexpr int UF = kAl ? SV_NUC_UF : 1;          // units in flight per thread
     for (int i = t; i < kRUnionWords; i += RT) (&sh.u.hist[0][0])[i] = 0u;
     __syncthreads();
     const int rows = a.nt_rows + a.nd_rows;
