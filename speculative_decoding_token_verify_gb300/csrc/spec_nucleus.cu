@@ -798,28 +798,38 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
         int I = 0x7fffffff;
         {
             int bk = -1;
-            for (int k0 = t; k0 < nu; k0 += UF * RT) {
-                if constexpr (kAl) {
-                    uint4 x[UF];
+            if constexpr (kAl) {
+                // one vector: its max (strict: the first unit holding the
+                // maximum), and its weights into the bins when fused
+                auto vec_body = [&](auto with_bins, const uint4 &xv, int k) {
+                    const float c = vec_max<T>(xv);
+                    if (c > M) {
+                        M = c;
+                        bk = k;
+                    }
+                    if constexpr (decltype(with_bins)::value) {
+                        float z[EU];
+                        Elem<T>::unpack(xv, z);
 #pragma unroll
-                    for (int u = 0; u < UF; ++u)
-                        if (k0 + u * RT < nu) x[u] = __ldg(vp + k0 + u * RT);
+                        for (int j = 0; j < EU; j += 2) bin_add2(z[j], z[j + 1]);
+                    }
+                };
+                // whole rounds of UF vectors unguarded, then the thread's rest
+                auto run = [&](auto with_bins) {
+                    int k0 = t;
+                    for (; k0 + (UF - 1) * RT < nu; k0 += UF * RT) {
+                        uint4 x[UF];
 #pragma unroll
-                    for (int u = 0; u < UF; ++u)
-                        if (k0 + u * RT < nu) {
-                            const float c = vec_max<T>(x[u]);
-                            if (c > M) {   // strict: the first unit holding the maximum
-                                M = c;
-                                bk = k0 + u * RT;
-                            }
-                            if (fused) {
-                                float z[EU];
-                                Elem<T>::unpack(x[u], z);
+                        for (int u = 0; u < UF; ++u) x[u] = __ldg(vp + k0 + u * RT);
 #pragma unroll
-                                for (int j = 0; j < EU; j += 2) bin_add2(z[j], z[j + 1]);
-                            }
-                        }
-                } else {
+                        for (int u = 0; u < UF; ++u) vec_body(with_bins, x[u], k0 + u * RT);
+                    }
+                    for (; k0 < nu; k0 += RT) vec_body(with_bins, __ldg(vp + k0), k0);
+                };
+                if (fused) run(std::true_type{});
+                else run(std::false_type{});
+            } else {
+                for (int k0 = t; k0 < nu; k0 += RT) {
                     float z[8];
                     load_unit(k0, z);
                     float c = neg_inf();
