@@ -1020,16 +1020,45 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
                 __syncwarp();
             };
             int qn = 0;   // warp-uniform
-            for (int k0 = t - l; k0 < nu; k0 += UF * RT) {
-                bool hit[UF];
-                uint4 x[UF];
-                if constexpr (kAl) {
+            // a unit with a hit goes to the warp's queue (warp-collective)
+            auto enqueue = [&](bool hit, int k, const uint4 &xv) {
+                const unsigned mk = __ballot_sync(kFull, hit);
+                if (mk) {
+                    if (hit) {
+                        const int slot = qn + __popc(mk & ((1u << l) - 1u));
+                        sh.u.c.qk[w][slot] = (uint32_t)k;
+                        if constexpr (kAl) sh.u.c.qv[w][slot] = xv;
+                    }
+                    qn += __popc(mk);
+                }
+            };
+            if constexpr (kAl) {
+                int k0 = t - l;
+                // whole rounds (every lane's UF vectors exist), unguarded
+                for (; k0 + 31 + (UF - 1) * RT < nu; k0 += UF * RT) {
+                    uint4 x[UF];
 #pragma unroll
-                    for (int u = 0; u < UF; ++u)
-                        if (k0 + l + u * RT < nu) x[u] = __ldg(vp + k0 + l + u * RT);
+                    for (int u = 0; u < UF; ++u) x[u] = __ldg(vp + k0 + l + u * RT);
 #pragma unroll
-                    for (int u = 0; u < UF; ++u) hit[u] = k0 + l + u * RT < nu && vec_in_range<T>(x[u], zl, zh);
-                } else {
+                    for (int u = 0; u < UF; ++u) enqueue(vec_in_range<T>(x[u], zl, zh), k0 + l + u * RT, x[u]);
+                    if (qn > kRQueue - UF * 32) {
+                        flush(qn);
+                        qn = 0;
+                    }
+                }
+                // the rest, one vector a lane at a time
+                for (; k0 < nu; k0 += RT) {
+                    const int k = k0 + l;
+                    uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+                    if (k < nu) xv = __ldg(vp + k);
+                    enqueue(k < nu && vec_in_range<T>(xv, zl, zh), k, xv);
+                    if (qn > kRQueue - 32) {
+                        flush(qn);
+                        qn = 0;
+                    }
+                }
+            } else {
+                for (int k0 = t - l; k0 < nu; k0 += RT) {
                     bool any = false;
                     if (k0 + l < nu) {
                         float z[8];
@@ -1037,23 +1066,11 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
 #pragma unroll
                         for (int j = 0; j < 8; ++j) any |= (z[j] >= zl) & (z[j] <= zh);
                     }
-                    hit[0] = any;
-                }
-#pragma unroll
-                for (int u = 0; u < UF; ++u) {
-                    const unsigned mk = __ballot_sync(kFull, hit[u]);
-                    if (mk) {
-                        if (hit[u]) {
-                            const int slot = qn + __popc(mk & ((1u << l) - 1u));
-                            sh.u.c.qk[w][slot] = (uint32_t)(k0 + l + u * RT);
-                            if constexpr (kAl) sh.u.c.qv[w][slot] = x[u];
-                        }
-                        qn += __popc(mk);
+                    enqueue(any, k0 + l, make_uint4(0u, 0u, 0u, 0u));
+                    if (qn > kRQueue - 32) {
+                        flush(qn);
+                        qn = 0;
                     }
-                }
-                if (qn > kRQueue - UF * 32) {
-                    flush(qn);
-                    qn = 0;
                 }
             }
             flush(qn);
