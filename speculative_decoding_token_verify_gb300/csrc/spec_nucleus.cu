@@ -1141,7 +1141,22 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
                     tc = fmaf(ex2(y), y, tc);
                 }
             };
-            for (int k0 = t; k0 < nu; k0 += RT) {
+            int k0 = t;
+            if constexpr (kAl) {
+                for (; k0 + (UF - 1) * RT < nu; k0 += UF * RT) {
+                    uint4 x[UF];
+#pragma unroll
+                    for (int u = 0; u < UF; ++u) x[u] = __ldg(vp + k0 + u * RT);
+#pragma unroll
+                    for (int u = 0; u < UF; ++u) {
+                        float z[EU];
+                        Elem<T>::unpack(x[u], z);
+#pragma unroll
+                        for (int j = 0; j < EU; ++j) add(z[j]);
+                    }
+                }
+            }
+            for (; k0 < nu; k0 += RT) {
                 float z[EU];
                 load_unit(k0, z);
 #pragma unroll
