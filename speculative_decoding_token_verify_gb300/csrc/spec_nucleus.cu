@@ -677,6 +677,7 @@ struct RShared {
     int wi[RW];
     int sel, sel_last;
     float sel_a, sel_r, sel_rs;
+    int next_row[2];                        // the CTA's next row, by iteration parity
 };
 constexpr int kRUnionWords = (int)(sizeof(RShared::u) / 4);
 
@@ -710,7 +711,17 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
     const int V = a.V, nu = V / EU, ut = V - nu * EU;
     const uint32_t umask = (1u << (23 - ushift)) - 1u, uimpl = 1u << (23 - ushift);
     auto unit = [&](uint32_t b) -> uint32_t { return ((b >> ushift) & umask) | uimpl; };
-    for (int row = blockIdx.x; row < nrow; row += gridDim.x) {
+    // the grid's first rows are the CTAs' own; the rest are claimed as CTAs
+    // finish (rows differ in cost), one claim a row, read after a barrier
+    // from a slot of that iteration's parity
+    int it_row = 0;
+    auto next_row = [&]() -> int {
+        const int q = (++it_row) & 1;
+        if (t == 0) sh.next_row[q] = (int)gridDim.x + (int)atomicAdd(a.row_ctr, 1u);
+        __syncthreads();
+        return sh.next_row[q];
+    };
+    for (int row = blockIdx.x; row < nrow; row = next_row()) {
         const int b = row / rows, r = row - b * rows;
         const bool target = r < a.nt_rows;
         const int kb = a.draft_len ? min(max(__ldg(a.draft_len + b), 0), a.K) : a.K;

@@ -24,6 +24,7 @@ struct NucleusArgs {
     float4 *rec;               // [B][rows] out: (M, R, T, I) of each row's nucleus
     float *zth;                // [B][rows] out: the nucleus threshold z* (raw logit)
     unsigned *status;          // device status word (atomicMax)
+    unsigned *row_ctr;         // zeroed counter: rows past the grid's first are claimed from it
 };
 
 // Enqueue the nucleus pass on `stream`. Returns a cudaError_t.

@@ -124,7 +124,7 @@ enum { MODE_STOCHASTIC = 0, MODE_GREEDY = 1, MODE_FLY = 2, MODE_CONF = 3 };
 // workspace header words (zeroed before every launch); the busy counters sit
 // on separate 128-byte lines so that their atomics and polls do not queue on
 // one L2 slice
-enum { CTR_CLAIM = 0, CTR_STATUS = 32, CTR_RES_ALLOC = 64, CTR_RES_CLAIM = 96, kHeaderWords = 128 };
+enum { CTR_CLAIM = 0, CTR_NUC_ROW = 16, CTR_STATUS = 32, CTR_RES_ALLOC = 64, CTR_RES_CLAIM = 96, kHeaderWords = 128 };
 
 // what finalise hands to the residual units of a sequence. At temperature 1
 // the weights are p_v = e^{z_v - lse}. With an inverse temperature s they are
@@ -1567,6 +1567,7 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
         n.rec = a.part;
         n.zth = const_cast<float *>(a.zth);
         n.status = a.ctr + CTR_STATUS;
+        n.row_ctr = a.ctr + CTR_NUC_ROW;
         e = launch_nucleus(n, st);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "nucleus launch failed: %s", cudaGetErrorString(e));
     }
