@@ -715,9 +715,11 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
     // finish (rows differ in cost), one claim a row, read after a barrier
     // from a slot of that iteration's parity
     int it_row = 0;
+    bool ahead = false;   // CTA-uniform: the next row was claimed during this one
     auto next_row = [&]() -> int {
         const int q = (++it_row) & 1;
-        if (t == 0) sh.next_row[q] = (int)gridDim.x + (int)atomicAdd(a.row_ctr, 1u);
+        if (!ahead && t == 0) sh.next_row[q] = (int)gridDim.x + (int)atomicAdd(a.row_ctr, 1u);
+        ahead = false;
         __syncthreads();
         return sh.next_row[q];
     };
@@ -1100,7 +1102,22 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
                 uI = (float)unit(bI);
                 sI = exact ? (int)d : (int)(((u64)d << 8) / W);
             }
+            // the CTA's next row, claimed now: after the barrier each thread
+            // asks L2 for its first unit of it (the next row's first loads)
+            const bool claim = !ahead;
+            if (claim && t == 0) sh.next_row[(it_row + 1) & 1] = (int)gridDim.x + (int)atomicAdd(a.row_ctr, 1u);
+            ahead = true;
             __syncthreads();
+            if constexpr (kAl) {
+                const int nx = sh.next_row[(it_row + 1) & 1];
+                if (claim && nx < nrow && t < nu) {
+                    const int b2 = nx / rows, r2 = nx - b2 * rows;
+                    const T *q = r2 < a.nt_rows
+                                     ? static_cast<const T *>(a.zt) + ((long long)b2 * (a.K + 1) + r2) * a.ts
+                                     : static_cast<const T *>(a.zd) + ((long long)b2 * a.K + (r2 - a.nt_rows)) * a.ds;
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint4 *>(q) + t));
+                }
+            }
             float us = 0.f;
             if (t < kKeyBins) {
                 u64 h = 0;
