@@ -1190,6 +1190,12 @@ enum { DUE_NONE = 0, DUE_STREAM = 1, DUE_RESIDUAL = 2 };
 
 template <typename T, int kTemp, bool kRing = false>
 __global__ void __launch_bounds__(NT, SV_MIN_BLOCKS) verify_kernel(const Args a) {
+    if constexpr (kTemp == 2) {
+        // top-p: the nucleus pass's records are read below, and this launch
+        // may begin as that kernel ends (a programmatic dependent launch):
+        // wait for its completion and its writes
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     const int l = threadIdx.x & 31;
     __shared__ float4 s_stage[NWARP][kStage];   // per-warp staging for finalize and locate
     float4 *const wbuf = s_stage[threadIdx.x >> 5];
@@ -1570,6 +1576,24 @@ static int launch(Args &a, const Plan &p_in, int dtype, void *ws, void *stream, 
         n.row_ctr = a.ctr + CTR_NUC_ROW;
         e = launch_nucleus(n, st);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "nucleus launch failed: %s", cudaGetErrorString(e));
+    }
+    if (a.pre) {
+        // after the nucleus pass, as a programmatic dependent launch: its
+        // blocks are scheduled as that kernel's end (0.5% of a top-p call)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(NT);
+        cfg.dynamicSmemBytes = kDynSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        e = dtype == SPEC_BF16 ? cudaLaunchKernelEx(&cfg, verify_kernel<__nv_bfloat16, 2>, a)
+                               : cudaLaunchKernelEx(&cfg, verify_kernel<float, 2>, a);
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+        return SPEC_OK;
     }
     if (dtype == SPEC_BF16) {
         if (temp)
