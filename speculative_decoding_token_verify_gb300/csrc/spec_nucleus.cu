@@ -661,31 +661,32 @@ __device__ __forceinline__ float block_sum(SH &sh, float v) {
 
 // ---------------------------------------------------------------------------
 // Row variant (nucleus_row_kernel): one CTA of 512 threads per row,
-// persistent over rows, two CTAs per SM. Pass A reads the row from HBM, the
-// later passes re-read it from L2 (two rows per SM in flight: under 80 MB at
-// V = 128256 bf16). The passes of one row:
+// persistent over rows (claimed from a counter as CTAs finish), two CTAs per
+// SM. One pass reads the row from HBM; the later passes re-read it from L2
+// (two rows per SM in flight: under 80 MB at V = 128256 bf16). The passes of
+// one row:
 //
-//  A. the max M and its lowest index I; R = ceil(M s log2e);
-//  B. the weights' significands into the mass bins above, a column of
-//     counters per lane; the first bin j1, from the top, whose running mass
-//     reaches top_p of the total;
+//  AB. one read: the max M and its lowest index I, and the weights'
+//     significands into the mass bins above (a column of counters per lane)
+//     against a provisional reference R, kHead binades above the largest
+//     element of the row's first 512 units. When M lies above what R covers
+//     (rare), the bins are taken again from L2 against R = ceil(M s log2e).
+//     The first bin j1, from the top, whose running mass reaches top_p of
+//     the total holds z*;
 //  C. the tokens of bin j1 -- a prefilter on the logit range the bin can hold
-//     (packed bf16x2 compares; units with a hit queued per warp), then pass
-//     B's exact bin test -- add their significands to a histogram over their
-//     keys: one bin per key while the range holds at most 256 keys, else 256
-//     sub-ranges, of which the selected one narrows the range for another
-//     round (bf16: at most two rounds; fp32: at most five). The first key
-//     whose running mass, on top of the bins above j1, reaches the target is
-//     z*;
+//     (bf16: the sign of (v - c)^2 - rr in packed FMAs; fp32: compares;
+//     units with a hit queued per warp), then pass AB's exact bin test --
+//     add their significands to a histogram over their keys: one bin per key
+//     while the range holds at most 256 keys, else 256 sub-ranges, of which
+//     the selected one narrows the range for another round (bf16: at most
+//     two rounds; fp32: at most five). The first key whose running mass, on
+//     top of the bins above j1, reaches the target is z*;
 //  -- R, the nucleus mass other than I's, comes from the same integer sums;
 //     when the entropy moment is wanted, one more pass sums e y over the
 //     tokens with z >= z*.
 // ---------------------------------------------------------------------------
 #ifndef SV_NUC_RT
 #define SV_NUC_RT 512
-#endif
-#ifndef SV_NUC_PREFETCH
-#define SV_NUC_PREFETCH 0
 #endif
 #ifndef SV_NUC_UF
 #define SV_NUC_UF 2    // 16-byte vectors in flight per thread (aligned rows): 2 beats 4 by 3.5%, 1 is 13% slower
@@ -771,25 +772,6 @@ __global__ void __launch_bounds__(RT, kRowCtas) nucleus_row_kernel(const Nucleus
         const T *p = target ? static_cast<const T *>(a.zt) + ((long long)b * (a.K + 1) + r) * a.ts
                             : static_cast<const T *>(a.zd) + ((long long)b * a.K + (r - a.nt_rows)) * a.ds;
         const uint4 *vp = reinterpret_cast<const uint4 *>(p);
-#if SV_NUC_PREFETCH
-        if constexpr (kAl) {
-            // the CTA's next row into L2 while this one is processed
-            const int nx = row + (int)gridDim.x;
-            if (t == 0 && nx < nrow) {
-                const int b2 = nx / rows, r2 = nx - b2 * rows;
-                const T *q = r2 < a.nt_rows
-                                 ? static_cast<const T *>(a.zt) + ((long long)b2 * (a.K + 1) + r2) * a.ts
-                                 : static_cast<const T *>(a.zd) + ((long long)b2 * a.K + (r2 - a.nt_rows)) * a.ds;
-                const long long bytes = (long long)nu * 16;
-                for (long long o = 0; o < bytes; o += 32768) {
-                    const unsigned n = (unsigned)min(32768LL, bytes - o);
-                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const char *>(q) + o),
-                                 "r"(n)
-                                 : "memory");
-                }
-            }
-        }
-#endif
         auto load_unit = [&](int k, float (&z)[EU]) {
             if constexpr (kAl) Elem<T>::unpack(__ldg(vp + k), z);
             else load8<T>(p, 8 * k, V, false, z);
